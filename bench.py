@@ -1,0 +1,307 @@
+"""Benchmark: MoE decode tokens/s of the page-scale quantized expert-FFN layer.
+
+Workload (one "step"): 1,000 decode tokens, batch 1, through the MoE layer of
+Qwen3.8-Flash-Next shape (H 2048, 512 routed experts top-10 + 1 shared,
+I 512, 4-bit block-32 weights, Zipf(1.1) router bias), cycling round-robin
+over 8 byte-identical layer replicas (8 x 0.91 GB of expert weights > L2),
+all experts resident.  Each token is one moe_forward call (three chained
+kernels); the 1,000 calls are replayed as one CUDA graph.
+
+  value  tokens/s with inputs resident in HBM (CUDA events on the stream)
+  e2e    the same through the public API with the step's activations copied
+         host -> device and the outputs device -> host inside the timed region
+  roofline  algorithmic bytes of one decode step (router fp32 + 11 experts)
+         per token / time per token, against the measured HBM copy bandwidth
+  cpu_baseline  the CPU oracle (single-threaded binary64) on a bounded sample
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU
+(replicas; the layer does not shard across GPUs here) and rank 0 prints the
+aggregate.  --impl reference times the CPU oracle instead (rank 0 only).
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE decode tokens/s per layer stack; expert-weight HBM GB/s vs 8 TB/s peak"
+UNIT = "tokens/s"
+TOKENS_PER_STEP = 1000
+REPLICAS = 8
+H, E, K, I = 2048, 512, 10, 512
+EXPERT_BYTES = 1_769_472
+ROUTER_BYTES = E * H * 4
+STEP_BYTES_PER_TOKEN = ROUTER_BYTES + (K + 1) * EXPERT_BYTES  # 23,658,496
+WORKLOAD = ("page-scale MoE layer decode, batch 1: H 2048, 512 routed experts top-10 + 1 shared, I 512, "
+            "4-bit block-32 fp16-scale weights, Zipf(1.1) router bias; 1000 tokens per step over 8 identical "
+            "layer replicas round-robin, all experts resident")
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_expert_ffn_gemv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """dram bytes per token from the committed ncu summary, if it was taken on this source."""
+    p = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    try:
+        d = json.load(open(p))
+        if d.get("source_hash") == source_hash():
+            return d["dram_bytes_per_token"]
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    def __init__(self, path):
+        self.path = path
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
+                 "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self, gpu_index):
+        try:
+            rows = [r.split(", ") for r in open(self.path).read().strip().splitlines()]
+        except Exception:
+            return None
+        rows = [r for r in rows if len(r) >= 9 and r[0].strip() == str(gpu_index)]
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows]
+        reasons = set()
+        for r in rows:
+            for name, col in (("hw_slowdown", 5), ("hw_thermal_slowdown", 6), ("sw_thermal_slowdown", 7),
+                              ("sw_power_cap", 8)):
+                if r[col].strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]), "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def cpu_baseline(L, tokens):
+    """Time the oracle, as written, on `tokens` decode tokens (one core)."""
+    import oracle
+    x = L_tokens(L, 0, tokens)
+    t0 = time.perf_counter()
+    for t in range(tokens):
+        oracle.moe_forward(H, I, E, K, L.W_r, L.bias, L.experts, L.shared, x[t:t + 1])
+    dt = time.perf_counter() - t0
+    return {"value": tokens / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{tokens} decode tokens (batch 1) of the page-scale layer, single-threaded binary64 C oracle"}
+
+
+def L_tokens(L, t0, n):
+    from quantized_expert_ffn_gemv_gb300 import synth
+    return synth.activations(L.shape, L.index, t0, n, stream=7)
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    from quantized_expert_ffn_gemv_gb300 import synth
+    import oracle
+    L = synth.make_layer(synth.PAGE, layer=0)
+    per_step = 4
+    x = L_tokens(L, 0, per_step * (args.steps + args.warmup))
+    times = []
+    for s in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        for t in range(per_step):
+            i = s * per_step + t
+            oracle.moe_forward(H, I, E, K, L.W_r, L.bias, L.experts, L.shared, x[i:i + 1])
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    tot = sum(times)
+    value = per_step * args.steps / tot
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": WORKLOAD, "sample_tokens_per_step": per_step},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": f"{per_step} decode tokens per step, single-threaded binary64 C oracle"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample", type=int, default=32, help="oracle tokens timed for cpu_baseline")
+    ap.add_argument("--tokens", type=int, default=TOKENS_PER_STEP)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from quantized_expert_ffn_gemv_gb300 import moe, synth
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+
+    L = synth.make_layer(synth.PAGE, layer=0)
+    layers = [moe.MoeLayer(L.shape, L.W_r, L.bias, L.experts, L.shared, max_tokens=1, device=local)
+              for _ in range(REPLICAS)]
+    ntok = args.tokens
+    x_host = L_tokens(L, 0, ntok)
+    x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_pin = torch.empty_like(x_pin).pin_memory()
+    xd = x_pin.to("cuda")
+    yd = torch.empty_like(xd)
+    stream = torch.cuda.Stream()
+
+    def step():
+        for t in range(ntok):
+            layers[t % REPLICAS].forward(xd[t:t + 1], yd[t:t + 1])
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timing
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    barrier()
+    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"bench_clocks_{rank}.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/bench_clocks_{rank}.csv")
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with clocks:
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            ev1.record(stream)
+        barrier()
+    ms = ev0.elapsed_time(ev1)
+    # ---- end to end through the public API: H2D x, the forwards, D2H y
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            xd.copy_(x_pin, non_blocking=True)
+            graph.replay()
+            y_pin.copy_(yd, non_blocking=True)
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            xd.copy_(x_pin, non_blocking=True)
+            graph.replay()
+            y_pin.copy_(yd, non_blocking=True)
+        e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    for l in layers:
+        s, code = l.stats()
+        if code != 0:
+            raise RuntimeError(f"layer error {code}")
+    if pg:
+        t = torch.tensor([ms, ms_e2e], device="cuda")
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms, ms_e2e = t.tolist()
+    if rank != 0:
+        pg.destroy_process_group() if pg else None
+        return
+    tokens = ntok * args.steps * ws
+    value = tokens / (ms * 1e-3)
+    per_token_s = (ms * 1e-3) / (ntok * args.steps)
+    peak, peak_kind = measured_peak()
+    achieved = STEP_BYTES_PER_TOKEN / per_token_s / 1e9
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16xf16+f32 (4-bit weights)", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "tokens_per_step": ntok, "replicas": REPLICAS,
+                   "l2": "inputs larger than L2 (8 layer replicas, 7.25 GB of expert weights, round-robin)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": {"bound": "hbm", "kernel": "moe_forward (route + gateup + down, PDL-chained)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "bytes_per_unit": STEP_BYTES_PER_TOKEN, "unit_of_work": "token",
+                     "traffic": recorded_traffic()},
+        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(x_pin.numel() * 2),
+                "d2h_bytes_per_step": int(y_pin.numel() * 2)},
+        "gpu_launches": 3 * ntok * args.steps,
+        "clocks": clocks.summary(local),
+    }
+    if ws == 1 and args.cpu_sample > 0:
+        line["cpu_baseline"] = cpu_baseline(L, args.cpu_sample)
+    print(json.dumps(line), flush=True)
+    for l in layers:
+        l.close()
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+/*
+ * moe.h - C ABI of the GB300 (sm_103a) quantized mixture-of-experts FFN layer.
+ *
+ * One call of moe_forward runs the MoE FFN layer of Qwen3.8-Flash-Next-style
+ * decode on one GPU: router GEMV, softmax and top-k selection, an in-stream
+ * check of whether each selected expert is resident in a VRAM expert-slot
+ * pool (misses copied from pinned host RAM behind a host doorbell, never
+ * dropped), 4-bit block-quantized gate/up/down expert GEMVs with SiLU gating,
+ * and the routing-weighted combine.
+ *
+ * Sources for what the layer is and how residency works:
+ *  - Betelgeuse news page ("Betelgeuse: RTX 3060 12GB + 16GB 内存跑 Qwen 3.8
+ *    Flash Next, 22 tok/s 不丢专家"), section 机制 (48 layers, 512 routed experts
+ *    per layer, 10 routed + 1 shared per token; table rows 显存: VRAM expert
+ *    slots, 调度: an in-stream kernel decides hits on the GPU and rings a host
+ *    doorbell only on a miss, 内存/盘: misses are served from host RAM) and
+ *    section "bit-exact 的确切含义" (top-10 routing never changed; an expert
+ *    read/DMA failure is reported as an error instead of continuing with
+ *    zero weights).
+ *  - Basalt README, section "Memory floors": refuse a memory setting that
+ *    does not fit instead of shrinking it.
+ *  - halogen-flash-server README, section "Bring your own GGUF": the packed
+ *    block-quantized values are repacked losslessly into the kernels' layout.
+ *
+ * Conventions shared by every call:
+ *  - Every call returns a moe_status_t; nothing throws or exits.
+ *  - "device" pointers are CUDA device addresses on the layer's device;
+ *    "host" pointers are ordinary process memory.
+ *  - bf16 tensors are raw IEEE bfloat16 bit patterns, row-major.
+ *  - A layer object is not re-entrant: issue its calls from one host thread
+ *    and on one stream at a time.
+ *  - Asynchronous failures (a slot copy that failed or timed out) are
+ *    sticky: the next moe_forward returns MOE_ERR_STATE and moe_get_stats
+ *    reports the original code; the affected y is undefined, never silently
+ *    zero.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* a pointer, size or shape is invalid */
+  MOE_ERR_UNSUPPORTED = 2,   /* valid but outside what this build implements */
+  MOE_ERR_OUT_OF_MEMORY = 3, /* an allocation or a caller arena is too small */
+  MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+  MOE_ERR_COPY = 5,          /* a host->slot expert copy failed */
+  MOE_ERR_TIMEOUT = 6,       /* the device gave up waiting for a slot copy */
+  MOE_ERR_STATE = 7,         /* the layer holds a sticky error from an earlier call */
+  MOE_ERR_DEVICE = 8         /* a device-side check failed (e.g. activation outside fp16 range) */
+} moe_status_t;
+
+typedef struct moe_layer moe_layer_t; /* opaque, library-owned */
+
+/*
+ * Layer description.  Shapes: H = hidden, E = routed experts, k = routed
+ * experts per token, I = expert intermediate size.  Weight format: each
+ * expert is one canonical blob [W_gate I x H][W_up I x H][W_down H x I];
+ * each R x K matrix is a nibble plane (R*K/2 bytes; element i of a row in
+ * byte i/2, low nibble for even i; stored value u = q + 8, q in [-8, 7])
+ * followed by a scale plane (R*K/32 binary16 scales, one per block of 32
+ * consecutive elements along K).  Weight = scale * (u - 8).
+ */
+typedef struct {
+  int32_t hidden;          /* H: multiple of 64, 64..4096 */
+  int32_t n_experts;       /* E: 1..4096 */
+  int32_t top_k;           /* k: 1..min(E, 16) */
+  int32_t n_shared;        /* 0 or 1 shared expert (weight 1, outside the softmax) */
+  int32_t inter;           /* I: multiple of 64, 64..4096 */
+  int32_t qblock;          /* quantization block; must be 32 */
+  int32_t max_tokens;      /* largest T a moe_forward call may pass: 1..64 */
+  int32_t device;          /* CUDA device ordinal */
+  const float* router_w;   /* device, fp32 [E][H] row-major; caller-owned, must outlive the layer */
+  const float* router_bias;/* device, fp32 [E] (per-expert logit bias), or NULL for none; caller-owned */
+  const uint8_t* experts;  /* host, E canonical blobs back to back; read during create only */
+  const uint8_t* shared;   /* host, one canonical blob, or NULL when n_shared == 0; read during create only */
+} moe_layer_desc_t;
+
+/* Bytes of one expert blob (canonical and repacked sizes are equal). */
+MOE_API size_t moe_expert_bytes(int32_t hidden, int32_t inter);
+
+/*
+ * The lossless repack between the canonical blob and the GPU layout the
+ * kernels stream (halogen-flash-server README, section "Bring your own GGUF":
+ * the file's quantized values are moved into the kernels' layout, not
+ * requantized).  Host-only; needs no GPU.  Both buffers hold
+ * moe_expert_bytes(hidden, inter) bytes; hidden and inter multiples of 64.
+ * The GPU layout groups 16 output rows into strips and orders each strip's
+ * nibbles and block scales so that every lane of a warp reads its
+ * mma.m16n8k16 A-fragment nibbles with one 16-byte load and its two block
+ * scales with one 8-byte load; moe_unpack_expert inverts it exactly.
+ * Errors: INVALID_ARG.
+ */
+MOE_API moe_status_t moe_repack_expert(const uint8_t* canonical, int32_t hidden, int32_t inter, uint8_t* gpu_layout);
+MOE_API moe_status_t moe_unpack_expert(const uint8_t* gpu_layout, int32_t hidden, int32_t inter, uint8_t* canonical);
+
+/*
+ * Create a layer.  Validates the description, repacks every expert blob
+ * losslessly into the GPU layout held in a library-owned pinned host master
+ * copy (the source of slot copies), uploads the shared expert, and
+ * allocates the layer's device scratch.  The layer has no expert slots
+ * until moe_slot_pool_configure.
+ * Errors: INVALID_ARG (NULL/out-of-range fields), UNSUPPORTED (qblock != 32
+ * or shapes this build does not implement), OUT_OF_MEMORY, CUDA.
+ * On error *out is NULL and nothing stays allocated.
+ */
+MOE_API moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out);
+
+/*
+ * Give the layer its VRAM expert-slot pool: n_slots slots of
+ * moe_expert_bytes() each, carved from the caller's device arena
+ * (e.g. a torch.empty buffer; caller-owned, must outlive the layer or the
+ * next configure call, 256-byte aligned).
+ *  - n_slots == E: every expert resident.  All blobs are copied into the
+ *    arena now (synchronously); no host traffic during moe_forward.
+ *  - min(E, max_tokens*k) <= n_slots < E: the pool starts empty; a host
+ *    copy-server thread serves misses.  Eviction is LRU over forward calls:
+ *    the misses of a call are filled in ascending expert index, taking
+ *    empty slots first (ascending), then slots whose expert the call does
+ *    not use, least recently used first (ties to the lower slot).
+ * Errors: INVALID_ARG (NULL arena, n_slots out of range), OUT_OF_MEMORY
+ * when n_slots * moe_expert_bytes() > arena_bytes (the request is never
+ * shrunk), CUDA.
+ */
+MOE_API moe_status_t moe_slot_pool_configure(moe_layer_t* layer, int32_t n_slots, void* arena_dev, size_t arena_bytes);
+
+/*
+ * y = MoE(x) for T tokens, enqueued on `cuda_stream` (a cudaStream_t; NULL =
+ * the legacy default stream).  Stream-ordered and asynchronous; safe to
+ * capture in a CUDA graph once the pool is configured.
+ *   x_bf16_dev:  device bf16 [T][H], 16-byte aligned (|x| < 65504; larger is MOE_ERR_DEVICE)
+ *   y_bf16_dev:  device bf16 [T][H], written (must not alias x)
+ *   topk_idx_dev: device int32 [T][k] or NULL: the selected experts of each
+ *                token in ascending expert index
+ *   topk_w_dev:  device fp32 [T][k] or NULL: their routing weights (softmax
+ *                over all E renormalised over the selected k)
+ * Selection: the k largest logits (router_w x + router_bias), ties to the
+ * lower index.  Output: y = sum over the selected experts, in ascending
+ * index, of w_j * FFN_j(x), plus FFN_shared(x), accumulated in fp32 and
+ * rounded once to bf16 (round to nearest even).
+ * Errors (synchronous): INVALID_ARG (T out of 1..max_tokens, NULL x/y),
+ * STATE (no pool configured, or a sticky error), CUDA (launch failure).
+ */
+MOE_API moe_status_t moe_forward(moe_layer_t* layer, const void* x_bf16_dev, int32_t T, void* y_bf16_dev,
+                                 int32_t* topk_idx_dev, float* topk_w_dev, void* cuda_stream);
+
+/*
+ * Residual + RMSNorm between the layers of a stack, enqueued on the stream:
+ *   x_out   = bf16(x + y)                 (y may be NULL: x_out = x)
+ *   xhat    = bf16(x_out / sqrt(mean(x_out^2) + eps))   (no learned weight)
+ * All device bf16 [T][H]; x_out may alias x; xhat must not alias the others.
+ */
+MOE_API moe_status_t moe_residual_rmsnorm(const void* x_bf16_dev, const void* y_bf16_dev, int32_t T, int32_t hidden,
+                                          float eps, void* x_out_bf16_dev, void* xhat_bf16_dev, void* cuda_stream);
+
+typedef struct {
+  uint64_t forwards;     /* moe_forward steps the device has completed routing for */
+  uint64_t hits;         /* distinct selected experts found resident, summed over steps */
+  uint64_t misses;       /* distinct selected experts copied in from host RAM */
+  uint64_t h2d_bytes;    /* bytes copied host -> slots */
+  uint64_t wait_ns;      /* device time spent waiting for slot copies */
+  int32_t n_slots;       /* configured pool size (0 = none) */
+  int32_t error;         /* sticky error code (moe_status_t), MOE_OK if none */
+} moe_stats_t;
+
+/* Synchronize the layer's device and copy stream, then report counters.
+ * Returns the sticky error code if one is set (stats still filled). */
+MOE_API moe_status_t moe_get_stats(moe_layer_t* layer, moe_stats_t* out);
+
+/*
+ * Copy the miss log (one (step, expert, slot) int32 triple per copy the
+ * copy server issued, step counted from 1 per layer) into out[0 .. 3*max).
+ * *n receives the total number logged.  Synchronizes like moe_get_stats.
+ */
+MOE_API moe_status_t moe_get_miss_log(moe_layer_t* layer, int32_t* out, int64_t max, int64_t* n);
+
+/* Device-side wait limit for a slot copy (default 2 s); 0 restores the default. */
+MOE_API moe_status_t moe_set_wait_timeout_ns(moe_layer_t* layer, uint64_t ns);
+
+/*
+ * Host-side fault injection for tests (no GPU fault is ever raised):
+ *   fail_copy_n > 0: the n-th copy (counted from 1 after this call) is not
+ *                    issued; it is reported to the device as failed, which
+ *                    makes the step end with MOE_ERR_COPY.
+ *   pause:           nonzero stops the copy server from serving the ring
+ *                    (the device wait then times out), zero resumes it.
+ */
+MOE_API moe_status_t moe_debug_copy_faults(moe_layer_t* layer, int64_t fail_copy_n, int32_t pause);
+
+/* Destroy: synchronizes, stops the copy server, frees library memory. NULL-safe. */
+MOE_API void moe_destroy(moe_layer_t* layer);
+
+MOE_API const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

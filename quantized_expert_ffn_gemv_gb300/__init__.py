@@ -12,6 +12,6 @@ __all__ = ["synth", "moe"]
 
 def __getattr__(name):
     if name == "moe":
-        from . import moe
-        return moe
+        import importlib
+        return importlib.import_module(__name__ + ".moe")
     raise AttributeError(name)

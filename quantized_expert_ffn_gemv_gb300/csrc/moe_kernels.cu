@@ -1,0 +1,834 @@
+// Decode-path kernels of the quantized MoE FFN layer (sm_103a).
+//
+// One moe_forward = three stream-ordered kernels chained with programmatic
+// dependent launch (griddepcontrol), so each grid is already resident when
+// its predecessor finishes:
+//   route_kernel   router GEMV (fp32, warp pair per expert row), then in the
+//                  last-arriving CTA: top-k per token, softmax weights,
+//                  grouping of (token, expert) pairs by expert, the slot hit
+//                  check with LRU victim choice, and the host doorbell.
+//   gateup_kernel  per (expert, 16-row strip): 4-bit gate and up rows
+//                  dequantized in registers into mma.m16n8k16 fragments,
+//                  fp32 accumulation with exact per-block scaling, then
+//                  h = silu(g) * u stored as fp16.
+//   down_kernel    per 16-row output strip: every selected expert's down rows,
+//                  then the routing-weighted combine in ascending expert
+//                  order (shared expert last) and one bf16 rounding.
+// Betelgeuse news page, section 机制: 调度 row (the hit check runs in-stream
+// on the GPU; the host is only involved on a miss) and 显存 row (VRAM slots).
+#include <cfloat>
+#include <climits>
+
+#include "moe.h"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint4 ld_cg4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint2 ld_cg2(const void* p) {
+  uint2 r;
+  asm volatile("ld.global.cg.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ int ld_cg_i32(const int* p) {
+  int r;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+  float r;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// 8 packed nibbles (GPU layout word) -> the 4 f16x2 registers of an A fragment,
+// holding q = u - 8 exactly.  A low nibble of a half becomes 1024 + u through
+// the 0x6400 exponent (minus 1032 -> q); a high nibble becomes 1024 + 16u
+// (times 1/16 minus 72 -> q).
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t lo0 = (w & 0x000F000Fu) | 0x64006400u;
+  const uint32_t hi0 = (w & 0x00F000F0u) | 0x64006400u;
+  const uint32_t w8 = w >> 8;
+  const uint32_t lo1 = (w8 & 0x000F000Fu) | 0x64006400u;
+  const uint32_t hi1 = (w8 & 0x00F000F0u) | 0x64006400u;
+  const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+  const __half2 km72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));
+  __half2 r0 = __hsub2(*reinterpret_cast<const __half2*>(&lo0), k1032);
+  __half2 r1 = __hsub2(*reinterpret_cast<const __half2*>(&lo1), k1032);
+  __half2 r2 = __hfma2(*reinterpret_cast<const __half2*>(&hi0), k16th, km72);
+  __half2 r3 = __hfma2(*reinterpret_cast<const __half2*>(&hi1), k16th, km72);
+  a[0] = *reinterpret_cast<uint32_t*>(&r0);  // row g,   k 2t..2t+1
+  a[1] = *reinterpret_cast<uint32_t*>(&r1);  // row g+8, k 2t..2t+1
+  a[2] = *reinterpret_cast<uint32_t*>(&r2);  // row g,   k 2t+8..2t+9
+  a[3] = *reinterpret_cast<uint32_t*>(&r3);  // row g+8, k 2t+8..2t+9
+}
+
+__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFF))); }
+__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
+
+// One 16 x 64 super-tile against one n8 group of activations: 2 scale blocks,
+// each the exact fp32 scaling of a 32-long integer-weight dot product.
+__device__ __forceinline__ void supertile_mma(float (&acc)[4], const uint4& nib, const uint2& sc, const uint4& b01,
+                                              const uint4& b23) {
+  const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
+  const uint32_t bb[4][2] = {{b01.x, b01.y}, {b01.z, b01.w}, {b23.x, b23.y}, {b23.z, b23.w}};
+  const float d[4] = {half_lo(sc.x), half_hi(sc.x), half_lo(sc.y), half_hi(sc.y)};
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) {
+    float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t a[4];
+    dequant_word(words[2 * blk], a);
+    mma16816(tmp, a, bb[2 * blk][0], bb[2 * blk][1]);
+    dequant_word(words[2 * blk + 1], a);
+    mma16816(tmp, a, bb[2 * blk + 1][0], bb[2 * blk + 1][1]);
+    const float dg = d[2 * blk], dg8 = d[2 * blk + 1];
+    acc[0] = fmaf(dg, tmp[0], acc[0]);
+    acc[1] = fmaf(dg, tmp[1], acc[1]);
+    acc[2] = fmaf(dg8, tmp[2], acc[2]);
+    acc[3] = fmaf(dg8, tmp[3], acc[3]);
+  }
+}
+
+__device__ void set_error(const LayerArgs& a, int code) {
+  atomicCAS(&a.st->error, 0, code);
+  volatile int32_t* m = &a.hm->error;
+  if (*m == 0) *m = code;
+  __threadfence_system();
+}
+
+__device__ __forceinline__ int dev_error(const LayerArgs& a) { return ld_cg_i32(&a.st->error); }
+
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------------------------ route
+
+constexpr int kRouteRows = 4;        // expert rows per CTA (two warps per row)
+constexpr int kRouteThreads = 256;
+constexpr int kRouteChunk = 8;       // tokens staged in shared memory at a time
+constexpr int kRouteVec = kMaxHidden / 256;  // float4 per lane per half row
+
+struct FinishSmem {
+  size_t lrow, tokmask, uidx, poff, sidx, sw, taken, misc, total;
+};
+
+__host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
+
+__host__ __device__ inline FinishSmem finish_layout(int E, int S) {
+  FinishSmem f;
+  f.lrow = 0;
+  f.tokmask = f.lrow + align16(sizeof(float) * 8 * (size_t)E);
+  f.uidx = f.tokmask + align16(sizeof(unsigned long long) * (size_t)E);
+  f.poff = f.uidx + align16(sizeof(int) * (size_t)E);
+  f.sidx = f.poff + align16(sizeof(int) * (size_t)E);
+  f.sw = f.sidx + align16(sizeof(int) * kMaxTokens * kMaxTopK);
+  f.taken = f.sw + align16(sizeof(float) * kMaxTokens * kMaxTopK);
+  f.misc = f.taken + align16((size_t)S);
+  f.total = f.misc + sizeof(unsigned long long) * 64;
+  return f;
+}
+
+// Block-wide exclusive scan of (a, b) pairs, 256 threads; returns totals.
+__device__ void block_scan2(int& a, int& b, int& tot_a, int& tot_b, int* scratch) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int ia = a, ib = b;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int va = __shfl_up_sync(0xffffffffu, ia, o), vb = __shfl_up_sync(0xffffffffu, ib, o);
+    if (lane >= o) { ia += va; ib += vb; }
+  }
+  if (lane == 31) { scratch[warp] = ia; scratch[8 + warp] = ib; }
+  __syncthreads();
+  int wa = 0, wb = 0, ta = 0, tb = 0;
+  for (int w = 0; w < 8; ++w) {
+    if (w < warp) { wa += scratch[w]; wb += scratch[8 + w]; }
+    ta += scratch[w];
+    tb += scratch[8 + w];
+  }
+  a = wa + ia - a;
+  b = wb + ib - b;
+  tot_a = ta;
+  tot_b = tb;
+  __syncthreads();
+}
+
+// The last CTA: top-k, grouping, hit check, LRU, doorbell.
+__device__ void route_finish(const LayerArgs& a, unsigned char* smem) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int E = a.E, k = a.k, T = a.T;
+  const FinishSmem f = finish_layout(E, a.n_slots);
+  float* lrow = reinterpret_cast<float*>(smem + f.lrow);
+  unsigned long long* tokmask = reinterpret_cast<unsigned long long*>(smem + f.tokmask);
+  int* uidx = reinterpret_cast<int*>(smem + f.uidx);
+  int* poff = reinterpret_cast<int*>(smem + f.poff);
+  int* sidx = reinterpret_cast<int*>(smem + f.sidx);
+  float* sw = reinterpret_cast<float*>(smem + f.sw);
+  uint8_t* taken = smem + f.taken;
+  unsigned long long* misc = reinterpret_cast<unsigned long long*>(smem + f.misc);
+  __shared__ uint32_t s_seq;
+  __shared__ int s_nunion, s_nmiss;
+
+  if (tid == 0) {
+    a.st->ticket = 0;
+    s_seq = a.st->step + 1;
+    a.st->step = s_seq;
+  }
+  for (int e = tid; e < E; e += kRouteThreads) tokmask[e] = 0ull;
+  __syncthreads();
+  const uint32_t seq = s_seq;
+
+  // ---- top-k per token (warp per token), ties to the lower index
+  for (int t = warp; t < T; t += 8) {
+    float* lr = lrow + warp * E;
+    for (int e = lane; e < E; e += 32) lr[e] = ld_cg_f32(&a.logits[(size_t)t * E + e]);
+    __syncwarp();
+    int sel[kMaxTopK];
+    float selv[kMaxTopK];
+    for (int r = 0; r < k; ++r) {
+      float bv = -FLT_MAX;
+      int bi = INT_MAX;
+      for (int e = lane; e < E; e += 32) {
+        float v = lr[e];  // NaN marks an expert already taken
+        if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      }
+      if (bi == INT_MAX) bi = 0;  // only reachable with non-finite logits
+      if (lane == (bi & 31)) lr[bi] = __int_as_float(0x7fc00000);
+      sel[r] = bi;
+      selv[r] = bv;
+      __syncwarp();
+    }
+    if (lane == 0) {
+      // ascending expert index, weights renormalised over the selection
+      const float m = selv[0];
+      for (int i = 1; i < k; ++i) {
+        int ki = sel[i];
+        float kv = selv[i];
+        int j = i - 1;
+        while (j >= 0 && sel[j] > ki) { sel[j + 1] = sel[j]; selv[j + 1] = selv[j]; --j; }
+        sel[j + 1] = ki;
+        selv[j + 1] = kv;
+      }
+      float z = 0.f;
+      for (int j = 0; j < k; ++j) z += expf(selv[j] - m);
+      for (int j = 0; j < k; ++j) {
+        float wj = expf(selv[j] - m) / z;
+        sidx[t * k + j] = sel[j];
+        sw[t * k + j] = wj;
+        a.topk_idx[t * k + j] = sel[j];
+        a.topk_w[t * k + j] = wj;
+        atomicOr(&tokmask[sel[j]], 1ull << t);
+      }
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+
+  // ---- union of selected experts (ascending) and pair offsets
+  const int per = (E + kRouteThreads - 1) / kRouteThreads;
+  const int e0 = tid * per;
+  int fl = 0, cn = 0;
+  for (int e = e0; e < e0 + per && e < E; ++e) {
+    int c = __popcll(tokmask[e]);
+    fl += c > 0;
+    cn += c;
+  }
+  int tot_f, tot_c;
+  block_scan2(fl, cn, tot_f, tot_c, reinterpret_cast<int*>(misc));
+  for (int e = e0; e < e0 + per && e < E; ++e) {
+    int c = __popcll(tokmask[e]);
+    uidx[e] = fl;
+    poff[e] = cn;
+    if (c > 0) {
+      a.u_expert[fl] = e;
+      a.u_off[fl] = cn;
+      ++fl;
+      cn += c;
+    }
+  }
+  if (tid == 0) {
+    a.u_off[tot_f] = tot_c;
+    s_nunion = tot_f;
+  }
+  __syncthreads();
+  const int n_union = s_nunion;
+
+  // ---- pairs sorted by (expert, token)
+  for (int p = tid; p < T * k; p += kRouteThreads) {
+    const int t = p / k;
+    const int e = sidx[p];
+    const int pos = __popcll(tokmask[e] & ((1ull << t) - 1ull));
+    const int dst = poff[e] + pos;
+    a.pair_token[dst] = t;
+    a.pair_w[dst] = sw[p];
+    a.tk_u[p] = uidx[e];
+    a.tk_pos[p] = pos;
+  }
+
+  // ---- slot hit check
+  int n_miss = 0;
+  if (!a.pool) {
+    for (int u = tid; u < n_union; u += kRouteThreads) {
+      a.u_slot[u] = a.u_expert[u];
+      a.u_wait[u] = 0u;
+    }
+  } else {
+    for (int s = tid; s < a.n_slots; s += kRouteThreads) taken[s] = 0;
+    for (int u = tid; u < n_union; u += kRouteThreads) {
+      const int e = a.u_expert[u];
+      const int s = a.slot_of[e];
+      a.u_slot[u] = s;
+      a.u_wait[u] = 0u;
+    }
+    __syncthreads();
+    // misses in ascending expert order; the i-th takes the i-th best victim
+    if (tid == 0) s_nmiss = 0;
+    __syncthreads();
+    for (int u0 = 0; u0 < n_union; ++u0) {
+      const int e = a.u_expert[u0];
+      if (a.slot_of[e] >= 0) continue;  // uniform across the block
+      unsigned long long best = ~0ull;
+      for (int s = tid; s < a.n_slots; s += kRouteThreads) {
+        if (taken[s]) continue;
+        const int ow = a.owner[s];
+        if (ow >= 0 && tokmask[ow] != 0ull) continue;  // used by this step
+        unsigned long long key = ((unsigned long long)(ow >= 0) << 44) |
+                                 ((unsigned long long)a.stamp[s] << 12) | (unsigned long long)s;
+        best = key < best ? key : best;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, o);
+        best = ob < best ? ob : best;
+      }
+      if (lane == 0) misc[16 + warp] = best;
+      __syncthreads();
+      if (tid == 0) {
+        unsigned long long b = misc[16];
+        for (int w = 1; w < 8; ++w) b = misc[16 + w] < b ? misc[16 + w] : b;
+        const int s = (int)(b & 0xFFFull);
+        if (b == ~0ull) {
+          // pool smaller than the step's distinct experts (configure forbids
+          // this); keep every address in bounds and fail the step
+          a.u_slot[u0] = 0;
+          set_error(a, MOE_ERR_STATE);
+        } else {
+          const int old = a.owner[s];
+          if (old >= 0) a.slot_of[old] = -1;
+          a.owner[s] = e;
+          a.slot_of[e] = s;
+          taken[s] = 1;
+          a.u_slot[u0] = s;
+          a.u_wait[u0] = seq;
+          const uint32_t slot_i = a.st->ring_head + (uint32_t)s_nmiss;
+          volatile RingEntry* re = &a.hm->ring[slot_i % kRingSize];
+          re->seq = seq;
+          re->expert = e;
+          re->slot = s;
+          s_nmiss = s_nmiss + 1;
+        }
+      }
+      __syncthreads();
+    }
+    n_miss = s_nmiss;
+    for (int u = tid; u < n_union; u += kRouteThreads) a.stamp[a.u_slot[u]] = seq;
+    if (tid == 0 && n_miss > 0) {
+      __threadfence_system();
+      const uint32_t head = a.st->ring_head + (uint32_t)n_miss;
+      a.st->ring_head = head;
+      *reinterpret_cast<volatile uint32_t*>(&a.hm->head) = head;
+      __threadfence_system();
+    }
+  }
+  if (tid == 0) {
+    a.st->n_union = n_union;
+    a.st->n_miss = n_miss;
+    a.st->forwards += 1ull;
+    a.st->hits += (unsigned long long)(n_union - n_miss);
+    a.st->misses += (unsigned long long)n_miss;
+  }
+  __threadfence();
+}
+
+__global__ void __launch_bounds__(kRouteThreads) route_kernel(LayerArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = a.H, E = a.E, T = a.T;
+  const int row = blockIdx.x * kRouteRows + (warp >> 1);
+  const int half = warp & 1;
+  const int q4 = H / 8;  // float4 per half row
+  const bool row_ok = row < E;
+
+  // Router rows do not depend on the previous kernel: load them first.
+  float4 w[kRouteVec];
+  const float4* wrow = reinterpret_cast<const float4*>(a.W_r + (size_t)(row_ok ? row : 0) * H) + half * q4;
+#pragma unroll
+  for (int i = 0; i < kRouteVec; ++i) {
+    const int q = lane + 32 * i;
+    w[i] = (row_ok && q < q4) ? __ldg(wrow + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  pdl_wait();
+
+  // x (bf16) -> x16: fp16 in B-fragment order, for the expert kernels
+  {
+    const int oct = T * H / 8;
+    int bad = 0;
+    for (int o = blockIdx.x * kRouteThreads + tid; o < oct; o += gridDim.x * kRouteThreads) {
+      const int t = o / (H / 8), k8 = (o % (H / 8)) * 8;
+      const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)t * H + k8);
+      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float f0 = __uint_as_float(vv[i] << 16), f1 = __uint_as_float(vv[i] & 0xFFFF0000u);
+        bad |= !(fabsf(f0) < 65504.f) | !(fabsf(f1) < 65504.f);
+        const __half2 h = __floats2half2_rn(f0, f1);
+        *reinterpret_cast<__half2*>(a.x16 + (size_t)t * H + frag_pos(k8 + 2 * i)) = h;
+      }
+    }
+    if (bad) set_error(a, MOE_ERR_DEVICE);
+  }
+
+  float* xs = reinterpret_cast<float*>(smem);            // [chunk][H]
+  float* red = xs + kRouteChunk * H;                      // [8 warps][chunk]
+  for (int t0 = 0; t0 < T; t0 += kRouteChunk) {
+    const int nt = min(kRouteChunk, T - t0);
+    __syncthreads();
+    const uint32_t* xsrc = reinterpret_cast<const uint32_t*>(a.x + (size_t)t0 * H);
+    for (int i = tid; i < nt * H / 2; i += kRouteThreads) {
+      const uint32_t v = xsrc[i];
+      xs[2 * i] = __uint_as_float(v << 16);
+      xs[2 * i + 1] = __uint_as_float(v & 0xFFFF0000u);
+    }
+    __syncthreads();
+    for (int tt = 0; tt < nt; ++tt) {
+      const float4* xr = reinterpret_cast<const float4*>(xs + tt * H) + half * q4;
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < kRouteVec; ++i) {
+        const int q = lane + 32 * i;
+        if (q < q4) {
+          const float4 xv = xr[q];
+          s = fmaf(w[i].x, xv.x, s);
+          s = fmaf(w[i].y, xv.y, s);
+          s = fmaf(w[i].z, xv.z, s);
+          s = fmaf(w[i].w, xv.w, s);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (lane == 0) red[warp * kRouteChunk + tt] = s;
+    }
+    __syncthreads();
+    if (tid < kRouteRows * nt) {
+      const int r = tid / nt, tt = tid % nt;
+      const int e = blockIdx.x * kRouteRows + r;
+      if (e < E) {
+        const float l = red[(2 * r) * kRouteChunk + tt] + red[(2 * r + 1) * kRouteChunk + tt];
+        a.logits[(size_t)(t0 + tt) * E + e] = l + ((a.bias) ? __ldg(a.bias + e) : 0.f);
+      }
+    }
+  }
+  __threadfence();
+  __syncthreads();
+  pdl_trigger();
+  __shared__ uint32_t s_ticket;
+  if (tid == 0) s_ticket = atomicAdd(&a.st->ticket, 1u);
+  __syncthreads();
+  if (s_ticket != gridDim.x - 1) return;
+  __threadfence();
+  route_finish(a, smem);
+}
+
+// ------------------------------------------------------------------ gate/up
+
+constexpr int kGuThreads = 256;  // 8 warps split the K = H reduction of a strip
+constexpr int kGuBatch = 4;      // super-tiles per warp with loads in flight together
+
+// Waits (one thread, bounded by the layer's timeout) until the slot holds the
+// step's copy.  Returns false when the copy failed, timed out or the layer
+// already carries an error.
+// Called by one thread: waits (bounded by the layer's timeout) until the slot
+// holds this step's copy.  Returns false when the copy failed, timed out or
+// the layer already carries an error.
+__device__ bool wait_slot(const LayerArgs& a, int slot, uint32_t seq, bool count_time) {
+  const uint64_t t0 = global_ns();
+  const uint64_t deadline = t0 + a.wait_timeout_ns;
+  bool ok = true;
+  for (;;) {
+    const uint32_t v = ld_acquire_sys(&a.ready[slot]);
+    if (v == seq) break;
+    if (v == (seq | kReadyError)) { set_error(a, MOE_ERR_COPY); ok = false; break; }
+    if (dev_error(a)) { ok = false; break; }
+    if (global_ns() > deadline) { set_error(a, MOE_ERR_TIMEOUT); ok = false; break; }
+    __nanosleep(200);
+  }
+  if (count_time) atomicAdd(&a.st->wait_ns, (unsigned long long)(global_ns() - t0));
+  return ok;
+}
+
+template <int NG>
+__global__ void __launch_bounds__(kGuThreads) gateup_kernel(LayerArgs a) {
+  extern __shared__ __align__(16) float red[];  // [8 warps][NG][32 lanes][8]
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int H = a.H, I = a.I;
+  const int NS = I / 16, nst = H / 64;
+  const int n_union = ld_cg_i32(&a.st->n_union);
+  const int n_tasks = (a.n_shared + n_union) * NS;
+  __shared__ int s_go;
+  for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
+    const int gu = task / NS, s = task % NS;
+    const bool sh = gu < a.n_shared;
+    const uint8_t* base;
+    int cnt, poff;
+    uint32_t wseq = 0u;
+    int slot = 0;
+    if (sh) {
+      base = a.shared;
+      cnt = a.T;
+      poff = a.T * a.k;
+    } else {
+      const int u = gu - a.n_shared;
+      slot = ld_cg_i32(&a.u_slot[u]);
+      base = a.arena + (int64_t)slot * a.blob;
+      poff = ld_cg_i32(&a.u_off[u]);
+      cnt = ld_cg_i32(&a.u_off[u + 1]) - poff;
+      wseq = (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.u_wait[u]));
+    }
+    // one thread decides for the block: no error so far, and the slot's
+    // copy (if this step missed the expert) has landed
+    if (tid == 0) s_go = (dev_error(a) == 0) && (wseq == 0u || wait_slot(a, slot, wseq, s == 0));
+    __syncthreads();
+    if (!s_go) return;
+    const uint8_t* strip = base + (int64_t)s * gu_strip_bytes(H);
+    const int ng = (cnt + 7) >> 3;
+    int tok[NG];
+#pragma unroll
+    for (int q = 0; q < NG; ++q) {
+      const int i = q * 8 + g;
+      tok[q] = (i < cnt) ? (sh ? i : ld_cg_i32(&a.pair_token[poff + i])) : 0;
+    }
+    float accg[NG][4], accu[NG][4];
+#pragma unroll
+    for (int q = 0; q < NG; ++q)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) accg[q][c] = accu[q][c] = 0.f;
+
+    for (int st0 = warp; st0 < nst; st0 += 8 * kGuBatch) {
+      uint4 ngw[kGuBatch], nuw[kGuBatch];
+      uint2 gsc[kGuBatch], usc[kGuBatch];
+#pragma unroll
+      for (int b = 0; b < kGuBatch; ++b) {
+        const int st = st0 + 8 * b;
+        if (st < nst) {
+          ngw[b] = ld_cg4(strip + st * 512 + lane * 16);
+          gsc[b] = ld_cg2(strip + 8 * H + st * 64 + g * 8);
+          nuw[b] = ld_cg4(strip + 9 * H + st * 512 + lane * 16);
+          usc[b] = ld_cg2(strip + 17 * H + st * 64 + g * 8);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kGuBatch; ++b) {
+        const int st = st0 + 8 * b;
+        if (st < nst) {
+#pragma unroll
+          for (int q = 0; q < NG; ++q) {
+            if (q < ng) {
+              const __half* xr = a.x16 + (size_t)tok[q] * H + st * 64 + t4 * 16;
+              const uint4 b01 = ld_cg4(xr), b23 = ld_cg4(xr + 8);
+              supertile_mma(accg[q], ngw[b], gsc[b], b01, b23);
+              supertile_mma(accu[q], nuw[b], usc[b], b01, b23);
+            }
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int q = 0; q < NG; ++q) {
+      float4* dst = reinterpret_cast<float4*>(red + (((warp * NG) + q) * 32 + lane) * 8);
+      dst[0] = make_float4(accg[q][0], accg[q][1], accg[q][2], accg[q][3]);
+      dst[1] = make_float4(accu[q][0], accu[q][1], accu[q][2], accu[q][3]);
+    }
+    __syncthreads();
+    if (warp < ng) {
+      const int q = warp;
+      float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int w = 0; w < 8; ++w) {
+        const float4* src = reinterpret_cast<const float4*>(red + (((w * NG) + q) * 32 + lane) * 8);
+        const float4 p = src[0], r = src[1];
+        gs[0] += p.x; gs[1] += p.y; gs[2] += p.z; gs[3] += p.w;
+        us[0] += r.x; us[1] += r.y; us[2] += r.z; us[3] += r.w;
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int rowin = (c < 2) ? g : g + 8;
+        const int col = 2 * t4 + (c & 1);
+        const int i = q * 8 + col;
+        if (i < cnt) {
+          const int hrow = poff + i;
+          a.h16[(size_t)hrow * I + frag_pos(s * 16 + rowin)] = __float2half_rn(silu(gs[c]) * us[c]);
+        }
+      }
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ down + combine
+
+constexpr int kDnThreads = 512;  // 16 warps, one expert each per batch
+constexpr int kDnWarps = kDnThreads / 32;
+constexpr int kDnBatch = 8;      // super-tiles with loads in flight together
+
+template <int NG>
+__global__ void __launch_bounds__(kDnThreads) down_kernel(LayerArgs a) {
+  extern __shared__ __align__(16) float dsm[];
+  float* zbuf = dsm;                                   // [16 warps][NG][32 lanes][4]
+  float* yacc = dsm + kDnWarps * NG * 32 * 4;          // [T][16]
+  pdl_wait();
+  pdl_trigger();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int H = a.H, I = a.I, T = a.T, k = a.k;
+  const int n_union = ld_cg_i32(&a.st->n_union);
+  const int n_ex = n_union + a.n_shared;
+  const int nst = I / 64;
+  for (int r = blockIdx.x; r < H / 16; r += gridDim.x) {
+    for (int q = tid; q < T * 16; q += kDnThreads) yacc[q] = 0.f;
+    for (int b0 = 0; b0 < n_ex; b0 += kDnWarps) {
+      const int xi = b0 + warp;
+      if (xi < n_ex) {
+        const bool sh = xi >= n_union;
+        const uint8_t* base;
+        int cnt, poff;
+        if (sh) {
+          base = a.shared;
+          cnt = T;
+          poff = T * k;
+        } else {
+          base = a.arena + (int64_t)ld_cg_i32(&a.u_slot[xi]) * a.blob;
+          poff = ld_cg_i32(&a.u_off[xi]);
+          cnt = ld_cg_i32(&a.u_off[xi + 1]) - poff;
+        }
+        const uint8_t* strip = base + down_base(H, I) + (int64_t)r * down_strip_bytes(I);
+        const int ng = (cnt + 7) >> 3;
+        int hrow[NG];
+#pragma unroll
+        for (int q = 0; q < NG; ++q) {
+          const int i = q * 8 + g;
+          hrow[q] = poff + ((i < cnt) ? i : 0);
+        }
+        float acc[NG][4];
+#pragma unroll
+        for (int q = 0; q < NG; ++q) acc[q][0] = acc[q][1] = acc[q][2] = acc[q][3] = 0.f;
+        for (int st0 = 0; st0 < nst; st0 += kDnBatch) {
+          uint4 nw[kDnBatch];
+          uint2 sc[kDnBatch];
+#pragma unroll
+          for (int b = 0; b < kDnBatch; ++b) {
+            const int st = st0 + b;
+            if (st < nst) {
+              nw[b] = ld_cg4(strip + st * 512 + lane * 16);
+              sc[b] = ld_cg2(strip + 8 * I + st * 64 + g * 8);
+            }
+          }
+#pragma unroll
+          for (int b = 0; b < kDnBatch; ++b) {
+            const int st = st0 + b;
+            if (st < nst) {
+#pragma unroll
+              for (int q = 0; q < NG; ++q) {
+                if (q < ng) {
+                  const __half* hr = a.h16 + (size_t)hrow[q] * I + st * 64 + t4 * 16;
+                  supertile_mma(acc[q], nw[b], sc[b], ld_cg4(hr), ld_cg4(hr + 8));
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < NG; ++q)
+          *reinterpret_cast<float4*>(zbuf + ((warp * NG + q) * 32 + lane) * 4) =
+              make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
+      }
+      __syncthreads();
+      // combine this batch: token t, output row; ascending expert order
+      for (int q = tid; q < T * 16; q += kDnThreads) {
+        const int t = q >> 4, row = q & 15;
+        float v = yacc[q];
+        for (int j = 0; j < k; ++j) {
+          const int u = ld_cg_i32(&a.tk_u[t * k + j]);
+          if (u >= b0 && u < b0 + kDnWarps) {
+            const int pos = ld_cg_i32(&a.tk_pos[t * k + j]);
+            const int grp = pos >> 3, col = pos & 7;
+            const int lz = (row & 7) * 4 + (col >> 1), rz = (row >> 3) * 2 + (col & 1);
+            v = fmaf(ld_cg_f32(&a.topk_w[t * k + j]), zbuf[(((u - b0) * NG + grp) * 32 + lz) * 4 + rz], v);
+          }
+        }
+        if (a.n_shared && n_union >= b0 && n_union < b0 + kDnWarps) {
+          const int grp = t >> 3, col = t & 7;
+          const int lz = (row & 7) * 4 + (col >> 1), rz = (row >> 3) * 2 + (col & 1);
+          v += zbuf[(((n_union - b0) * NG + grp) * 32 + lz) * 4 + rz];
+        }
+        yacc[q] = v;
+      }
+      __syncthreads();
+    }
+    for (int q = tid; q < T * 16; q += kDnThreads) {
+      const int t = q >> 4, row = q & 15;
+      a.y[(size_t)t * H + r * 16 + row] = __bfloat16_as_ushort(__float2bfloat16_rn(yacc[q]));
+    }
+    __syncthreads();
+  }
+}
+
+// ------------------------------------------------------------------ residual + RMSNorm
+
+__global__ void __launch_bounds__(256) residual_rmsnorm_kernel(const uint16_t* x, const uint16_t* y, int H, float eps,
+                                                                 uint16_t* x_out, uint16_t* xhat) {
+  extern __shared__ float xs[];  // [H]
+  __shared__ float part[8];
+  const int t = blockIdx.x, tid = threadIdx.x;
+  float ss = 0.f;
+  for (int i = tid; i < H; i += 256) {
+    float v = __uint_as_float((uint32_t)x[(size_t)t * H + i] << 16);
+    if (y) v += __uint_as_float((uint32_t)y[(size_t)t * H + i] << 16);
+    const __nv_bfloat16 b = __float2bfloat16_rn(v);
+    const float vr = __bfloat162float(b);
+    xs[i] = vr;
+    ss = fmaf(vr, vr, ss);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if ((tid & 31) == 0) part[tid >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < 8; ++w) tot += part[w];
+  const float inv = 1.0f / sqrtf(tot / (float)H + eps);
+  for (int i = tid; i < H; i += 256) {
+    if (x_out) x_out[(size_t)t * H + i] = __bfloat16_as_ushort(__float2bfloat16_rn(xs[i]));
+    xhat[(size_t)t * H + i] = __bfloat16_as_ushort(__float2bfloat16_rn(xs[i] * inv));
+  }
+}
+
+template <typename K>
+cudaError_t launch(K kernel, int grid, int block, size_t smem, cudaStream_t s, bool pdl, const LayerArgs& a) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, a);
+}
+
+size_t gateup_smem(int NG) { return sizeof(float) * 8 * NG * 32 * 8; }
+size_t down_smem(int NG, int T) { return sizeof(float) * (kDnWarps * NG * 32 * 4 + T * 16); }
+
+}  // namespace
+
+size_t route_smem_bytes(int H, int E) {
+  size_t a = sizeof(float) * (kRouteChunk * (size_t)H + 8 * kRouteChunk);
+  size_t b = finish_layout(E, kMaxExperts).total;
+  return a > b ? a : b;
+}
+
+cudaError_t configure_kernels(int H, int E) {
+  cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)route_smem_bytes(kMaxHidden, kMaxExperts));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(gateup_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gateup_smem(8));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(down_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)down_smem(8, kMaxTokens));
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(residual_rmsnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)(sizeof(float) * kMaxHidden));
+  (void)H;
+  (void)E;
+  return e;
+}
+
+int gateup_max_blocks_per_sm(int T) {
+  int n = 0;
+  if (T <= 8)
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gateup_kernel<1>, kGuThreads, gateup_smem(1));
+  else
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, gateup_kernel<8>, kGuThreads, gateup_smem(8));
+  return n > 0 ? n : 1;
+}
+
+int down_max_blocks_per_sm(int T) {
+  int n = 0;
+  if (T <= 8)
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, down_kernel<1>, kDnThreads, down_smem(1, 8));
+  else
+    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, down_kernel<8>, kDnThreads, down_smem(8, kMaxTokens));
+  return n > 0 ? n : 1;
+}
+
+cudaError_t launch_route(const LayerArgs& a, cudaStream_t s, bool pdl) {
+  const int grid = (a.E + kRouteRows - 1) / kRouteRows;
+  size_t smem = route_smem_bytes(a.H, a.E);
+  const size_t fin = finish_layout(a.E, a.n_slots).total;
+  if (fin > smem) smem = fin;
+  return launch(route_kernel, grid, kRouteThreads, smem, s, pdl, a);
+}
+
+cudaError_t launch_gateup(const LayerArgs& a, cudaStream_t s, bool pdl, int grid) {
+  if (a.T <= 8) return launch(gateup_kernel<1>, grid, kGuThreads, gateup_smem(1), s, pdl, a);
+  return launch(gateup_kernel<8>, grid, kGuThreads, gateup_smem(8), s, pdl, a);
+}
+
+cudaError_t launch_down(const LayerArgs& a, cudaStream_t s, bool pdl, int grid) {
+  if (a.T <= 8) return launch(down_kernel<1>, grid, kDnThreads, down_smem(1, a.T), s, pdl, a);
+  return launch(down_kernel<8>, grid, kDnThreads, down_smem(8, a.T), s, pdl, a);
+}
+
+cudaError_t launch_residual_rmsnorm(const uint16_t* x, const uint16_t* y, int T, int H, float eps, uint16_t* x_out,
+                                    uint16_t* xhat, cudaStream_t s) {
+  residual_rmsnorm_kernel<<<T, 256, sizeof(float) * H, s>>>(x, y, H, eps, x_out, xhat);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,586 @@
+// Host runtime behind include/moe.h: layer objects, the lossless repack into
+// the GPU layout, the VRAM expert-slot pool, and the copy server that serves
+// misses from the pinned host master copy.
+//
+// Residency design (Betelgeuse news page, section 机制): every selected
+// expert is resolved on the GPU (route kernel); only a miss involves the
+// host.  The device appends {seq, expert, slot} to a ring in mapped pinned
+// memory and publishes the ring head; this thread polls the head, issues one
+// contiguous cudaMemcpyAsync per missed expert on its own stream and then a
+// stream write of `seq` into the slot's ready flag, which the expert kernels
+// wait on (with a deadline).  A failed or skipped copy is written back as
+// seq | kReadyError and surfaces as MOE_ERR_COPY (section "bit-exact 的确切
+// 含义": a failed expert read stops with an error rather than using zeros).
+#include <cuda.h>
+
+#include <atomic>
+#include <chrono>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <thread>
+#include <vector>
+
+#include "moe.h"
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+typedef CUresult (*WriteValue32Fn)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    ok = cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+inline uint8_t nibble_at(const uint8_t* nib, int K, int r, int c) {
+  return (uint8_t)((nib[(size_t)r * (K / 2) + c / 2] >> ((c & 1) * 4)) & 15);
+}
+
+// Canonical R x K matrix -> GPU-layout strips (see moe_internal.h).
+void repack_matrix(const uint8_t* canon, int R, int K, uint8_t* dst, int64_t strip_stride, int64_t nib_off,
+                   int64_t sc_off) {
+  const uint8_t* nib = canon;
+  const uint8_t* sc = canon + (size_t)R * (K / 2);
+  for (int s = 0; s < R / 16; ++s) {
+    uint8_t* strip = dst + s * strip_stride;
+    for (int st = 0; st < K / 64; ++st) {
+      for (int lane = 0; lane < 32; ++lane) {
+        const int g = lane >> 2, t = lane & 3;
+        const int rg = 16 * s + g, rg8 = rg + 8;
+        for (int kt = 0; kt < 4; ++kt) {
+          const int k0 = 64 * st + 16 * kt;
+          uint32_t w = 0;
+          w |= (uint32_t)nibble_at(nib, K, rg, k0 + 2 * t) << 0;
+          w |= (uint32_t)nibble_at(nib, K, rg, k0 + 2 * t + 8) << 4;
+          w |= (uint32_t)nibble_at(nib, K, rg8, k0 + 2 * t) << 8;
+          w |= (uint32_t)nibble_at(nib, K, rg8, k0 + 2 * t + 8) << 12;
+          w |= (uint32_t)nibble_at(nib, K, rg, k0 + 2 * t + 1) << 16;
+          w |= (uint32_t)nibble_at(nib, K, rg, k0 + 2 * t + 9) << 20;
+          w |= (uint32_t)nibble_at(nib, K, rg8, k0 + 2 * t + 1) << 24;
+          w |= (uint32_t)nibble_at(nib, K, rg8, k0 + 2 * t + 9) << 28;
+          std::memcpy(strip + nib_off + st * 512 + lane * 16 + kt * 4, &w, 4);
+        }
+      }
+      for (int g = 0; g < 8; ++g) {
+        const int rg = 16 * s + g, rg8 = rg + 8;
+        const int b0 = 2 * st, b1 = 2 * st + 1;
+        uint8_t* o = strip + sc_off + st * 64 + g * 8;
+        std::memcpy(o + 0, sc + ((size_t)rg * (K / 32) + b0) * 2, 2);
+        std::memcpy(o + 2, sc + ((size_t)rg8 * (K / 32) + b0) * 2, 2);
+        std::memcpy(o + 4, sc + ((size_t)rg * (K / 32) + b1) * 2, 2);
+        std::memcpy(o + 6, sc + ((size_t)rg8 * (K / 32) + b1) * 2, 2);
+      }
+    }
+  }
+}
+
+// Inverse of repack_matrix.
+void unpack_matrix(const uint8_t* src, int R, int K, uint8_t* canon, int64_t strip_stride, int64_t nib_off,
+                   int64_t sc_off) {
+  uint8_t* nib = canon;
+  uint8_t* sc = canon + (size_t)R * (K / 2);
+  std::memset(nib, 0, (size_t)R * (K / 2));
+  for (int s = 0; s < R / 16; ++s) {
+    const uint8_t* strip = src + s * strip_stride;
+    for (int st = 0; st < K / 64; ++st) {
+      for (int lane = 0; lane < 32; ++lane) {
+        const int g = lane >> 2, t = lane & 3;
+        const int rg = 16 * s + g, rg8 = rg + 8;
+        for (int kt = 0; kt < 4; ++kt) {
+          const int k0 = 64 * st + 16 * kt;
+          uint32_t w;
+          std::memcpy(&w, strip + nib_off + st * 512 + lane * 16 + kt * 4, 4);
+          const int rows[8] = {rg, rg, rg8, rg8, rg, rg, rg8, rg8};
+          const int cols[8] = {k0 + 2 * t, k0 + 2 * t + 8, k0 + 2 * t, k0 + 2 * t + 8,
+                               k0 + 2 * t + 1, k0 + 2 * t + 9, k0 + 2 * t + 1, k0 + 2 * t + 9};
+          for (int i = 0; i < 8; ++i) {
+            const uint8_t v = (uint8_t)((w >> (4 * i)) & 15);
+            nib[(size_t)rows[i] * (K / 2) + cols[i] / 2] |= (uint8_t)(v << ((cols[i] & 1) * 4));
+          }
+        }
+      }
+      for (int g = 0; g < 8; ++g) {
+        const int rg = 16 * s + g, rg8 = rg + 8;
+        const int b0 = 2 * st, b1 = 2 * st + 1;
+        const uint8_t* o = strip + sc_off + st * 64 + g * 8;
+        std::memcpy(sc + ((size_t)rg * (K / 32) + b0) * 2, o + 0, 2);
+        std::memcpy(sc + ((size_t)rg8 * (K / 32) + b0) * 2, o + 2, 2);
+        std::memcpy(sc + ((size_t)rg * (K / 32) + b1) * 2, o + 4, 2);
+        std::memcpy(sc + ((size_t)rg8 * (K / 32) + b1) * 2, o + 6, 2);
+      }
+    }
+  }
+}
+
+inline int64_t mat_bytes(int R, int K) { return (int64_t)R * (K / 2) + (int64_t)R * (K / 32) * 2; }
+
+void repack_expert(const uint8_t* canon, int H, int I, uint8_t* gpu) {
+  const int64_t mb = mat_bytes(I, H);
+  repack_matrix(canon, I, H, gpu, gu_strip_bytes(H), 0, 8ll * H);
+  repack_matrix(canon + mb, I, H, gpu, gu_strip_bytes(H), 9ll * H, 17ll * H);
+  repack_matrix(canon + 2 * mb, H, I, gpu + down_base(H, I), down_strip_bytes(I), 0, 8ll * I);
+}
+
+void unpack_expert(const uint8_t* gpu, int H, int I, uint8_t* canon) {
+  const int64_t mb = mat_bytes(I, H);
+  unpack_matrix(gpu, I, H, canon, gu_strip_bytes(H), 0, 8ll * H);
+  unpack_matrix(gpu, I, H, canon + mb, gu_strip_bytes(H), 9ll * H, 17ll * H);
+  unpack_matrix(gpu + down_base(H, I), H, I, canon + 2 * mb, down_strip_bytes(I), 0, 8ll * I);
+}
+
+// Repack n experts on all host cores.
+void repack_many(const uint8_t* canon, int64_t n, int H, int I, uint8_t* gpu) {
+  const int64_t eb = expert_bytes(H, I);
+  unsigned nt = std::thread::hardware_concurrency();
+  if (nt == 0) nt = 1;
+  if (nt > 32) nt = 32;
+  if ((int64_t)nt > n) nt = (unsigned)(n > 0 ? n : 1);
+  std::vector<std::thread> th;
+  for (unsigned t = 0; t < nt; ++t) {
+    const int64_t a = n * t / nt, b = n * (t + 1) / nt;
+    auto job = [=] {
+      for (int64_t e = a; e < b; ++e) repack_expert(canon + e * eb, H, I, gpu + e * eb);
+    };
+    try {
+      th.emplace_back(job);
+    } catch (...) {
+      job();
+    }
+  }
+  for (auto& t : th) t.join();
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+}  // namespace
+
+struct moe_layer {
+  moe_layer_desc_t d{};
+  int sm_count = 0;
+  int64_t blob = 0;
+  uint8_t* master = nullptr;  // pinned host, GPU layout, E experts
+  uint8_t* shared_dev = nullptr;
+  void* dev_block = nullptr;
+  HostMapped* hm_host = nullptr;
+  HostMapped* hm_dev = nullptr;
+  LayerArgs args{};
+  int n_slots = 0;
+  uint8_t* arena = nullptr;
+  cudaStream_t copy_stream = nullptr;
+  WriteValue32Fn write_value = nullptr;
+  std::thread server;
+  std::atomic<bool> stop{false};
+  std::atomic<bool> paused{false};
+  std::atomic<int64_t> fail_copy_n{0};
+  std::atomic<int64_t> copies_since_arm{0};
+  std::atomic<int> host_error{0};
+  std::mutex log_mu;
+  std::vector<int32_t> miss_log;
+  std::atomic<uint64_t> h2d_bytes{0};
+  uint64_t wait_timeout_ns = 2000000000ull;
+};
+
+namespace {
+
+void serve_entry(moe_layer* L, const RingEntry& e) {
+  bool fail = false;
+  const int64_t n = L->fail_copy_n.load();
+  if (n > 0 && ++L->copies_since_arm == n) fail = true;
+  if (e.slot < 0 || e.slot >= L->n_slots || e.expert < 0 || e.expert >= L->d.n_experts) fail = true;
+  if (!fail) {
+    const cudaError_t err = cudaMemcpyAsync(L->arena + (int64_t)e.slot * L->blob, L->master + (int64_t)e.expert * L->blob,
+                                            (size_t)L->blob, cudaMemcpyHostToDevice, L->copy_stream);
+    if (err != cudaSuccess) fail = true;
+  }
+  uint32_t val = e.seq;
+  if (fail) {
+    val |= kReadyError;
+    int expected = 0;
+    L->host_error.compare_exchange_strong(expected, MOE_ERR_COPY);
+  } else {
+    L->h2d_bytes += (uint64_t)L->blob;
+  }
+  const int slot = (e.slot >= 0 && e.slot < L->n_slots) ? e.slot : 0;
+  L->write_value((CUstream)L->copy_stream, (CUdeviceptr)(L->args.ready + slot), val, 0);
+  std::lock_guard<std::mutex> g(L->log_mu);
+  L->miss_log.push_back((int32_t)e.seq);
+  L->miss_log.push_back(e.expert);
+  L->miss_log.push_back(e.slot);
+}
+
+void server_main(moe_layer* L) {
+  cudaSetDevice(L->d.device);
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  cudaThreadExchangeStreamCaptureMode(&mode);
+  uint32_t tail = __atomic_load_n(&L->hm_host->head, __ATOMIC_ACQUIRE);
+  uint64_t idle = 0;
+  while (!L->stop.load(std::memory_order_relaxed)) {
+    if (L->paused.load(std::memory_order_relaxed)) {
+      std::this_thread::sleep_for(std::chrono::microseconds(200));
+      continue;
+    }
+    const uint32_t head = __atomic_load_n(&L->hm_host->head, __ATOMIC_ACQUIRE);
+    if (head == tail) {
+      if (++idle > 200000) std::this_thread::sleep_for(std::chrono::microseconds(20));
+      continue;
+    }
+    idle = 0;
+    while (tail != head) {
+      RingEntry e;
+      const volatile RingEntry* src = &L->hm_host->ring[tail % kRingSize];
+      e.seq = src->seq;
+      e.expert = src->expert;
+      e.slot = src->slot;
+      e.pad = 0;
+      serve_entry(L, e);
+      ++tail;
+    }
+  }
+}
+
+void stop_server(moe_layer* L) {
+  if (L->server.joinable()) {
+    L->stop = true;
+    L->server.join();
+    L->stop = false;
+  }
+}
+
+int sticky_error(moe_layer* L) {
+  int e = L->host_error.load();
+  if (e) return e;
+  return __atomic_load_n(&L->hm_host->error, __ATOMIC_ACQUIRE);
+}
+
+void free_layer(moe_layer* L) {
+  if (!L) return;
+  stop_server(L);
+  if (L->copy_stream) cudaStreamDestroy(L->copy_stream);
+  if (L->dev_block) cudaFree(L->dev_block);
+  if (L->shared_dev) cudaFree(L->shared_dev);
+  if (L->hm_host) cudaFreeHost(L->hm_host);
+  if (L->master) cudaFreeHost(L->master);
+  delete L;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_expert_bytes(int32_t hidden, int32_t inter) {
+  if (hidden <= 0 || inter <= 0 || hidden % 32 || inter % 32) return 0;
+  return (size_t)mat_bytes(inter, hidden) * 3;
+}
+
+MOE_API moe_status_t moe_repack_expert(const uint8_t* canon, int32_t hidden, int32_t inter, uint8_t* gpu) {
+  if (!canon || !gpu || hidden % 64 || inter % 64 || hidden <= 0 || inter <= 0) return MOE_ERR_INVALID_ARG;
+  repack_expert(canon, hidden, inter, gpu);
+  return MOE_OK;
+}
+
+MOE_API moe_status_t moe_unpack_expert(const uint8_t* gpu, int32_t hidden, int32_t inter, uint8_t* canon) {
+  if (!canon || !gpu || hidden % 64 || inter % 64 || hidden <= 0 || inter <= 0) return MOE_ERR_INVALID_ARG;
+  unpack_expert(gpu, hidden, inter, canon);
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!desc) return MOE_ERR_INVALID_ARG;
+  const moe_layer_desc_t& d = *desc;
+  if (d.qblock != kQBlock) return MOE_ERR_UNSUPPORTED;
+  if (d.hidden <= 0 || d.inter <= 0 || d.n_experts <= 0 || d.top_k <= 0 || d.max_tokens <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (d.hidden % 64 || d.inter % 64 || d.hidden > kMaxHidden || d.inter > kMaxInter) return MOE_ERR_UNSUPPORTED;
+  if (d.n_experts > kMaxExperts || d.top_k > kMaxTopK || d.top_k > d.n_experts) return MOE_ERR_UNSUPPORTED;
+  if (d.max_tokens > kMaxTokens) return MOE_ERR_UNSUPPORTED;
+  if (d.n_shared != 0 && d.n_shared != 1) return MOE_ERR_UNSUPPORTED;
+  if (!d.router_w || !d.experts || (d.n_shared && !d.shared)) return MOE_ERR_INVALID_ARG;
+
+  DeviceGuard guard(d.device);
+  if (!guard.ok) return MOE_ERR_INVALID_ARG;
+  moe_layer* L = new (std::nothrow) moe_layer();
+  if (!L) return MOE_ERR_OUT_OF_MEMORY;
+  L->d = d;
+  L->d.experts = nullptr;  // read during create only
+  L->d.shared = nullptr;
+  L->blob = expert_bytes(d.hidden, d.inter);
+  const int E = d.n_experts, H = d.hidden, I = d.inter, k = d.top_k, Tm = d.max_tokens;
+  moe_status_t st = MOE_OK;
+  auto fail = [&](moe_status_t s) {
+    free_layer(L);
+    return s;
+  };
+  if (cudaDeviceGetAttribute(&L->sm_count, cudaDevAttrMultiProcessorCount, d.device) != cudaSuccess)
+    return fail(MOE_ERR_CUDA);
+  int cc_major = 0;
+  cudaDeviceGetAttribute(&cc_major, cudaDevAttrComputeCapabilityMajor, d.device);
+  if (cc_major < 10) return fail(MOE_ERR_UNSUPPORTED);
+  if (configure_kernels(H, E) != cudaSuccess) return fail(MOE_ERR_CUDA);
+
+  // stream write for the ready flags (driver entry point; no link-time libcuda)
+  {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return fail(MOE_ERR_CUDA);
+    L->write_value = (WriteValue32Fn)fn;
+  }
+
+  // pinned master copy in GPU layout
+  if (cudaHostAlloc((void**)&L->master, (size_t)L->blob * E, cudaHostAllocDefault) != cudaSuccess) {
+    L->master = nullptr;
+    return fail(MOE_ERR_OUT_OF_MEMORY);
+  }
+  repack_many(d.experts, E, H, I, L->master);
+
+  if (d.n_shared) {
+    std::vector<uint8_t> tmp((size_t)L->blob);
+    repack_expert(d.shared, H, I, tmp.data());
+    if (cudaMalloc((void**)&L->shared_dev, (size_t)L->blob) != cudaSuccess) {
+      L->shared_dev = nullptr;
+      return fail(MOE_ERR_OUT_OF_MEMORY);
+    }
+    if (cudaMemcpy(L->shared_dev, tmp.data(), (size_t)L->blob, cudaMemcpyHostToDevice) != cudaSuccess)
+      return fail(MOE_ERR_CUDA);
+  }
+
+  // mapped host block (doorbell ring + error mirror)
+  if (cudaHostAlloc((void**)&L->hm_host, sizeof(HostMapped), cudaHostAllocMapped) != cudaSuccess) {
+    L->hm_host = nullptr;
+    return fail(MOE_ERR_OUT_OF_MEMORY);
+  }
+  std::memset(L->hm_host, 0, sizeof(HostMapped));
+  if (cudaHostGetDevicePointer((void**)&L->hm_dev, L->hm_host, 0) != cudaSuccess) return fail(MOE_ERR_CUDA);
+
+  // device state + scratch, one allocation
+  const int Um = E < Tm * k ? E : Tm * k;
+  const size_t P = (size_t)Tm * k;
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    size_t o = off;
+    off += align256(bytes);
+    return o;
+  };
+  const size_t o_st = carve(sizeof(DevState)), o_slot_of = carve(4ull * E), o_owner = carve(4ull * E),
+               o_stamp = carve(4ull * E), o_ready = carve(4ull * E), o_logits = carve(4ull * Tm * E),
+               o_x16 = carve(2ull * Tm * H), o_uexp = carve(4ull * Um), o_uslot = carve(4ull * Um),
+               o_uwait = carve(4ull * Um), o_uoff = carve(4ull * (Um + 1)), o_ptok = carve(4 * P),
+               o_pw = carve(4 * P), o_tku = carve(4 * P), o_tkpos = carve(4 * P),
+               o_h16 = carve(2ull * (P + Tm) * I), o_tki = carve(4 * P), o_tkw = carve(4 * P);
+  if (cudaMalloc(&L->dev_block, off) != cudaSuccess) {
+    L->dev_block = nullptr;
+    return fail(MOE_ERR_OUT_OF_MEMORY);
+  }
+  uint8_t* b = (uint8_t*)L->dev_block;
+  if (cudaMemset(b, 0, off) != cudaSuccess) return fail(MOE_ERR_CUDA);
+  LayerArgs& a = L->args;
+  a.H = H;
+  a.E = E;
+  a.k = k;
+  a.I = I;
+  a.n_shared = d.n_shared;
+  a.W_r = d.router_w;
+  a.bias = d.router_bias;
+  a.shared = L->shared_dev;
+  a.blob = L->blob;
+  a.st = (DevState*)(b + o_st);
+  a.hm = L->hm_dev;
+  a.slot_of = (int32_t*)(b + o_slot_of);
+  a.owner = (int32_t*)(b + o_owner);
+  a.stamp = (uint32_t*)(b + o_stamp);
+  a.ready = (uint32_t*)(b + o_ready);
+  a.logits = (float*)(b + o_logits);
+  a.x16 = (__half*)(b + o_x16);
+  a.u_expert = (int32_t*)(b + o_uexp);
+  a.u_slot = (int32_t*)(b + o_uslot);
+  a.u_wait = (uint32_t*)(b + o_uwait);
+  a.u_off = (int32_t*)(b + o_uoff);
+  a.pair_token = (int32_t*)(b + o_ptok);
+  a.pair_w = (float*)(b + o_pw);
+  a.tk_u = (int32_t*)(b + o_tku);
+  a.tk_pos = (int32_t*)(b + o_tkpos);
+  a.h16 = (__half*)(b + o_h16);
+  a.topk_idx = (int32_t*)(b + o_tki);
+  a.topk_w = (float*)(b + o_tkw);
+  a.wait_timeout_ns = L->wait_timeout_ns;
+  if (cudaStreamCreateWithFlags(&L->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    L->copy_stream = nullptr;
+    return fail(MOE_ERR_CUDA);
+  }
+  (void)st;
+  *out = L;
+  return MOE_OK;
+}
+
+moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* arena_dev, size_t arena_bytes) {
+  if (!L || !arena_dev) return MOE_ERR_INVALID_ARG;
+  const int E = L->d.n_experts;
+  const int need = E < L->d.max_tokens * L->d.top_k ? E : L->d.max_tokens * L->d.top_k;
+  if (n_slots < need || n_slots > E) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)arena_dev & 255) != 0) return MOE_ERR_INVALID_ARG;
+  if ((size_t)n_slots * (size_t)L->blob > arena_bytes) return MOE_ERR_OUT_OF_MEMORY;
+  DeviceGuard guard(L->d.device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  stop_server(L);
+  L->arena = (uint8_t*)arena_dev;
+  L->n_slots = n_slots;
+  LayerArgs& a = L->args;
+  a.arena = L->arena;
+  a.n_slots = n_slots;
+  a.pool = n_slots < E;
+  std::vector<int32_t> slot_of(E), owner(E, -1);
+  if (!a.pool) {
+    if (cudaMemcpy(L->arena, L->master, (size_t)L->blob * E, cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+    for (int e = 0; e < E; ++e) slot_of[e] = owner[e] = e;
+  } else {
+    for (int e = 0; e < E; ++e) slot_of[e] = -1;
+  }
+  std::vector<uint32_t> zeros(E, 0u);
+  if (cudaMemcpy(a.slot_of, slot_of.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(a.owner, owner.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(a.stamp, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(a.ready, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (a.pool) {
+    try {
+      L->server = std::thread(server_main, L);
+    } catch (...) {
+      return MOE_ERR_OUT_OF_MEMORY;
+    }
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_forward(moe_layer_t* L, const void* x, int32_t T, void* y, int32_t* topk_idx, float* topk_w,
+                         void* stream) {
+  if (!L || !x || !y) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > L->d.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)x & 15) || ((uintptr_t)y & 3)) return MOE_ERR_INVALID_ARG;
+  if (L->n_slots == 0) return MOE_ERR_STATE;
+  if (sticky_error(L)) return MOE_ERR_STATE;
+  DeviceGuard guard(L->d.device);
+  LayerArgs a = L->args;
+  a.T = T;
+  a.x = (const uint16_t*)x;
+  a.y = (uint16_t*)y;
+  if (topk_idx) a.topk_idx = topk_idx;
+  if (topk_w) a.topk_w = topk_w;
+  a.wait_timeout_ns = L->wait_timeout_ns;
+  cudaStream_t s = (cudaStream_t)stream;
+  const int Um = L->d.n_experts < T * L->d.top_k ? L->d.n_experts : T * L->d.top_k;
+  const int max_tasks = (L->d.n_shared + Um) * (L->d.inter / 16);
+  int gu_grid = L->sm_count * gateup_max_blocks_per_sm(T);
+  if (gu_grid > max_tasks) gu_grid = max_tasks;
+  int dn_grid = L->sm_count * down_max_blocks_per_sm(T);
+  if (dn_grid > L->d.hidden / 16) dn_grid = L->d.hidden / 16;
+  if (launch_route(a, s, true) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_gateup(a, s, true, gu_grid) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_down(a, s, true, dn_grid) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_residual_rmsnorm(const void* x, const void* y, int32_t T, int32_t hidden, float eps, void* x_out,
+                                  void* xhat, void* stream) {
+  if (!x || !xhat || T < 1 || hidden < 1 || hidden > kMaxHidden || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if (xhat == x || (y && xhat == y) || (x_out && xhat == x_out)) return MOE_ERR_INVALID_ARG;
+  if (launch_residual_rmsnorm((const uint16_t*)x, (const uint16_t*)y, T, hidden, eps, (uint16_t*)x_out,
+                              (uint16_t*)xhat, (cudaStream_t)stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_get_stats(moe_layer_t* L, moe_stats_t* out) {
+  if (!L || !out) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(L->d.device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  DevState ds;
+  if (cudaMemcpy(&ds, L->args.st, sizeof(ds), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  std::memset(out, 0, sizeof(*out));
+  out->forwards = ds.forwards;
+  out->hits = ds.hits;
+  out->misses = ds.misses;
+  out->h2d_bytes = L->h2d_bytes.load();
+  out->wait_ns = ds.wait_ns;
+  out->n_slots = L->n_slots;
+  int e = L->host_error.load();
+  if (!e) e = ds.error;
+  out->error = e;
+  return (moe_status_t)e;
+}
+
+moe_status_t moe_get_miss_log(moe_layer_t* L, int32_t* out, int64_t max, int64_t* n) {
+  if (!L || !n || (max > 0 && !out)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(L->d.device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  // the server may still be issuing the last entries: wait until it caught up
+  if (L->n_slots < L->d.n_experts) {
+    uint32_t head = 0;
+    cudaMemcpy(&head, &L->args.st->ring_head, 4, cudaMemcpyDeviceToHost);
+    for (int spin = 0; spin < 20000; ++spin) {
+      {
+        std::lock_guard<std::mutex> g(L->log_mu);
+        if (L->miss_log.size() / 3 >= head || L->paused.load()) break;
+      }
+      std::this_thread::sleep_for(std::chrono::microseconds(100));
+    }
+  }
+  std::lock_guard<std::mutex> g(L->log_mu);
+  const int64_t total = (int64_t)(L->miss_log.size() / 3);
+  *n = total;
+  const int64_t m = total < max ? total : max;
+  if (m > 0) std::memcpy(out, L->miss_log.data(), (size_t)m * 3 * sizeof(int32_t));
+  return MOE_OK;
+}
+
+moe_status_t moe_set_wait_timeout_ns(moe_layer_t* L, uint64_t ns) {
+  if (!L) return MOE_ERR_INVALID_ARG;
+  L->wait_timeout_ns = ns ? ns : 2000000000ull;
+  return MOE_OK;
+}
+
+moe_status_t moe_debug_copy_faults(moe_layer_t* L, int64_t fail_copy_n, int32_t pause) {
+  if (!L || fail_copy_n < 0) return MOE_ERR_INVALID_ARG;
+  L->copies_since_arm = 0;
+  L->fail_copy_n = fail_copy_n;
+  L->paused = pause != 0;
+  return MOE_OK;
+}
+
+void moe_destroy(moe_layer_t* L) {
+  if (!L) return;
+  DeviceGuard guard(L->d.device);
+  L->paused = false;
+  cudaDeviceSynchronize();
+  free_layer(L);
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_OUT_OF_MEMORY: return "out of memory";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_COPY: return "expert copy failed";
+    case MOE_ERR_TIMEOUT: return "timed out waiting for an expert copy";
+    case MOE_ERR_STATE: return "layer not ready or holding an earlier error";
+    case MOE_ERR_DEVICE: return "device-side check failed";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,63 @@
+"""Helpers shared by the GPU parity tests."""
+import numpy as np
+
+import oracle
+from quantized_expert_ffn_gemv_gb300 import synth
+
+REL_L2 = 2e-3   # per token row
+MAX_ABS = 5e-3  # every element
+W_RTOL = 1e-5   # routing weights (fp32 softmax vs binary64)
+
+
+def to_torch_bf16(x_u16, device="cuda"):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(x_u16).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def from_torch_bf16(t):
+    import torch
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def make_gpu_layer(L, max_tokens=1, n_slots=None, with_shared=True):
+    from quantized_expert_ffn_gemv_gb300 import moe
+    return moe.MoeLayer(L.shape, L.W_r, L.bias, L.experts, L.shared if with_shared else None,
+                        max_tokens=max_tokens, n_slots=n_slots)
+
+
+def run(layer, x_u16, T=None):
+    """Run the GPU layer on x in calls of T tokens; returns (y u16, idx, w)."""
+    import torch
+    n = x_u16.shape[0]
+    T = T or n
+    k = layer.shape.k
+    y = np.empty_like(x_u16)
+    idx = np.empty((n, k), np.int32)
+    w = np.empty((n, k), np.float32)
+    xd = to_torch_bf16(x_u16)
+    yd = torch.empty_like(xd)
+    idd = torch.empty((n, k), dtype=torch.int32, device="cuda")
+    wd = torch.empty((n, k), dtype=torch.float32, device="cuda")
+    for t0 in range(0, n, T):
+        t1 = min(n, t0 + T)
+        layer.forward(xd[t0:t1], yd[t0:t1], idd[t0:t1], wd[t0:t1])
+    torch.cuda.synchronize()
+    y[:] = from_torch_bf16(yd)
+    idx[:] = idd.cpu().numpy()
+    w[:] = wd.cpu().numpy()
+    return y, idx, w
+
+
+def check_against_oracle(L, x_u16, y, idx, w, rows=None):
+    sh = L.shape
+    rows = np.arange(x_u16.shape[0]) if rows is None else np.asarray(rows)
+    ref = oracle.moe_forward(sh.H, sh.I, sh.E, sh.k, L.W_r, L.bias, L.experts, L.shared, x_u16[rows])
+    assert np.array_equal(idx[rows], ref["idx"]), "routing differs from the oracle"
+    assert np.allclose(w[rows], ref["w"], rtol=W_RTOL, atol=1e-7)
+    yg = synth.bf16_to_f32(y[rows]).astype(np.float64)
+    r = ref["y"]
+    err = yg - r
+    rel = np.linalg.norm(err, axis=1) / np.linalg.norm(r, axis=1)
+    assert rel.max() <= REL_L2, f"rel-L2 {rel.max():.3e}"
+    assert np.abs(err).max() <= MAX_ABS, f"max-abs {np.abs(err).max():.3e}"
+    return rel.max(), np.abs(err).max()

@@ -1,0 +1,65 @@
+"""The VRAM expert-slot pool on the GPU: misses match the LRU simulator,
+output is bit-identical to the all-resident run, and copy failures or a
+stalled copy server end in an error status (no GPU fault, no hang)."""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_expert_ffn_gemv_gb300 import synth
+from tests.gpu_common import check_against_oracle, make_gpu_layer, run
+from tests.inputs import resampled_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def small():
+    return synth.make_layer(synth.SMALL, layer=0)
+
+
+@pytest.mark.parametrize("T,S", [(1, 16), (4, 20)])
+def test_pool_is_residency_invariant_and_matches_lru(small, T, S):
+    x, _ = resampled_tokens(small, 500, 96)
+    full = make_gpu_layer(small, max_tokens=T)
+    y0, i0, w0 = run(full, x, T=T)
+    pool = make_gpu_layer(small, max_tokens=T, n_slots=S)
+    y1, i1, w1 = run(pool, x, T=T)
+    assert np.array_equal(y0, y1) and np.array_equal(i0, i1) and np.array_equal(w0, w1)
+    steps = [sorted(set(i1[t0:t0 + T].ravel().tolist())) for t0 in range(0, 96, T)]
+    expect, _ = oracle.pool_sim(small.shape.E, S, steps)
+    got = pool.miss_log()
+    assert np.array_equal(got, expect)
+    stats, code = pool.stats()
+    assert code == 0
+    assert stats["misses"] == len(expect)
+    assert stats["hits"] + stats["misses"] == sum(len(s) for s in steps)
+    assert stats["h2d_bytes"] == len(expect) * small.shape.expert_bytes
+    check_against_oracle(small, x, y1, i1, w1, rows=np.arange(0, 96, 12))
+    pool.close()
+    full.close()
+
+
+def test_failed_copy_is_an_error_not_zero_weights(small):
+    from quantized_expert_ffn_gemv_gb300 import moe
+    x, _ = resampled_tokens(small, 700, 8)
+    pool = make_gpu_layer(small, max_tokens=1, n_slots=8)
+    pool.debug_copy_faults(fail_copy_n=3)
+    with pytest.raises(moe.MoeError) as ei:
+        run(pool, x, T=1)
+        run(pool, x, T=1)
+    assert ei.value.code == 7  # sticky
+    stats, code = pool.stats()
+    assert code == 5 and stats["error"] == 5
+    pool.close()
+
+
+def test_stalled_copy_server_times_out(small):
+    x, _ = resampled_tokens(small, 800, 1)
+    pool = make_gpu_layer(small, max_tokens=1, n_slots=8)
+    pool.set_wait_timeout_ns(200_000_000)
+    pool.debug_copy_faults(pause=True)
+    run(pool, x, T=1)  # the cold pool misses; nothing serves the doorbell
+    stats, code = pool.stats()
+    assert code == 6 and stats["error"] == 6 and stats["wait_ns"] >= 150_000_000
+    pool.debug_copy_faults(pause=False)
+    pool.close()
