@@ -60,12 +60,12 @@ def check_against_oracle(L, x_u16, y, idx, w, rows=None):
     rel = np.linalg.norm(err, axis=1) / np.linalg.norm(r, axis=1)
     assert rel.max() <= REL_L2, f"rel-L2 {rel.max():.3e}"
     assert np.abs(err).max() <= MAX_ABS, f"max-abs {np.abs(err).max():.3e}"
-    # stronger: every element lies within half a bf16 ulp of the oracle value
-    # (the rounding itself) plus a slack of 1e-4 of the row's largest value
-    # for the fp32 accumulation and the fp16 intermediate
+    # per element: the output's own bf16 rounding (half an ulp of the oracle
+    # value) plus the fp16 rounding of the intermediate h (relative RMS about
+    # 2e-4, so 2e-3 of the row RMS is a 7-sigma bound)
     mag = np.abs(r)
     e = np.floor(np.log2(np.maximum(mag, 1e-30)))
     half_ulp = np.ldexp(1.0, (e - 8).astype(np.int64))
-    slack = 1e-4 * mag.max(axis=1, keepdims=True)
+    slack = 2e-3 * np.sqrt((r * r).mean(axis=1, keepdims=True))
     assert np.all(np.abs(err) <= half_ulp + slack), f"{(np.abs(err) > half_ulp + slack).sum()} elements off"
     return rel.max(), np.abs(err).max()
