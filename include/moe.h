@@ -202,6 +202,30 @@ MOE_API moe_status_t moe_debug_copy_faults(moe_layer_t* layer, int64_t fail_copy
 /* Destroy: synchronizes, stops the copy server, frees library memory. NULL-safe. */
 MOE_API void moe_destroy(moe_layer_t* layer);
 
+/*
+ * Router + top-k for callers that cannot allocate device memory (no
+ * counterpart in the source pages; see moe_noalloc.cu for which callers).
+ * Computes, like moe_forward's routing step, the logits router_w x +
+ * router_bias, the k largest per token (ties to the lower index) in
+ * ascending expert order, and their softmax weights renormalised over the
+ * k, writing topk_idx [T][k] (int32) and topk_w [T][k] (fp32), on the
+ * current device and the given stream.
+ *   router_w: device fp32 [E][H], 16-byte aligned; router_bias: device fp32
+ *   [E] or NULL; x_bf16: device bf16 [T][H].
+ * Scratch: a fixed 256 KiB device array inside the library (T * E <= 65536
+ * logits), shared by every call on a device and kept by it until the
+ * process exits.  Nothing is allocated, ever.  The first call on a device
+ * sets the array up (resolves its device address, clears its ticket):
+ * make that first call before any stream capture.  Calls that overlap on
+ * the GPU race on the array: serialize them.
+ * Errors: INVALID_ARG (NULL or misaligned pointers, bad shapes),
+ * UNSUPPORTED (T > 64, k > 16, H > 4096, E > 4096 or T * E > 65536),
+ * CUDA (set-up or launch failure).
+ */
+MOE_API moe_status_t moe_route_noalloc(const float* router_w, const float* router_bias, const void* x_bf16, int32_t T,
+                                       int32_t hidden, int32_t n_experts, int32_t top_k, int32_t* topk_idx,
+                                       float* topk_w, void* cuda_stream);
+
 MOE_API const char* moe_status_string(moe_status_t status);
 
 #ifdef __cplusplus

@@ -17,7 +17,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
           4: "MOE_ERR_CUDA", 5: "MOE_ERR_COPY", 6: "MOE_ERR_TIMEOUT", 7: "MOE_ERR_STATE", 8: "MOE_ERR_DEVICE"}
 EXPORTS = ["moe_expert_bytes", "moe_repack_expert", "moe_unpack_expert", "moe_layer_create",
            "moe_slot_pool_configure", "moe_forward", "moe_residual_rmsnorm", "moe_get_stats", "moe_get_miss_log",
-           "moe_set_wait_timeout_ns", "moe_debug_copy_faults", "moe_destroy", "moe_status_string"]
+           "moe_set_wait_timeout_ns", "moe_debug_copy_faults", "moe_destroy", "moe_status_string",
+           "moe_route_noalloc"]
 
 
 class MoeError(RuntimeError):
@@ -66,6 +67,7 @@ def lib(build_if_missing=False):
         L.moe_debug_copy_faults.argtypes = [p, i64, i32]
         L.moe_destroy.argtypes = [p]
         L.moe_destroy.restype = None
+        L.moe_route_noalloc.argtypes = [p, p, p, i32, i32, i32, i32, p, p, p]
         L.moe_status_string.argtypes = [C.c_int]
         L.moe_status_string.restype = C.c_char_p
         for f in EXPORTS:
@@ -118,6 +120,14 @@ def residual_rmsnorm(x, y, eps, x_out, xhat, stream=None):
     check(lib().moe_residual_rmsnorm(x.data_ptr(), None if y is None else y.data_ptr(), T, H, eps,
                                      None if x_out is None else x_out.data_ptr(), xhat.data_ptr(),
                                      _stream_ptr(stream)), "moe_residual_rmsnorm")
+
+
+def route_noalloc(W_r, bias, x, k, topk_idx, topk_w, stream=None):
+    """Router + top-k without any device allocation (torch CUDA tensors)."""
+    T, H = x.shape
+    check(lib().moe_route_noalloc(W_r.data_ptr(), None if bias is None else bias.data_ptr(), x.data_ptr(), T, H,
+                                  W_r.shape[0], k, topk_idx.data_ptr(), topk_w.data_ptr(), _stream_ptr(stream)),
+          "moe_route_noalloc")
 
 
 class MoeLayer:
