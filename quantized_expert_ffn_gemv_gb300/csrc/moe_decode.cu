@@ -1,0 +1,1067 @@
+// Fused decode kernel (T <= 8 tokens per call): the whole MoE layer in one
+// cooperative launch of one CTA per SM, 16 warps.
+//
+// Weights stream through shared-memory rings filled with 1-D TMA bulk copies
+// (cp.async.bulk + mbarrier); lane 0 of warp 15 is the producer and keeps
+// refilling the rings whenever it would otherwise wait.
+//
+//   prologue   this CTA's router rows, its shared-expert gate/up strip and
+//              down strip start loading; x -> fp16 in B-fragment order.
+//   router     fp32 dot products -> logits, each stored with the step number
+//              in one 64-bit word; readers poll for the tag (no grid barrier).
+//   routing    every CTA redundantly: top-k per token as a warp tournament
+//              (redux max over order-preserving keys) and a merge of the
+//              warps' lists, ascending expert order, softmax
+//              weights renormalised over the k, the union of selected experts
+//              and the (expert, token) pair lists, the slot hit check and LRU
+//              victims (double-buffered pool state; CTA 0 writes the next
+//              state and rings the host doorbell).  Betelgeuse news page,
+//              section 机制, 调度 row: the hit check runs in-stream on the GPU.
+//   gate/up    four warps per 16-row strip (K split four ways), one strip per
+//              ring stage at once; h = silu(g) * u goes to global as fp16 and the
+//              expert's completion counter (double-buffered by step parity)
+//              is bumped with a release reduction.
+//   down       warp w handles selected experts w, w + ds, ...: waits for the
+//              expert's counter, z = W_d h for this CTA's 16 output rows;
+//              then y = sum_j w_j z_j (ascending expert) + z_shared in fp32,
+//              rounded once to bf16.
+#include <cfloat>
+#include <climits>
+
+#include "moe.h"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kWarps = 16;
+constexpr int kGroupWarps = 4;             // warps per gate/up strip
+constexpr int kProdWarp = 15;
+constexpr int kMaxT = 8;
+constexpr int kMaxE = 1024;
+constexpr int kRtVec = kMaxHidden / 256;   // float4 per lane per half router row
+constexpr int kMaxGuStages = 4;
+constexpr int kMaxDnStages = 16;
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ int ld_cg_i32(const int* p) {
+  int r;
+  asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint4 ld_cg4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t ld_acquire_gpu_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// GPU-layout word (8 nibbles) -> the 4 f16x2 registers of an A fragment (q = u - 8).
+__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&a)[4]) {
+  const uint32_t lo0 = (w & 0x000F000Fu) | 0x64006400u;
+  const uint32_t hi0 = (w & 0x00F000F0u) | 0x64006400u;
+  const uint32_t w8 = w >> 8;
+  const uint32_t lo1 = (w8 & 0x000F000Fu) | 0x64006400u;
+  const uint32_t hi1 = (w8 & 0x00F000F0u) | 0x64006400u;
+  const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
+  const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
+  const __half2 km72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));
+  __half2 r0 = __hsub2(*reinterpret_cast<const __half2*>(&lo0), k1032);
+  __half2 r1 = __hsub2(*reinterpret_cast<const __half2*>(&lo1), k1032);
+  __half2 r2 = __hfma2(*reinterpret_cast<const __half2*>(&hi0), k16th, km72);
+  __half2 r3 = __hfma2(*reinterpret_cast<const __half2*>(&hi1), k16th, km72);
+  a[0] = *reinterpret_cast<uint32_t*>(&r0);
+  a[1] = *reinterpret_cast<uint32_t*>(&r1);
+  a[2] = *reinterpret_cast<uint32_t*>(&r2);
+  a[3] = *reinterpret_cast<uint32_t*>(&r3);
+}
+
+__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFF))); }
+__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
+
+// One 16 x 64 super-tile times one n8 activation group, exact fp32 block scaling.
+__device__ __forceinline__ void supertile_mma(float (&acc)[4], const uint4& nib, const uint2& sc, const uint4& b01,
+                                              const uint4& b23) {
+  const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
+  const uint32_t bb[4][2] = {{b01.x, b01.y}, {b01.z, b01.w}, {b23.x, b23.y}, {b23.z, b23.w}};
+  const float d[4] = {half_lo(sc.x), half_hi(sc.x), half_lo(sc.y), half_hi(sc.y)};
+#pragma unroll
+  for (int blk = 0; blk < 2; ++blk) {
+    float tmp[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t a[4];
+    dequant_word(words[2 * blk], a);
+    mma16816(tmp, a, bb[2 * blk][0], bb[2 * blk][1]);
+    dequant_word(words[2 * blk + 1], a);
+    mma16816(tmp, a, bb[2 * blk + 1][0], bb[2 * blk + 1][1]);
+    acc[0] = fmaf(d[2 * blk], tmp[0], acc[0]);
+    acc[1] = fmaf(d[2 * blk], tmp[1], acc[1]);
+    acc[2] = fmaf(d[2 * blk + 1], tmp[2], acc[2]);
+    acc[3] = fmaf(d[2 * blk + 1], tmp[3], acc[3]);
+  }
+}
+
+__device__ void set_error(const LayerArgs& a, int code) {
+  atomicCAS(&a.st->error, 0, code);
+  volatile int32_t* m = &a.hm->error;
+  if (*m == 0) *m = code;
+  __threadfence_system();
+}
+__device__ __forceinline__ int dev_error(const LayerArgs& a) { return ld_cg_i32(&a.st->error); }
+__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+// ------------------------------------------------------------------ shared memory plan
+
+struct Plan {
+  int rows_max, umax, gu_stages, dn_stages;
+  size_t bars, x16, xraw, regA, gu, dn, red, lists, total;
+};
+
+__host__ __device__ inline size_t al128(size_t v) { return (v + 127) & ~size_t(127); }
+
+__host__ __device__ inline Plan plan_with(int H, int I, int E, int k, int T, int G, int gs, int ds) {
+  Plan p;
+  p.rows_max = (E + G - 1) / G;
+  p.umax = E < T * k ? E : T * k;
+  p.gu_stages = gs;
+  p.dn_stages = ds;
+  size_t o = 0;
+  p.bars = o;
+  o += al128(8 * (2 * kMaxGuStages + 2 * kMaxDnStages + 2));
+  p.x16 = o;
+  o += al128((size_t)T * H * 2);
+  p.xraw = o;
+  o += al128((size_t)T * H * 2);
+  // region A: router rows (prologue), routing scratch, then down results
+  const size_t router = (size_t)p.rows_max * H * 4;
+  // tokmask [E], then (key, e) entries: 16 lists of kMaxTopK, merge candidates, selections
+  const size_t routing = al128((size_t)E * 8) + (size_t)4 * kWarps * kMaxTopK * 8;
+  const size_t zbuf = (size_t)(p.umax + 1) * 32 * 4 * 4;
+  size_t ra = router > routing ? router : routing;
+  ra = ra > zbuf ? ra : zbuf;
+  p.regA = o;
+  o += al128(ra);
+  p.gu = o;
+  o += (size_t)gs * al128((size_t)gu_strip_bytes(H));
+  p.dn = o;
+  o += (size_t)ds * al128((size_t)down_strip_bytes(I));
+  p.red = o;
+  o += al128((size_t)kWarps * 32 * 8 * 4);
+  p.lists = o;
+  o += al128((size_t)T * k * 4 * 5 + (size_t)(p.umax + 2) * 4 * 4 + 64 * 8);
+  p.total = o;
+  return p;
+}
+
+__host__ __device__ inline Plan make_plan(int H, int I, int E, int k, int T, int G, size_t limit) {
+  const int nex = (E < T * k ? E : T * k) + 1;
+  const int want_dn = nex < kMaxDnStages ? nex : kMaxDnStages;
+  const int gs_opts[4] = {3, 2, 2, 1};
+  const int ds_opts[4] = {want_dn, want_dn < 8 ? want_dn : 8, want_dn < 4 ? want_dn : 4, want_dn < 2 ? want_dn : 2};
+  Plan p = plan_with(H, I, E, k, T, G, gs_opts[0], ds_opts[0]);
+  for (int i = 1; i < 4 && p.total > limit; ++i) p = plan_with(H, I, E, k, T, G, gs_opts[i], ds_opts[i]);
+  return p;
+}
+
+struct Lists {
+  int* s_idx;
+  float* s_w;
+  int* tk_u;
+  int* tk_pos;
+  int* pair_token;
+  int* u_expert;
+  int* u_slot;
+  uint32_t* u_wait;
+  int* u_off;
+  unsigned long long* misc;
+};
+
+__device__ inline Lists carve_lists(unsigned char* base, int T, int k, int umax) {
+  Lists l;
+  int* p = reinterpret_cast<int*>(base);
+  const int P = T * k;
+  l.s_idx = p;
+  l.s_w = reinterpret_cast<float*>(p + P);
+  l.tk_u = p + 2 * P;
+  l.tk_pos = p + 3 * P;
+  l.pair_token = p + 4 * P;
+  l.u_expert = p + 5 * P;
+  l.u_slot = l.u_expert + (umax + 2);
+  l.u_wait = reinterpret_cast<uint32_t*>(l.u_slot + (umax + 2));
+  l.u_off = reinterpret_cast<int*>(l.u_wait + (umax + 2));
+  size_t off = (size_t)(5 * P + 4 * (umax + 2)) * 4;
+  off = (off + 7) & ~size_t(7);
+  l.misc = reinterpret_cast<unsigned long long*>(base + off);
+  return l;
+}
+
+// Expert list index xi: 0 = shared expert (when present), then routed u.
+struct Task {
+  const uint8_t* base;
+  int cnt, poff, slot;
+  uint32_t wait_seq;
+};
+
+__device__ __forceinline__ Task task_of(const LayerArgs& a, const Lists& L, int xi, int n_shared) {
+  Task t;
+  if (xi < n_shared) {
+    t.base = a.shared;
+    t.cnt = a.T;
+    t.poff = a.T * a.k;
+    t.wait_seq = 0u;
+    t.slot = 0;
+  } else {
+    const int u = xi - n_shared;
+    t.slot = L.u_slot[u];
+    t.base = a.arena + (int64_t)t.slot * a.blob;
+    t.poff = L.u_off[u];
+    t.cnt = L.u_off[u + 1] - t.poff;
+    t.wait_seq = L.u_wait[u];
+  }
+  return t;
+}
+
+// ------------------------------------------------------------------ producer
+
+struct Ring {
+  uint64_t *full_gu, *empty_gu, *full_dn, *empty_dn;
+  unsigned char *gu, *dn;
+  size_t gu_pitch, dn_pitch, gu_bytes, dn_bytes;
+  int gs, ds;
+};
+
+// Producer state (lane 0 of warp 15): next gate/up task and down entry to issue.
+struct Producer {
+  int m, d, n_gu, n_dn;
+  bool routed;
+  uint64_t t_wait0;  // when the producer started waiting for a slot copy (0: not waiting)
+};
+
+struct Ctx {
+  const LayerArgs* a;
+  const Ring* R;
+  const Lists* L;
+  int c, G, NS, NSh, H, I;
+};
+
+// Time spent waiting for slot copies, counted once (by CTA 0's producer).
+__device__ __forceinline__ void note_wait_end(Producer& P, const Ctx& x) {
+  if (P.t_wait0) {
+    if (x.c == 0) atomicAdd(&x.a->st->wait_ns, (unsigned long long)(global_ns() - P.t_wait0));
+    P.t_wait0 = 0;
+  }
+}
+
+// Issue every copy whose ring stage is free; never blocks.  A missed expert
+// is only issued once the copy server has published its slot.
+__device__ void pump(Producer& P, const Ctx& x) {
+  if (!P.routed) return;
+  const LayerArgs& a = *x.a;
+  const Ring& R = *x.R;
+  while (P.m < P.n_gu) {
+    const int s = P.m % R.gs;
+    if (P.m >= R.gs && !mbar_try_wait(&R.empty_gu[s], ((P.m / R.gs) - 1) & 1)) break;
+    const int t = x.c + x.G * P.m;
+    const Task tk = task_of(a, *x.L, t / x.NS, x.NSh);
+    if (tk.wait_seq) {
+      const uint32_t v = ld_acquire_sys(&a.ready[tk.slot]);
+      if (v == (tk.wait_seq | kReadyError)) { set_error(a, MOE_ERR_COPY); P.m = P.n_gu; P.d = P.n_dn; return; }
+      if (v != tk.wait_seq) {  // copy still in flight
+        if (!P.t_wait0) P.t_wait0 = global_ns();
+        break;
+      }
+      note_wait_end(P, x);
+    }
+    mbar_expect_tx(&R.full_gu[s], (uint32_t)R.gu_bytes);
+    bulk_g2s(R.gu + s * R.gu_pitch, tk.base + (size_t)(t % x.NS) * R.gu_bytes, (uint32_t)R.gu_bytes, &R.full_gu[s]);
+    ++P.m;
+  }
+  while (P.d < P.n_dn) {
+    const int s = P.d % R.ds;
+    if (P.d >= R.ds && !mbar_try_wait(&R.empty_dn[s], ((P.d / R.ds) - 1) & 1)) break;
+    const Task tk = task_of(a, *x.L, P.d, x.NSh);
+    if (tk.wait_seq) {
+      const uint32_t v = ld_acquire_sys(&a.ready[tk.slot]);
+      if (v == (tk.wait_seq | kReadyError)) { set_error(a, MOE_ERR_COPY); P.m = P.n_gu; P.d = P.n_dn; return; }
+      if (v != tk.wait_seq) {
+        if (!P.t_wait0) P.t_wait0 = global_ns();
+        break;
+      }
+      note_wait_end(P, x);
+    }
+    mbar_expect_tx(&R.full_dn[s], (uint32_t)R.dn_bytes);
+    bulk_g2s(R.dn + s * R.dn_pitch, tk.base + down_base(x.H, x.I) + (size_t)x.c * R.dn_bytes, (uint32_t)R.dn_bytes,
+             &R.full_dn[s]);
+    ++P.d;
+  }
+}
+
+// Bounded wait on an mbarrier phase; the producer lane keeps pumping while it
+// waits, so no warp ever waits on a copy that only it could issue.
+__device__ bool wait_full(uint64_t* bar, uint32_t parity, uint64_t deadline, bool is_prod, Producer& P,
+                          const Ctx& x) {
+  int spins = 0;
+  while (!mbar_try_wait(bar, parity)) {
+    if (is_prod) pump(P, x);
+    if (((++spins) & 31) == 0) {
+      if (global_ns() > deadline) { set_error(*x.a, MOE_ERR_TIMEOUT); return false; }
+      if (dev_error(*x.a)) return false;
+    }
+  }
+  return true;
+}
+
+
+// ------------------------------------------------------------------ top-k
+
+// Order-preserving key of a finite float (never 0), and its inverse.
+__device__ __forceinline__ uint32_t fkey(float v) {
+  const uint32_t u = __float_as_uint(v);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// (key, e) ranks before (key2, e2): larger logit, or equal logit and lower index
+__device__ __forceinline__ bool before(uint32_t key, int e, uint32_t key2, int e2) {
+  return key > key2 || (key == key2 && e < e2);
+}
+
+// Poll one tagged logit until it carries this step's tag.
+__device__ __forceinline__ float wait_logit(const unsigned long long* p, uint32_t seq, const LayerArgs& a,
+                                            uint64_t deadline) {
+  unsigned long long v = ld_relaxed_u64(p);
+  int spins = 0;
+  while ((uint32_t)(v >> 32) != seq) {
+    if (((++spins) & 63) == 0 && global_ns() > deadline) {
+      set_error(a, MOE_ERR_TIMEOUT);
+      break;
+    }
+    v = ld_relaxed_u64(p);
+  }
+  return __uint_as_float((uint32_t)v);
+}
+
+// The top k of this warp's range [base, base + range) in rank order, written
+// to out[0..k) as (key, expert); key 0 marks "none".  CPL keys per lane.
+template <int CPL>
+__device__ void warp_topk(const unsigned long long* logits, int E, int k, int base, int range, uint32_t seq,
+                          uint2* out, const LayerArgs& a, uint64_t deadline) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[CPL];
+#pragma unroll
+  for (int j = 0; j < CPL; ++j) {
+    const int e = base + lane + 32 * j;
+    key[j] = (lane + 32 * j < range && e < E) ? fkey(wait_logit(logits + e, seq, a, deadline)) : 0u;
+  }
+  if (CPL == 1) {
+    // exact rank inside the warp from 32 independent shuffles
+    const int e = base + lane;
+    int r = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const uint32_t ki = __shfl_sync(0xffffffffu, key[0], i);
+      r += (ki != 0u) && before(ki, base + i, key[0], e);
+    }
+    if (key[0] != 0u && r < k) out[r] = make_uint2(key[0], (uint32_t)e);
+    const int n = __popc(__ballot_sync(0xffffffffu, key[0] != 0u));
+    if (lane >= n && lane < k) out[lane] = make_uint2(0u, 0u);
+    return;
+  }
+  // k rounds of a warp max; equal keys -> lowest j, then lowest lane
+  uint32_t taken = 0u;
+  for (int r = 0; r < k; ++r) {
+    uint32_t my = 0u;
+    int myj = CPL;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j)
+      if (key[j] != 0u && !((taken >> j) & 1u) && (key[j] > my || myj == CPL)) { my = key[j]; myj = j; }
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, my);
+    const uint32_t jmin = __reduce_min_sync(0xffffffffu, (mx != 0u && my == mx) ? (uint32_t)myj : 0xFFFFu);
+    const uint32_t ball = __ballot_sync(0xffffffffu, mx != 0u && my == mx && (uint32_t)myj == jmin);
+    const int wl = ball ? __ffs(ball) - 1 : 0;
+    if (lane == wl && ball) taken |= 1u << myj;
+    if (lane == 0) out[r] = make_uint2(ball ? mx : 0u, (uint32_t)(base + wl + 32 * (int)(jmin & 0xFF)));
+  }
+}
+
+// Merge one token's nl rank-ordered lists (nl <= 16, k entries each): the
+// k-th largest list head is a lower bound of the token's k-th largest key, so
+// only entries at or above it can be selected; those are ranked exactly.
+// Writes the selection in ascending expert order with renormalised softmax
+// weights, and marks the token in tokmask.
+__device__ void merge_topk(const uint2* lists, int nl, int k, const Lists& L, unsigned long long* tokmask, int t,
+                           bool write_out, const LayerArgs& a) {
+  const int lane = threadIdx.x & 31;
+  // threshold: k-th largest of the list heads (k <= nl); else take everything
+  uint2 hd = (lane < nl) ? lists[lane * kMaxTopK] : make_uint2(0u, 0u);
+  uint32_t thr = 0u;
+  if (k <= nl) {
+    int r = 0;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t ki = __shfl_sync(0xffffffffu, hd.x, i);
+      const int ei = (int)__shfl_sync(0xffffffffu, hd.y, i);
+      r += (i < nl) && (ki != 0u) && before(ki, ei, hd.x, (int)hd.y);
+    }
+    const unsigned b = __ballot_sync(0xffffffffu, lane < nl && hd.x != 0u && r == k - 1);
+    thr = b ? __shfl_sync(0xffffffffu, hd.x, __ffs(b) - 1) : 0u;
+  }
+  // gather the entries >= thr (each list is sorted: a prefix of it)
+  int cnt = 0;
+  if (lane < nl) {
+    uint32_t kk[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) kk[j] = (j < k) ? lists[lane * kMaxTopK + j].x : 0u;
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) cnt += (kk[j] != 0u && kk[j] >= thr);
+  }
+  int inc = cnt;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += v;
+  }
+  const int total = __shfl_sync(0xffffffffu, inc, 31);
+  uint2* cand = const_cast<uint2*>(lists) + 16 * kMaxTopK;  // scratch after the lists
+  for (int j = 0; j < cnt; ++j) cand[inc - cnt + j] = lists[lane * kMaxTopK + j];
+  __syncwarp();
+  // exact ranks of the candidates, scattered by rank into cand_sel
+  uint2* cand_sel = cand + 16 * kMaxTopK;
+  if (total <= 32) {
+    const uint2 me = (lane < total) ? cand[lane] : make_uint2(0u, 0xFFFFFFFFu);
+    int r = 0;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint32_t xj = __shfl_sync(0xffffffffu, me.x, j), yj = __shfl_sync(0xffffffffu, me.y, j);
+      r += (j < total) && before(xj, (int)yj, me.x, (int)me.y);
+    }
+    if (lane < total && r < k) cand_sel[r] = me;
+  } else {
+    for (int i = lane; i < total; i += 32) {
+      const uint2 me = cand[i];
+      int r = 0;
+      for (int j = 0; j < total; ++j) r += before(cand[j].x, (int)cand[j].y, me.x, (int)me.y);
+      if (r < k) cand_sel[r] = me;
+    }
+  }
+  __syncwarp();
+  const uint2 sel = (lane < k) ? cand_sel[lane] : make_uint2(0u, 0u);
+  // ascending expert order; softmax over the k renormalised (max = rank 0)
+  const int my_e = (lane < k) ? (int)sel.y : INT_MAX;
+  const float v = (lane < k) ? fkey_value(sel.x) : 0.f;
+  int pos = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) pos += (j < k) && (__shfl_sync(0xffffffffu, my_e, j) < my_e);
+  const float m = __shfl_sync(0xffffffffu, v, 0);
+  float vs = 0.f;
+  int es = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    const int pj = __shfl_sync(0xffffffffu, pos, j);
+    const float vj = __shfl_sync(0xffffffffu, v, j);
+    const int ej = __shfl_sync(0xffffffffu, my_e, j);
+    if (j < k && lane == pj) { vs = vj; es = ej; }
+  }
+  float ex[kMaxTopK];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) ex[j] = expf(__shfl_sync(0xffffffffu, vs, j) - m);
+  float z = 0.f;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < k) z += ex[j];
+  if (lane < k) {
+    const float wj = expf(vs - m) / z;
+    L.s_idx[t * k + lane] = es;
+    L.s_w[t * k + lane] = wj;
+    if (write_out) {
+      a.topk_idx[t * k + lane] = es;
+      a.topk_w[t * k + lane] = wj;
+    }
+    atomicOr(&tokmask[es], 1ull << t);
+  }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsigned long long* tagged_logits,
+                                                             int32_t* pool_state, size_t smem_limit) {
+  extern __shared__ __align__(128) unsigned char sm[];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, t4 = lane & 3;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int H = a.H, I = a.I, E = a.E, k = a.k, T = a.T, NS = I / 16, NSh = a.n_shared;
+  const Plan PL = make_plan(H, I, E, k, T, G, smem_limit);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PL.bars);
+  Ring R;
+  R.full_gu = bars;
+  R.empty_gu = bars + kMaxGuStages;
+  R.full_dn = bars + 2 * kMaxGuStages;
+  R.empty_dn = bars + 2 * kMaxGuStages + kMaxDnStages;
+  uint64_t* full_rt = bars + 2 * kMaxGuStages + 2 * kMaxDnStages;
+  R.gu = sm + PL.gu;
+  R.dn = sm + PL.dn;
+  R.gu_bytes = (size_t)gu_strip_bytes(H);
+  R.dn_bytes = (size_t)down_strip_bytes(I);
+  R.gu_pitch = al128(R.gu_bytes);
+  R.dn_pitch = al128(R.dn_bytes);
+  R.gs = PL.gu_stages;
+  R.ds = PL.dn_stages;
+  __half* x16 = reinterpret_cast<__half*>(sm + PL.x16);
+  uint16_t* xraw = reinterpret_cast<uint16_t*>(sm + PL.xraw);
+  float* wrows = reinterpret_cast<float*>(sm + PL.regA);
+  float* red = reinterpret_cast<float*>(sm + PL.red);
+  const Lists L = carve_lists(sm + PL.lists, T, k, PL.umax);
+  __shared__ uint32_t s_seq;
+  __shared__ int s_nunion, s_nmiss;
+  const uint64_t deadline = global_ns() + a.wait_timeout_ns;
+  const bool is_prod = (warp == kProdWarp && lane == 0);
+  const Ctx X{&a, &R, &L, c, G, NS, NSh, H, I};
+  Producer P;
+  P.m = 0;
+  P.d = 0;
+  P.n_gu = 0;
+  P.n_dn = 0;
+  P.routed = false;
+  P.t_wait0 = 0;
+
+  const int r0 = (int)((long long)c * E / G), r1 = (int)((long long)(c + 1) * E / G);
+  const int nrows = r1 - r0;
+  const bool has_dn = c < H / 16;
+  const bool pre_gu = NSh && c < NS;  // task 0 of this CTA is a shared-expert strip, loaded early
+
+  if (tid == 0) {
+    for (int s = 0; s < R.gs; ++s) { mbar_init(&R.full_gu[s], 1); mbar_init(&R.empty_gu[s], kGroupWarps); }
+    for (int s = 0; s < R.ds; ++s) { mbar_init(&R.full_dn[s], 1); mbar_init(&R.empty_dn[s], 1); }
+    mbar_init(full_rt, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_seq = (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.st->step)) + 1u;
+  }
+  __syncthreads();
+  const uint32_t seq = s_seq;
+  uint32_t* cnt_cur = a.counters + (size_t)(seq & 1u) * a.cnt_stride;
+  uint32_t* cnt_next = a.counters + (size_t)((seq + 1u) & 1u) * a.cnt_stride;
+
+  // ---- prologue: weights that do not depend on this call's input
+  if (is_prod) {
+    if (nrows > 0) {
+      mbar_expect_tx(full_rt, (uint32_t)(nrows * H * 4));
+      bulk_g2s(wrows, a.W_r + (size_t)r0 * H, (uint32_t)(nrows * H * 4), full_rt);
+    }
+    if (pre_gu) {
+      mbar_expect_tx(&R.full_gu[0], (uint32_t)R.gu_bytes);
+      bulk_g2s(R.gu, a.shared + (size_t)c * R.gu_bytes, (uint32_t)R.gu_bytes, &R.full_gu[0]);
+      P.m = 1;
+    }
+    if (NSh && has_dn) {
+      mbar_expect_tx(&R.full_dn[0], (uint32_t)R.dn_bytes);
+      bulk_g2s(R.dn, a.shared + down_base(H, I) + (size_t)c * R.dn_bytes, (uint32_t)R.dn_bytes, &R.full_dn[0]);
+      P.d = 1;
+    }
+  }
+  // x -> fp16 in B-fragment order (this CTA's own copy)
+  {
+    int bad = 0;
+    for (int o = tid; o < T * H / 8; o += kThreads) {
+      const int t = o / (H / 8), k8 = (o % (H / 8)) * 8;
+      const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)t * H + k8);
+      *reinterpret_cast<uint4*>(xraw + t * H + k8) = v;
+      const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float f0 = __uint_as_float(vv[i] << 16), f1 = __uint_as_float(vv[i] & 0xFFFF0000u);
+        bad |= !(fabsf(f0) < 65504.f) | !(fabsf(f1) < 65504.f);
+        *reinterpret_cast<__half2*>(x16 + t * H + frag_pos(k8 + 2 * i)) = __floats2half2_rn(f0, f1);
+      }
+    }
+    if (bad) set_error(a, MOE_ERR_DEVICE);
+  }
+  __syncthreads();
+
+  // ---- router: two warps per row (one per half), the same summation order
+  // as the batched path's router; bf16 x read exactly (shared-memory copy)
+  {
+    float* part = red;  // [16 warps][kMaxT]
+    const int row = warp >> 1, half = warp & 1;
+    if (nrows > 0) {
+      int spins = 0;
+      while (!mbar_try_wait(full_rt, 0)) {
+        if (((++spins) & 31) == 0 && global_ns() > deadline) { set_error(a, MOE_ERR_TIMEOUT); break; }
+      }
+    }
+    if (row < nrows) {
+      const float* wr = wrows + (size_t)row * H + half * (H / 2);
+      for (int t = 0; t < T; ++t) {
+        const uint16_t* xr = xraw + t * H + half * (H / 2);
+        uint2 xv[kRtVec];
+#pragma unroll
+        for (int i = 0; i < kRtVec; ++i) {
+          const int q = lane + 32 * i;
+          xv[i] = (q < H / 8) ? *reinterpret_cast<const uint2*>(xr + 4 * q) : make_uint2(0u, 0u);
+        }
+        float s = 0.f;
+#pragma unroll
+        for (int i = 0; i < kRtVec; ++i) {
+          const int q = lane + 32 * i;
+          if (q < H / 8) {
+            const float4 wv = *reinterpret_cast<const float4*>(wr + 4 * q);
+            s = fmaf(wv.x, __uint_as_float(xv[i].x << 16), s);
+            s = fmaf(wv.y, __uint_as_float(xv[i].x & 0xFFFF0000u), s);
+            s = fmaf(wv.z, __uint_as_float(xv[i].y << 16), s);
+            s = fmaf(wv.w, __uint_as_float(xv[i].y & 0xFFFF0000u), s);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) part[warp * kMaxT + t] = s;
+      }
+    }
+    __syncthreads();
+    if (tid < nrows * T) {
+      const int rr = tid / T, t = tid % T, e = r0 + rr;
+      const float l = part[(2 * rr) * kMaxT + t] + part[(2 * rr + 1) * kMaxT + t];
+      const float v = l + (a.bias ? __ldg(a.bias + e) : 0.f);
+      // value and step number in one 64-bit word: a reader that sees this
+      // step's tag sees this step's value (no fence, no grid barrier)
+      st_relaxed_u64(&tagged_logits[(size_t)t * E + e], ((unsigned long long)seq << 32) | __float_as_uint(v));
+    }
+  }
+
+  // ---- gate/up of one strip by a group of four warps (K split four ways)
+  auto gateup_task = [&](int m) {
+    const int grp = warp / kGroupWarps, wg = warp % kGroupWarps;
+    const int s = m % R.gs;
+    const int t_gu = c + G * m;
+    const int xi = t_gu / NS, strip = t_gu % NS;
+    const Task tk = task_of(a, L, xi, NSh);
+    const int col_tok = (g < tk.cnt) ? (xi < NSh ? g : L.pair_token[tk.poff + g]) : 0;
+    const bool ok = wait_full(&R.full_gu[s], (m / R.gs) & 1, deadline, is_prod, P, X);
+    float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
+    const int nst = H / 64;
+    if (ok) {
+      const unsigned char* sb = R.gu + s * R.gu_pitch;
+      for (int st = wg; st < nst; st += kGroupWarps) {
+        const __half* xr = x16 + col_tok * H + st * 64 + t4 * 16;
+        const uint4 b01 = *reinterpret_cast<const uint4*>(xr);
+        const uint4 b23 = *reinterpret_cast<const uint4*>(xr + 8);
+        const uint4 ng4 = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
+        const uint2 gsc = *reinterpret_cast<const uint2*>(sb + 8 * H + st * 64 + g * 8);
+        const uint4 nu4 = *reinterpret_cast<const uint4*>(sb + 9 * H + st * 512 + lane * 16);
+        const uint2 usc = *reinterpret_cast<const uint2*>(sb + 17 * H + st * 64 + g * 8);
+        supertile_mma(accg, ng4, gsc, b01, b23);
+        supertile_mma(accu, nu4, usc, b01, b23);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&R.empty_gu[s]);
+    float4* dst = reinterpret_cast<float4*>(red + (warp * 32 + lane) * 8);
+    dst[0] = make_float4(accg[0], accg[1], accg[2], accg[3]);
+    dst[1] = make_float4(accu[0], accu[1], accu[2], accu[3]);
+    named_sync(1 + grp, kGroupWarps * 32);
+    if (wg == 0) {
+      float gsum[4] = {0.f, 0.f, 0.f, 0.f}, usum[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int w = 0; w < kGroupWarps; ++w) {
+        const float4* src = reinterpret_cast<const float4*>(red + ((grp * kGroupWarps + w) * 32 + lane) * 8);
+        const float4 p = src[0], q = src[1];
+        gsum[0] += p.x; gsum[1] += p.y; gsum[2] += p.z; gsum[3] += p.w;
+        usum[0] += q.x; usum[1] += q.y; usum[2] += q.z; usum[3] += q.w;
+      }
+#pragma unroll
+      for (int cc = 0; cc < 4; ++cc) {
+        const int rowin = (cc < 2) ? g : g + 8;
+        const int col = 2 * t4 + (cc & 1);
+        if (col < tk.cnt)
+          a.h16[(size_t)(tk.poff + col) * I + frag_pos(strip * 16 + rowin)] =
+              __float2half_rn(silu(gsum[cc]) * usum[cc]);
+      }
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) red_release_add(&cnt_cur[xi], 1u);
+    }
+    named_sync(1 + grp, kGroupWarps * 32);
+  };
+
+
+
+  // ---- routing, redundantly in every CTA
+  unsigned long long* tokmask = reinterpret_cast<unsigned long long*>(sm + PL.regA);
+  uint2* wlist = reinterpret_cast<uint2*>(sm + PL.regA + al128((size_t)E * 8));  // [16 warps][kMaxTopK] (key, e)
+  for (int e = tid; e < E; e += kThreads) tokmask[e] = 0ull;
+  if (c == 0)  // the other parity's counters, for the next call
+    for (int i = tid; i < a.cnt_stride; i += kThreads) cnt_next[i] = 0u;
+  {
+    // warps per token: 16, 8, 4 or 2 for T = 1, 2, 3-4, 5-8; each warp takes a
+    // contiguous range of E / wpt experts, cpl per lane (e = base + lane + 32 j)
+    const int wpt = T == 1 ? 16 : (T == 2 ? 8 : (T <= 4 ? 4 : 2));
+    const int t = warp / wpt, wt = warp % wpt;
+    const int range = (E + wpt - 1) / wpt;
+    const int cpl = (range + 31) / 32;
+    const int base = wt * range;
+    if (t < T) {
+      if (cpl == 1)
+        warp_topk<1>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
+      else if (cpl <= 2)
+        warp_topk<2>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
+      else if (cpl <= 4)
+        warp_topk<4>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
+      else if (cpl <= 8)
+        warp_topk<8>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
+      else
+        warp_topk<16>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
+    }
+    __syncthreads();
+    if (warp < T) merge_topk(wlist + warp * wpt * kMaxTopK, wpt, k, L, tokmask, warp, c == 0, a);
+  }
+  __syncthreads();
+  // union of the selected experts (ascending) and pair offsets, from the
+  // T*k selected pairs: entry p is the first of its expert when no earlier
+  // token selected it.  One token: the union is the selection itself.
+  if (T == 1) {
+    if (tid < k) {
+      const int e = L.s_idx[tid];
+      L.u_expert[tid] = e;
+      L.u_off[tid] = tid;
+      L.u_slot[tid] = e;  // all-resident slot; the pool path overwrites it
+      L.u_wait[tid] = 0u;
+      L.pair_token[tid] = 0;
+      L.tk_u[tid] = tid;
+      L.tk_pos[tid] = 0;
+    }
+    if (tid == 0) {
+      L.u_off[k] = k;
+      s_nunion = k;
+    }
+  } else {
+    const int P = T * k;
+    int first = 0, ue = 0, po = 0, pos = 0, e = 0, t = 0;
+    if (tid < P) {
+      e = L.s_idx[tid];
+      t = tid / k;
+      const unsigned long long below = tokmask[e] & ((1ull << t) - 1ull);
+      first = below == 0ull;
+      pos = __popcll(below);
+      for (int q = 0; q < P; ++q) {
+        const int eq = L.s_idx[q];
+        if (eq < e) {
+          ++po;
+          ue += (tokmask[eq] & ((1ull << (q / k)) - 1ull)) == 0ull;
+        }
+      }
+    }
+    const int n_u = __syncthreads_count(first);
+    if (tid < P) {
+      if (first) {
+        L.u_expert[ue] = e;
+        L.u_off[ue] = po;
+        L.u_slot[ue] = e;
+        L.u_wait[ue] = 0u;
+      }
+      L.pair_token[po + pos] = t;
+      L.tk_u[tid] = ue;
+      L.tk_pos[tid] = pos;
+    }
+    if (tid == 0) {
+      L.u_off[n_u] = P;
+      s_nunion = n_u;
+    }
+  }
+  __syncthreads();
+  const int n_union = s_nunion;
+  // slot hit check: identity when every expert is resident, else LRU on the
+  // double-buffered pool state (every CTA derives the same victims)
+  const int S = a.n_slots;
+  int32_t* pre_slot = pool_state + (size_t)(seq & 1u) * (E + 2 * S);
+  int32_t* pre_owner = pre_slot + E;
+  uint32_t* pre_stamp = reinterpret_cast<uint32_t*>(pre_owner + S);
+  int32_t* nxt_slot = pool_state + (size_t)((seq + 1u) & 1u) * (E + 2 * S);
+  int32_t* nxt_owner = nxt_slot + E;
+  uint32_t* nxt_stamp = reinterpret_cast<uint32_t*>(nxt_owner + S);
+  if (!a.pool) {
+    if (tid == 0) s_nmiss = 0;
+  } else if (tid == 0) {
+    int nm = 0;
+    for (int u = 0; u < n_union; ++u) {
+      const int s = ld_cg_i32(&pre_slot[L.u_expert[u]]);
+      L.u_slot[u] = s;
+      L.u_wait[u] = 0u;
+      nm += s < 0;
+    }
+    s_nmiss = nm;
+    if (nm > 0) {
+      // misses in ascending expert order take the best free candidate each:
+      // empty slots first (ascending), then slots unused by this call by
+      // (last-use step, slot) ascending
+      unsigned long long* taken_bits = L.misc;  // one bit per slot, S <= 4096
+      for (int i = 0; i < 64; ++i) taken_bits[i] = 0ull;
+      for (int u = 0; u < n_union; ++u) {
+        if (L.u_slot[u] >= 0) continue;
+        unsigned long long best = ~0ull;
+        for (int s = 0; s < S; ++s) {
+          if ((taken_bits[s >> 6] >> (s & 63)) & 1ull) continue;
+          const int ow = ld_cg_i32(&pre_owner[s]);
+          if (ow >= 0 && tokmask[ow] != 0ull) continue;
+          const unsigned long long kk = ((unsigned long long)(ow >= 0) << 44) |
+                                        ((unsigned long long)(uint32_t)ld_cg_i32((const int*)&pre_stamp[s]) << 12) |
+                                        (unsigned long long)s;
+          best = kk < best ? kk : best;
+        }
+        if (best == ~0ull) {  // cannot happen with n_slots >= max distinct per call
+          L.u_slot[u] = 0;
+          set_error(a, MOE_ERR_STATE);
+          continue;
+        }
+        const int s = (int)(best & 0xFFFull);
+        taken_bits[s >> 6] |= 1ull << (s & 63);
+        L.u_slot[u] = s;
+        L.u_wait[u] = seq;
+      }
+    }
+  }
+  __syncthreads();
+  if (a.pool && c == 0) {
+    for (int e = tid; e < E; e += kThreads) nxt_slot[e] = ld_cg_i32(&pre_slot[e]);
+    for (int s = tid; s < S; s += kThreads) {
+      nxt_owner[s] = ld_cg_i32(&pre_owner[s]);
+      nxt_stamp[s] = (uint32_t)ld_cg_i32((const int*)&pre_stamp[s]);
+    }
+    __syncthreads();
+    if (tid == 0) {
+      int nm = 0;
+      for (int u = 0; u < n_union; ++u) {
+        const int e = L.u_expert[u], s = L.u_slot[u];
+        if (L.u_wait[u] != 0u) {
+          const int old = nxt_owner[s];
+          if (old >= 0) nxt_slot[old] = -1;
+          nxt_owner[s] = e;
+          nxt_slot[e] = s;
+          volatile RingEntry* re = &a.hm->ring[(a.st->ring_head + (uint32_t)nm) % kRingSize];
+          re->seq = seq;
+          re->expert = e;
+          re->slot = s;
+          ++nm;
+        }
+        nxt_stamp[s] = seq;
+      }
+      if (nm > 0) {
+        __threadfence_system();
+        const uint32_t head = a.st->ring_head + (uint32_t)nm;
+        a.st->ring_head = head;
+        *reinterpret_cast<volatile uint32_t*>(&a.hm->head) = head;
+        __threadfence_system();
+      }
+    }
+  }
+  if (c == 0 && tid == 0) {
+    a.st->step = seq;
+    a.st->n_union = n_union;
+    a.st->n_miss = s_nmiss;
+    a.st->forwards += 1ull;
+    a.st->hits += (unsigned long long)(n_union - s_nmiss);
+    a.st->misses += (unsigned long long)s_nmiss;
+  }
+  __syncthreads();
+
+  // ---- experts
+  const int n_ex = NSh + n_union;
+  const int n_gu_tasks = n_ex * NS;
+  const int n_my = c < n_gu_tasks ? (n_gu_tasks - c + G - 1) / G : 0;
+  if (is_prod) {
+    P.n_gu = n_my;
+    P.n_dn = has_dn ? n_ex : 0;
+    P.routed = true;
+    pump(P, X);
+  }
+  // gate/up: group grp owns ring stage grp and takes this CTA's tasks
+  // m = grp, grp + gs, ... in order (a stage's uses are consumed in order by
+  // one group, so parity waits never alias a later use)
+  {
+    const int grp = warp / kGroupWarps;
+    if (grp < R.gs)
+      for (int m = grp; m < n_my; m += R.gs) gateup_task(m);
+  }
+  // every gate/up copy must be issued before the block barrier below: a
+  // group may still be waiting for one that only the producer can issue
+  if (is_prod) {
+    int spins = 0;
+    while (P.m < P.n_gu) {
+      pump(P, X);
+      if (((++spins) & 31) == 0 && (global_ns() > deadline || dev_error(a))) break;
+    }
+  }
+  // down: warp w takes expert entries w, w + 16, ...
+  float* zbuf = reinterpret_cast<float*>(sm + PL.regA);  // [xi][32 lanes][4]
+  __syncthreads();  // region A holds routing scratch until here
+  if (has_dn && warp < R.ds) {
+    // warp w owns down stage w: entries w, w + ds, ... in order
+    const int nst = I / 64;
+    for (int xi = warp; xi < n_ex; xi += R.ds) {
+      const Task tk = task_of(a, L, xi, NSh);
+      const int s = xi % R.ds;
+      if (lane == 0) {
+        int spins = 0;
+        while (ld_acquire_gpu_u32(&cnt_cur[xi]) < (uint32_t)NS) {
+          if (is_prod) pump(P, X);
+          if (((++spins) & 15) == 0) {
+            if (global_ns() > deadline) { set_error(a, MOE_ERR_TIMEOUT); break; }
+            if (dev_error(a)) break;
+          }
+          __nanosleep(128);
+        }
+      }
+      __syncwarp();
+      const bool ok = wait_full(&R.full_dn[s], (xi / R.ds) & 1, deadline, is_prod, P, X);
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (ok) {
+        const unsigned char* sb = R.dn + s * R.dn_pitch;
+        const int hrow = tk.poff + ((g < tk.cnt) ? g : 0);
+        for (int st = 0; st < nst; ++st) {
+          const __half* hr = a.h16 + (size_t)hrow * I + st * 64 + t4 * 16;
+          const uint4 b01 = ld_cg4(hr), b23 = ld_cg4(hr + 8);
+          const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
+          const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
+          supertile_mma(acc, nb, scv, b01, b23);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&R.empty_dn[s]);
+      *reinterpret_cast<float4*>(zbuf + (xi * 32 + lane) * 4) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    }
+  }
+  // no async copy may outlive the CTA: the producer drains what it still owes
+  if (is_prod) {
+    int spins = 0;
+    while (P.m < P.n_gu || P.d < P.n_dn) {
+      pump(P, X);
+      if (((++spins) & 31) == 0 && (global_ns() > deadline || dev_error(a))) break;
+    }
+    note_wait_end(P, X);  // a wait cut short by an error or the deadline
+  }
+  __syncthreads();
+  if (has_dn) {
+    for (int q = tid; q < T * 16; q += kThreads) {
+      const int t = q >> 4, row = q & 15;
+      float v = 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int xi = NSh + L.tk_u[t * k + j];
+        const int col = L.tk_pos[t * k + j];
+        const int lz = (row & 7) * 4 + (col >> 1), rz = (row >> 3) * 2 + (col & 1);
+        v = fmaf(L.s_w[t * k + j], zbuf[(xi * 32 + lz) * 4 + rz], v);
+      }
+      if (NSh) {
+        const int col = t;
+        const int lz = (row & 7) * 4 + (col >> 1), rz = (row >> 3) * 2 + (col & 1);
+        v += zbuf[(0 * 32 + lz) * 4 + rz];
+      }
+      a.y[(size_t)t * H + c * 16 + row] = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    }
+  }
+}
+
+size_t g_decode_smem_limit = 0;  // dynamic shared memory the kernel may use
+
+}  // namespace
+
+size_t decode_smem_bytes(int H, int I, int E, int k, int T, int G) {
+  return make_plan(H, I, E, k, T, G, g_decode_smem_limit).total;
+}
+
+cudaError_t decode_configure() {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, decode_kernel);
+  if (e != cudaSuccess) return e;
+  const size_t limit = (size_t)optin - fa.sharedSizeBytes;
+  e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
+  if (e == cudaSuccess) g_decode_smem_limit = limit;
+  return e;
+}
+
+bool decode_supported(int H, int I, int E, int k, int T, int G) {
+  if (T > kMaxT || E > kMaxE || k > kMaxTopK) return false;
+  if ((E + G - 1) / G > 8) return false;  // router: two warps per row, 16 warps
+  return g_decode_smem_limit > 0 && decode_smem_bytes(H, I, E, k, T, G) <= g_decode_smem_limit;
+}
+
+cudaError_t launch_decode(const LayerArgs& a, unsigned long long* tagged_logits, int32_t* pool_state, int G,
+                          cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = decode_smem_bytes(a.H, a.I, a.E, a.k, a.T, G);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_kernel, a, tagged_logits, pool_state, g_decode_smem_limit);
+}
+
+}  // namespace moe

@@ -115,6 +115,8 @@ struct LayerArgs {
   const uint16_t* x;    // bf16 [T][H]
   uint16_t* y;          // bf16 [T][H]
   unsigned long long wait_timeout_ns;
+  uint32_t* counters;   // [2][cnt_stride] gate/up completion counts, by step parity
+  int cnt_stride;       // max distinct experts per call + 2
 };
 
 // Launch helpers (moe_kernels.cu).  All return cudaSuccess or the launch error.
@@ -127,5 +129,12 @@ size_t route_smem_bytes(int H, int E);
 cudaError_t configure_kernels(int H, int E);
 int gateup_max_blocks_per_sm(int T);
 int down_max_blocks_per_sm(int T);
+
+// Fused single-launch decode path (moe_decode.cu), T <= 8.
+size_t decode_smem_bytes(int H, int I, int E, int k, int T, int G);
+bool decode_supported(int H, int I, int E, int k, int T, int G);
+cudaError_t decode_configure();
+cudaError_t launch_decode(const LayerArgs& a, unsigned long long* tagged_logits, int32_t* pool_state, int G,
+                          cudaStream_t s);
 
 }  // namespace moe

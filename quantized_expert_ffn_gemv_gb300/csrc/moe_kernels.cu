@@ -205,6 +205,8 @@ __device__ void route_finish(const LayerArgs& a, unsigned char* smem) {
   for (int e = tid; e < E; e += kRouteThreads) tokmask[e] = 0ull;
   __syncthreads();
   const uint32_t seq = s_seq;
+  // keep the fused decode path's gate/up counters of the next step at zero
+  for (int i = tid; i < a.cnt_stride; i += kRouteThreads) a.counters[(size_t)((seq + 1u) & 1u) * a.cnt_stride + i] = 0u;
 
   // ---- top-k per token (warp per token), ties to the lower index
   for (int t = warp; t < T; t += 8) {
@@ -475,7 +477,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(LayerArgs a) {
 
 // ------------------------------------------------------------------ gate/up
 
-constexpr int kGuThreads = 256;  // 8 warps split the K = H reduction of a strip
+constexpr int kGuThreads = 128;  // 4 warps split the K = H reduction of a strip, as in the fused path
+constexpr int kGuWarpsPerTask = kGuThreads / 32;
 constexpr int kGuBatch = 4;      // super-tiles per warp with loads in flight together
 
 // Waits (one thread, bounded by the layer's timeout) until the slot holds the
@@ -502,7 +505,7 @@ __device__ bool wait_slot(const LayerArgs& a, int slot, uint32_t seq, bool count
 
 template <int NG>
 __global__ void __launch_bounds__(kGuThreads) gateup_kernel(LayerArgs a) {
-  extern __shared__ __align__(16) float red[];  // [8 warps][NG][32 lanes][8]
+  extern __shared__ __align__(16) float red[];  // [4 warps][NG][32 lanes][8]
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -550,12 +553,12 @@ __global__ void __launch_bounds__(kGuThreads) gateup_kernel(LayerArgs a) {
 #pragma unroll
       for (int c = 0; c < 4; ++c) accg[q][c] = accu[q][c] = 0.f;
 
-    for (int st0 = warp; st0 < nst; st0 += 8 * kGuBatch) {
+    for (int st0 = warp; st0 < nst; st0 += kGuWarpsPerTask * kGuBatch) {
       uint4 ngw[kGuBatch], nuw[kGuBatch];
       uint2 gsc[kGuBatch], usc[kGuBatch];
 #pragma unroll
       for (int b = 0; b < kGuBatch; ++b) {
-        const int st = st0 + 8 * b;
+        const int st = st0 + kGuWarpsPerTask * b;
         if (st < nst) {
           ngw[b] = ld_cg4(strip + st * 512 + lane * 16);
           gsc[b] = ld_cg2(strip + 8 * H + st * 64 + g * 8);
@@ -565,7 +568,7 @@ __global__ void __launch_bounds__(kGuThreads) gateup_kernel(LayerArgs a) {
       }
 #pragma unroll
       for (int b = 0; b < kGuBatch; ++b) {
-        const int st = st0 + 8 * b;
+        const int st = st0 + kGuWarpsPerTask * b;
         if (st < nst) {
 #pragma unroll
           for (int q = 0; q < NG; ++q) {
@@ -586,10 +589,9 @@ __global__ void __launch_bounds__(kGuThreads) gateup_kernel(LayerArgs a) {
       dst[1] = make_float4(accu[q][0], accu[q][1], accu[q][2], accu[q][3]);
     }
     __syncthreads();
-    if (warp < ng) {
-      const int q = warp;
+    for (int q = warp; q < ng; q += kGuWarpsPerTask) {
       float gs[4] = {0.f, 0.f, 0.f, 0.f}, us[4] = {0.f, 0.f, 0.f, 0.f};
-      for (int w = 0; w < 8; ++w) {
+      for (int w = 0; w < kGuWarpsPerTask; ++w) {
         const float4* src = reinterpret_cast<const float4*>(red + (((w * NG) + q) * 32 + lane) * 8);
         const float4 p = src[0], r = src[1];
         gs[0] += p.x; gs[1] += p.y; gs[2] += p.z; gs[3] += p.w;
@@ -762,7 +764,7 @@ cudaError_t launch(K kernel, int grid, int block, size_t smem, cudaStream_t s, b
   return cudaLaunchKernelEx(&cfg, kernel, a);
 }
 
-size_t gateup_smem(int NG) { return sizeof(float) * 8 * NG * 32 * 8; }
+size_t gateup_smem(int NG) { return sizeof(float) * kGuWarpsPerTask * NG * 32 * 8; }
 size_t down_smem(int NG, int T) { return sizeof(float) * (kDnWarps * NG * 32 * 4 + T * 16); }
 
 }  // namespace

@@ -189,6 +189,8 @@ struct moe_layer {
   std::vector<int32_t> miss_log;
   std::atomic<uint64_t> h2d_bytes{0};
   uint64_t wait_timeout_ns = 2000000000ull;
+  unsigned long long* tagged_logits = nullptr;  // fused kernel: [T][E] (step << 32 | logit bits)
+  int32_t* pool_state = nullptr;           // fused kernel: double-buffered slot table
 };
 
 namespace {
@@ -380,7 +382,8 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
                o_x16 = carve(2ull * Tm * H), o_uexp = carve(4ull * Um), o_uslot = carve(4ull * Um),
                o_uwait = carve(4ull * Um), o_uoff = carve(4ull * (Um + 1)), o_ptok = carve(4 * P),
                o_pw = carve(4 * P), o_tku = carve(4 * P), o_tkpos = carve(4 * P),
-               o_h16 = carve(2ull * (P + Tm) * I), o_tki = carve(4 * P), o_tkw = carve(4 * P);
+               o_h16 = carve(2ull * (P + Tm) * I), o_tki = carve(4 * P), o_tkw = carve(4 * P),
+               o_bar = carve(8ull * Tm * E), o_cnt = carve(8ull * (Um + 2)), o_pool = carve(4ull * 2 * 3 * E);
   if (cudaMalloc(&L->dev_block, off) != cudaSuccess) {
     L->dev_block = nullptr;
     return fail(MOE_ERR_OUT_OF_MEMORY);
@@ -417,6 +420,11 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.topk_idx = (int32_t*)(b + o_tki);
   a.topk_w = (float*)(b + o_tkw);
   a.wait_timeout_ns = L->wait_timeout_ns;
+  L->tagged_logits = (unsigned long long*)(b + o_bar);
+  a.counters = (uint32_t*)(b + o_cnt);
+  a.cnt_stride = Um + 2;
+  L->pool_state = (int32_t*)(b + o_pool);
+  if (decode_configure() != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (cudaStreamCreateWithFlags(&L->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
     L->copy_stream = nullptr;
     return fail(MOE_ERR_CUDA);
@@ -450,6 +458,18 @@ moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* aren
     for (int e = 0; e < E; ++e) slot_of[e] = -1;
   }
   std::vector<uint32_t> zeros(E, 0u);
+  // the fused kernel's double-buffered copy: [slot_of E][owner S][stamp S] twice
+  {
+    const int S = n_slots;
+    std::vector<int32_t> ps((size_t)2 * (E + 2 * S), 0);
+    for (int h = 0; h < 2; ++h) {
+      int32_t* base = ps.data() + (size_t)h * (E + 2 * S);
+      for (int e = 0; e < E; ++e) base[e] = slot_of[e];
+      for (int q = 0; q < S; ++q) base[E + q] = owner[q];
+    }
+    if (cudaMemcpy(L->pool_state, ps.data(), ps.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if (cudaMemcpy(a.slot_of, slot_of.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemcpy(a.owner, owner.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemcpy(a.stamp, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess ||
@@ -481,6 +501,11 @@ moe_status_t moe_forward(moe_layer_t* L, const void* x, int32_t T, void* y, int3
   if (topk_w) a.topk_w = topk_w;
   a.wait_timeout_ns = L->wait_timeout_ns;
   cudaStream_t s = (cudaStream_t)stream;
+  if (decode_supported(L->d.hidden, L->d.inter, L->d.n_experts, L->d.top_k, T, L->sm_count)) {
+    if (launch_decode(a, L->tagged_logits, L->pool_state, L->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  if (a.pool) return MOE_ERR_UNSUPPORTED;  // the slot pool runs on the fused path only
   const int Um = L->d.n_experts < T * L->d.top_k ? L->d.n_experts : T * L->d.top_k;
   const int max_tasks = (L->d.n_shared + Um) * (L->d.inter / 16);
   int gu_grid = L->sm_count * gateup_max_blocks_per_sm(T);
