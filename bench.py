@@ -174,19 +174,146 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def h2d_peak_gbs(torch, nbytes, reps):
+    src = torch.empty(nbytes * 4, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes * 4, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for i in range(4):
+            dst[i * nbytes:(i + 1) * nbytes].copy_(src[i * nbytes:(i + 1) * nbytes], non_blocking=True)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(s)
+        for r in range(reps):
+            i = r % 4
+            dst[i * nbytes:(i + 1) * nbytes].copy_(src[i * nbytes:(i + 1) * nbytes], non_blocking=True)
+        e1.record(s)
+    torch.cuda.synchronize()
+    return nbytes * reps / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+
+def run_stack(args):
+    """48 distinct page-scale layers, residual + RMSNorm between them, each
+    layer's VRAM slot pool capped at 128 of 512 experts (LRU, misses copied
+    from pinned host RAM); 64 warm-up then 256 measured decode tokens, batch 1.
+    The same stack then runs with every expert resident: outputs must be
+    bit-identical, and that run gives the HBM roofline figure."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from quantized_expert_ffn_gemv_gb300 import moe, synth
+    from quantized_expert_ffn_gemv_gb300.stack import MoeStack
+    torch.cuda.set_device(0)
+    n_layers, slots = args.layers, 128
+    warm = max(args.warmup, 64)
+    meas = args.steps
+    t0 = time.time()
+    layer_objs = []
+    for l in range(n_layers):
+        L = synth.make_layer(synth.PAGE, layer=l)
+        layer_objs.append(moe.MoeLayer(L.shape, L.W_r, L.bias, L.experts, L.shared, max_tokens=1, n_slots=slots))
+        del L
+    setup_s = time.time() - t0
+
+    class _Stack(MoeStack):
+        def __init__(self, layers):
+            self.layers, self.eps, self.H, self.k = layers, 1e-6, synth.PAGE.H, synth.PAGE.k
+            self.device = torch.device("cuda", 0)
+
+    st = _Stack(layer_objs)
+    ntok = warm + meas
+    x = synth.activations(synth.PAGE, 1000, 0, ntok, stream=9)
+    x_pin = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    xin = torch.empty((1, synth.PAGE.H), dtype=torch.bfloat16, device="cuda")
+    bufs = st.buffers(1)
+    stream = torch.cuda.Stream()
+
+    def totals():
+        ss = [l.stats() for l in st.layers]
+        return (sum(s["misses"] for s, _ in ss), sum(s["h2d_bytes"] for s, _ in ss), [c for _, c in ss])
+
+    def run(n_slots):
+        for l in st.layers:
+            l.configure(n_slots)
+        outs = torch.empty((ntok, synth.PAGE.H), dtype=torch.bfloat16, device="cuda")
+        with torch.cuda.stream(stream):
+            xin.copy_(x_pin[0:1], non_blocking=True)
+            st.forward(xin, bufs, stream)  # first call: host-side set-up
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            o = st.forward(xin, bufs, stream)
+        for l in st.layers:  # start every pool empty again
+            l.configure(n_slots)
+        with torch.cuda.stream(stream):
+            for t in range(warm):
+                xin.copy_(x_pin[t:t + 1], non_blocking=True)
+                graph.replay()
+                outs[t:t + 1].copy_(o)
+        torch.cuda.synchronize()
+        m0, b0, _ = totals()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for t in range(warm, ntok):
+                xin.copy_(x_pin[t:t + 1], non_blocking=True)
+                graph.replay()
+                outs[t:t + 1].copy_(o)
+            ev[1].record(stream)
+        torch.cuda.synchronize()
+        m1, b1, codes = totals()
+        return ev[0].elapsed_time(ev[1]), outs, m1 - m0, b1 - b0, codes
+
+    ms_pool, out_pool, misses, h2d_bytes, codes = run(slots)
+    ms_res, out_res, _, _, codes_res = run(synth.PAGE.E)
+    identical = bool(torch.equal(out_pool.view(torch.int16), out_res.view(torch.int16)))
+    peak_small = h2d_peak_gbs(torch, synth.PAGE.expert_bytes, 256)
+    peak_large = h2d_peak_gbs(torch, 64 << 20, 16)
+    hbm_peak, peak_kind = measured_peak()
+    step_bytes = n_layers * STEP_BYTES_PER_TOKEN
+    res_tps = meas / (ms_res * 1e-3)
+    pool_tps = meas / (ms_pool * 1e-3)
+    h2d_gbs = h2d_bytes / (ms_pool * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": pool_tps, "unit": UNIT, "n_gpus": 1, "steps": meas, "warmup": warm,
+        "ms_per_step": ms_pool / meas, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16xf16+f32 (4-bit weights)", "data": "synthetic",
+        "config": {"workload": f"{n_layers}-layer page-scale MoE stack, residual + RMSNorm, 128-slot (25%) "
+                               "LRU pool per layer, misses from pinned host RAM; 64 warm-up tokens, then the "
+                               "timed tokens, batch 1",
+                   "layers": n_layers, "slots_per_layer": slots},
+        "pool": {"tokens_per_s": pool_tps, "misses": misses, "h2d_bytes": h2d_bytes,
+                 "h2d_bytes_per_token": h2d_bytes / meas, "h2d_gbs": h2d_gbs,
+                 "h2d_peak_gbs_expert_copies": peak_small, "h2d_peak_gbs_64MB_copies": peak_large,
+                 "h2d_frac_of_expert_copy_peak": h2d_gbs / peak_small, "status": codes},
+        "resident": {"tokens_per_s": res_tps, "status": codes_res, "roofline": {
+            "bound": "hbm", "achieved": step_bytes * res_tps / 1e9, "peak": hbm_peak, "unit": "GB/s",
+            "frac": step_bytes * res_tps / 1e9 / hbm_peak, "peak_kind": peak_kind, "bytes_per_token": step_bytes}},
+        "bit_identical_pool_vs_resident": identical,
+        "setup_s": setup_s,
+    }
+    print(json.dumps(line), flush=True)
+    st.close()
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=32, help="oracle tokens timed for cpu_baseline")
     ap.add_argument("--tokens", type=int, default=TOKENS_PER_STEP)
+    ap.add_argument("--workload", default="decode", choices=["decode", "stack"],
+                    help="decode: one page-scale layer, batch 1 (default); stack: 48-layer stack with a 25%% pool")
+    ap.add_argument("--layers", type=int, default=48, help="stack depth for --workload stack")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 256 if args.workload == "stack" else 10
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload == "stack":
+        return run_stack(args)
 
     import torch
     import __graft_entry__

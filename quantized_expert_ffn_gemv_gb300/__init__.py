@@ -7,11 +7,11 @@ CUDA library, or without a GPU, raises.
 """
 from . import synth  # noqa: F401
 
-__all__ = ["synth", "moe"]
+__all__ = ["synth", "moe", "stack"]
 
 
 def __getattr__(name):
-    if name == "moe":
+    if name in ("moe", "stack"):
         import importlib
-        return importlib.import_module(__name__ + ".moe")
+        return importlib.import_module(__name__ + "." + name)
     raise AttributeError(name)

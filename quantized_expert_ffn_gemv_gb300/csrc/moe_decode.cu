@@ -197,8 +197,10 @@ __host__ __device__ inline Plan plan_with(int H, int I, int E, int k, int T, int
   o += al128((size_t)T * H * 2);
   // region A: router rows (prologue), routing scratch, then down results
   const size_t router = (size_t)p.rows_max * H * 4;
-  // tokmask [E], then (key, e) entries: 16 lists of kMaxTopK, merge candidates, selections
-  const size_t routing = al128((size_t)E * 8) + (size_t)4 * kWarps * kMaxTopK * 8;
+  // tokmask [E], then (key, e) entries: 16 lists of kMaxTopK, merge candidates,
+  // selections; then the pool scratch (owner, stamp, key per slot, S <= E)
+  const size_t routing = al128((size_t)E * 8) + (size_t)4 * kWarps * kMaxTopK * 8 + (size_t)E * 16 + 16 +
+                         (size_t)(p.umax + 2) * 8;
   const size_t zbuf = (size_t)(p.umax + 1) * 32 * 4 * 4;
   size_t ra = router > routing ? router : routing;
   ra = ra > zbuf ? ra : zbuf;
@@ -841,75 +843,96 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   uint32_t* nxt_stamp = reinterpret_cast<uint32_t*>(nxt_owner + S);
   if (!a.pool) {
     if (tid == 0) s_nmiss = 0;
-  } else if (tid == 0) {
-    int nm = 0;
-    for (int u = 0; u < n_union; ++u) {
-      const int s = ld_cg_i32(&pre_slot[L.u_expert[u]]);
-      L.u_slot[u] = s;
+  } else {
+    // pool scratch in region A after tokmask: per slot owner, stamp and
+    // candidate key; per union entry its miss number; the ranked victims
+    int* own_s = reinterpret_cast<int*>(sm + PL.regA + al128((size_t)E * 8) + (size_t)4 * kWarps * kMaxTopK * 8);
+    uint32_t* stp_s = reinterpret_cast<uint32_t*>(own_s + S);
+    unsigned long long* key_s = reinterpret_cast<unsigned long long*>(stp_s + S);  // 8-byte aligned: 8S bytes precede it
+    int* miss_no = reinterpret_cast<int*>(key_s + S);
+    int* victim = miss_no + PL.umax + 2;
+    __shared__ int s_ncand;
+    if (tid == 0) s_ncand = 0;
+    __syncthreads();
+    // candidates: empty slots first (ascending), then slots whose expert this
+    // call does not use, least recently used first, ties to the lower slot
+    for (int q = tid; q < S; q += kThreads) {
+      const int ow = ld_cg_i32(&pre_owner[q]);
+      const uint32_t stp = (uint32_t)ld_cg_i32((const int*)&pre_stamp[q]);
+      own_s[q] = ow;
+      stp_s[q] = stp;
+      const bool elig = ow < 0 || tokmask[ow] == 0ull;
+      key_s[q] = elig ? (((unsigned long long)(ow >= 0) << 44) | ((unsigned long long)stp << 12) | (unsigned long long)q)
+                      : ~0ull;
+      if (elig) atomicAdd(&s_ncand, 1);
+    }
+    for (int u = tid; u < n_union; u += kThreads) {
+      L.u_slot[u] = ld_cg_i32(&pre_slot[L.u_expert[u]]);
       L.u_wait[u] = 0u;
-      nm += s < 0;
-    }
-    s_nmiss = nm;
-    if (nm > 0) {
-      // misses in ascending expert order take the best free candidate each:
-      // empty slots first (ascending), then slots unused by this call by
-      // (last-use step, slot) ascending
-      unsigned long long* taken_bits = L.misc;  // one bit per slot, S <= 4096
-      for (int i = 0; i < 64; ++i) taken_bits[i] = 0ull;
-      for (int u = 0; u < n_union; ++u) {
-        if (L.u_slot[u] >= 0) continue;
-        unsigned long long best = ~0ull;
-        for (int s = 0; s < S; ++s) {
-          if ((taken_bits[s >> 6] >> (s & 63)) & 1ull) continue;
-          const int ow = ld_cg_i32(&pre_owner[s]);
-          if (ow >= 0 && tokmask[ow] != 0ull) continue;
-          const unsigned long long kk = ((unsigned long long)(ow >= 0) << 44) |
-                                        ((unsigned long long)(uint32_t)ld_cg_i32((const int*)&pre_stamp[s]) << 12) |
-                                        (unsigned long long)s;
-          best = kk < best ? kk : best;
-        }
-        if (best == ~0ull) {  // cannot happen with n_slots >= max distinct per call
-          L.u_slot[u] = 0;
-          set_error(a, MOE_ERR_STATE);
-          continue;
-        }
-        const int s = (int)(best & 0xFFFull);
-        taken_bits[s >> 6] |= 1ull << (s & 63);
-        L.u_slot[u] = s;
-        L.u_wait[u] = seq;
-      }
-    }
-  }
-  __syncthreads();
-  if (a.pool && c == 0) {
-    for (int e = tid; e < E; e += kThreads) nxt_slot[e] = ld_cg_i32(&pre_slot[e]);
-    for (int s = tid; s < S; s += kThreads) {
-      nxt_owner[s] = ld_cg_i32(&pre_owner[s]);
-      nxt_stamp[s] = (uint32_t)ld_cg_i32((const int*)&pre_stamp[s]);
     }
     __syncthreads();
-    if (tid == 0) {
-      int nm = 0;
-      for (int u = 0; u < n_union; ++u) {
-        const int e = L.u_expert[u], s = L.u_slot[u];
-        if (L.u_wait[u] != 0u) {
-          const int old = nxt_owner[s];
-          if (old >= 0) nxt_slot[old] = -1;
-          nxt_owner[s] = e;
-          nxt_slot[e] = s;
-          volatile RingEntry* re = &a.hm->ring[(a.st->ring_head + (uint32_t)nm) % kRingSize];
-          re->seq = seq;
-          re->expert = e;
-          re->slot = s;
-          ++nm;
-        }
-        nxt_stamp[s] = seq;
+    // misses in ascending expert order (the union order) get numbers 0, 1, ...
+    if (warp == 0) {
+      int base = 0;
+      for (int u0 = 0; u0 < n_union; u0 += 32) {
+        const int u = u0 + lane;
+        const bool m = u < n_union && L.u_slot[u] < 0;
+        const unsigned b = __ballot_sync(0xffffffffu, m);
+        if (m) miss_no[u] = base + __popc(b & ((1u << lane) - 1u));
+        base += __popc(b);
       }
-      if (nm > 0) {
+      if (lane == 0) s_nmiss = base;
+    }
+    // the i-th best candidate slot is the i-th miss's victim
+    for (int q = tid; q < S; q += kThreads) {
+      const unsigned long long kq = key_s[q];
+      if (kq == ~0ull) continue;
+      int r = 0;
+      for (int j = 0; j < S; ++j) r += key_s[j] < kq;
+      if (r < PL.umax) victim[r] = q;
+    }
+    __syncthreads();
+    const int nm = s_nmiss;
+    if (nm > s_ncand && tid == 0) set_error(a, MOE_ERR_STATE);  // configure forbids this
+    for (int u = tid; u < n_union; u += kThreads)
+      if (L.u_slot[u] < 0) {
+        const int i = miss_no[u];
+        L.u_slot[u] = (i < s_ncand) ? victim[i] : 0;  // 0 keeps addresses in bounds on error
+        L.u_wait[u] = seq;
+      }
+    __syncthreads();
+    // CTA 0 writes the next state and rings the host doorbell
+    if (c == 0) {
+      for (int e = tid; e < E; e += kThreads) nxt_slot[e] = ld_cg_i32(&pre_slot[e]);
+      for (int q = tid; q < S; q += kThreads) {
+        nxt_owner[q] = own_s[q];
+        nxt_stamp[q] = stp_s[q];
+      }
+      __syncthreads();
+      for (int u = tid; u < n_union; u += kThreads) {
+        const int e = L.u_expert[u], q = L.u_slot[u];
+        if (L.u_wait[u] != 0u) {
+          const int old = own_s[q];
+          if (old >= 0) nxt_slot[old] = -1;  // an evicted expert is never selected now
+          nxt_owner[q] = e;
+          nxt_slot[e] = q;
+        }
+        nxt_stamp[q] = seq;
+      }
+      if (tid == 0 && nm > 0) {
+        int i = 0;
+        const uint32_t head0 = a.st->ring_head;
+        for (int u = 0; u < n_union; ++u)
+          if (L.u_wait[u] != 0u) {
+            volatile RingEntry* re = &a.hm->ring[(head0 + (uint32_t)i) % kRingSize];
+            re->seq = seq;
+            re->expert = L.u_expert[u];
+            re->slot = L.u_slot[u];
+            ++i;
+          }
         __threadfence_system();
-        const uint32_t head = a.st->ring_head + (uint32_t)nm;
-        a.st->ring_head = head;
-        *reinterpret_cast<volatile uint32_t*>(&a.hm->head) = head;
+        a.st->ring_head = head0 + (uint32_t)nm;
+        *reinterpret_cast<volatile uint32_t*>(&a.hm->head) = head0 + (uint32_t)nm;
         __threadfence_system();
       }
     }

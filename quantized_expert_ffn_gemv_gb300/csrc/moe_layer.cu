@@ -177,10 +177,11 @@ struct moe_layer {
   LayerArgs args{};
   int n_slots = 0;
   uint8_t* arena = nullptr;
-  cudaStream_t copy_stream = nullptr;
+  cudaStream_t copy_stream[2] = {nullptr, nullptr};  // misses alternate between two copy engines' queues
   WriteValue32Fn write_value = nullptr;
-  std::thread server;
-  std::atomic<bool> stop{false};
+  uint32_t tail = 0;         // ring entries served (copy-server thread only)
+  uint64_t copies = 0;       // copies issued (copy-server thread only)
+  bool registered = false;   // polled by the copy server
   std::atomic<bool> paused{false};
   std::atomic<int64_t> fail_copy_n{0};
   std::atomic<int64_t> copies_since_arm{0};
@@ -200,9 +201,10 @@ void serve_entry(moe_layer* L, const RingEntry& e) {
   const int64_t n = L->fail_copy_n.load();
   if (n > 0 && ++L->copies_since_arm == n) fail = true;
   if (e.slot < 0 || e.slot >= L->n_slots || e.expert < 0 || e.expert >= L->d.n_experts) fail = true;
+  cudaStream_t cs = L->copy_stream[L->copies++ & 1];
   if (!fail) {
     const cudaError_t err = cudaMemcpyAsync(L->arena + (int64_t)e.slot * L->blob, L->master + (int64_t)e.expert * L->blob,
-                                            (size_t)L->blob, cudaMemcpyHostToDevice, L->copy_stream);
+                                            (size_t)L->blob, cudaMemcpyHostToDevice, cs);
     if (err != cudaSuccess) fail = true;
   }
   uint32_t val = e.seq;
@@ -214,49 +216,121 @@ void serve_entry(moe_layer* L, const RingEntry& e) {
     L->h2d_bytes += (uint64_t)L->blob;
   }
   const int slot = (e.slot >= 0 && e.slot < L->n_slots) ? e.slot : 0;
-  L->write_value((CUstream)L->copy_stream, (CUdeviceptr)(L->args.ready + slot), val, 0);
+  // published on the same stream after the copy (with a memory barrier)
+  L->write_value((CUstream)cs, (CUdeviceptr)(L->args.ready + slot), val, 0);
   std::lock_guard<std::mutex> g(L->log_mu);
   L->miss_log.push_back((int32_t)e.seq);
   L->miss_log.push_back(e.expert);
   L->miss_log.push_back(e.slot);
 }
 
-void server_main(moe_layer* L) {
-  cudaSetDevice(L->d.device);
+// One copy-server thread for the whole process polls the doorbell rings of
+// every layer that has a slot pool.  It spins while doorbells are recent
+// (decode rings one every few tens of microseconds) and sleeps in 50 us steps
+// after 20 ms without one.
+struct CopyServer {
+  std::mutex mu;
+  std::vector<moe_layer*> layers;
+  std::thread th;
+  std::atomic<bool> stop{false};
+  std::atomic<uint64_t> epoch{0};  // bumped after every poll round
+  int device = -1;
+};
+CopyServer& copy_server() {
+  static CopyServer* cs = new CopyServer();  // never destroyed: outlives every layer
+  return *cs;
+}
+
+bool poll_layer(moe_layer* L) {
+  if (L->paused.load(std::memory_order_relaxed)) return false;
+  const uint32_t head = __atomic_load_n(&L->hm_host->head, __ATOMIC_ACQUIRE);
+  if (head == L->tail) return false;
+  while (L->tail != head) {
+    RingEntry e;
+    const volatile RingEntry* src = &L->hm_host->ring[L->tail % kRingSize];
+    e.seq = src->seq;
+    e.expert = src->expert;
+    e.slot = src->slot;
+    e.pad = 0;
+    serve_entry(L, e);
+    ++L->tail;
+  }
+  return true;
+}
+
+void server_main() {
+  CopyServer& S = copy_server();
   cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
   cudaThreadExchangeStreamCaptureMode(&mode);
-  uint32_t tail = __atomic_load_n(&L->hm_host->head, __ATOMIC_ACQUIRE);
-  uint64_t idle = 0;
-  while (!L->stop.load(std::memory_order_relaxed)) {
-    if (L->paused.load(std::memory_order_relaxed)) {
-      std::this_thread::sleep_for(std::chrono::microseconds(200));
-      continue;
+  int cur_dev = -1;
+  auto last = std::chrono::steady_clock::now();
+  std::vector<moe_layer*> snap;
+  while (!S.stop.load(std::memory_order_relaxed)) {
+    {
+      std::lock_guard<std::mutex> g(S.mu);
+      snap = S.layers;
     }
-    const uint32_t head = __atomic_load_n(&L->hm_host->head, __ATOMIC_ACQUIRE);
-    if (head == tail) {
-      if (++idle > 200000) std::this_thread::sleep_for(std::chrono::microseconds(20));
-      continue;
+    bool any = false;
+    for (moe_layer* L : snap) {
+      if (L->d.device != cur_dev) {
+        cudaSetDevice(L->d.device);
+        cur_dev = L->d.device;
+      }
+      any |= poll_layer(L);
     }
-    idle = 0;
-    while (tail != head) {
-      RingEntry e;
-      const volatile RingEntry* src = &L->hm_host->ring[tail % kRingSize];
-      e.seq = src->seq;
-      e.expert = src->expert;
-      e.slot = src->slot;
-      e.pad = 0;
-      serve_entry(L, e);
-      ++tail;
-    }
+    S.epoch.fetch_add(1, std::memory_order_acq_rel);
+    const auto now = std::chrono::steady_clock::now();
+    if (any) last = now;
+    else if (now - last > std::chrono::milliseconds(20)) std::this_thread::sleep_for(std::chrono::microseconds(50));
   }
 }
 
-void stop_server(moe_layer* L) {
-  if (L->server.joinable()) {
-    L->stop = true;
-    L->server.join();
-    L->stop = false;
+// At process exit the server stops before the CUDA runtime tears down (its
+// exit handler was registered earlier, so it runs later).
+void shutdown_server() {
+  CopyServer& S = copy_server();
+  S.stop = true;
+  if (S.th.joinable()) S.th.join();
+}
+
+void register_layer(moe_layer* L) {
+  static const bool exit_hook = (std::atexit(shutdown_server), true);
+  (void)exit_hook;
+  CopyServer& S = copy_server();
+  std::lock_guard<std::mutex> g(S.mu);
+  L->tail = __atomic_load_n(&L->hm_host->head, __ATOMIC_ACQUIRE);
+  S.layers.push_back(L);
+  L->registered = true;
+  if (!S.th.joinable()) {
+    S.stop = false;
+    S.th = std::thread(server_main);
   }
+}
+
+// After this returns the server no longer touches L.
+void stop_server(moe_layer* L) {
+  if (!L->registered) return;
+  CopyServer& S = copy_server();
+  bool join = false;
+  {
+    std::lock_guard<std::mutex> g(S.mu);
+    for (size_t i = 0; i < S.layers.size(); ++i)
+      if (S.layers[i] == L) {
+        S.layers.erase(S.layers.begin() + (long)i);
+        break;
+      }
+    join = S.layers.empty();
+    if (join) S.stop = true;
+  }
+  if (join) {
+    if (S.th.joinable()) S.th.join();
+    S.stop = false;
+  } else {
+    // wait for two poll rounds: a round that started before the erase has ended
+    const uint64_t e0 = S.epoch.load();
+    for (int i = 0; i < 200000 && S.epoch.load() < e0 + 2; ++i) std::this_thread::sleep_for(std::chrono::microseconds(5));
+  }
+  L->registered = false;
 }
 
 int sticky_error(moe_layer* L) {
@@ -268,7 +342,8 @@ int sticky_error(moe_layer* L) {
 void free_layer(moe_layer* L) {
   if (!L) return;
   stop_server(L);
-  if (L->copy_stream) cudaStreamDestroy(L->copy_stream);
+  for (auto& cs : L->copy_stream)
+    if (cs) cudaStreamDestroy(cs);
   if (L->dev_block) cudaFree(L->dev_block);
   if (L->shared_dev) cudaFree(L->shared_dev);
   if (L->hm_host) cudaFreeHost(L->hm_host);
@@ -425,10 +500,11 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.cnt_stride = Um + 2;
   L->pool_state = (int32_t*)(b + o_pool);
   if (decode_configure() != cudaSuccess) return fail(MOE_ERR_CUDA);
-  if (cudaStreamCreateWithFlags(&L->copy_stream, cudaStreamNonBlocking) != cudaSuccess) {
-    L->copy_stream = nullptr;
-    return fail(MOE_ERR_CUDA);
-  }
+  for (auto& cs : L->copy_stream)
+    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+      cs = nullptr;
+      return fail(MOE_ERR_CUDA);
+    }
   (void)st;
   *out = L;
   return MOE_OK;
@@ -477,7 +553,7 @@ moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* aren
     return MOE_ERR_CUDA;
   if (a.pool) {
     try {
-      L->server = std::thread(server_main, L);
+      register_layer(L);
     } catch (...) {
       return MOE_ERR_OUT_OF_MEMORY;
     }

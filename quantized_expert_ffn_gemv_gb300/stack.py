@@ -1,0 +1,63 @@
+"""A stack of MoE layers with residual + RMSNorm between them.
+
+Per layer l (pre-norm, no learned weight, eps 1e-6):
+    xhat_l  = bf16(x_l / sqrt(mean(x_l^2) + eps))
+    y_l     = MoE_l(xhat_l)                        (moe_forward)
+    x_{l+1} = bf16(x_l + y_l)
+The stack's output is x_L.  Every layer owns its own VRAM expert-slot pool
+(Betelgeuse news page, section 机制, 显存 row: per-layer slot budgets), fed
+from its pinned host master copy on a miss.  Marshalling only: each step is
+one of the library's kernels.
+"""
+import numpy as np
+
+from . import moe
+
+
+class MoeStack:
+    def __init__(self, layers, max_tokens=1, n_slots=None, eps=1e-6, device=0):
+        """layers: synth.Layer objects (router, bias, canonical blobs)."""
+        import torch
+        self.eps = eps
+        self.layers = [moe.MoeLayer(L.shape, L.W_r, L.bias, L.experts, L.shared, max_tokens=max_tokens,
+                                    n_slots=n_slots, device=device) for L in layers]
+        self.H = layers[0].shape.H
+        self.k = layers[0].shape.k
+        self.device = torch.device("cuda", device)
+
+    def buffers(self, T, record=False):
+        import torch
+        n = len(self.layers)
+        z = lambda *s, dt=torch.bfloat16: torch.empty(*s, dtype=dt, device=self.device)
+        b = {"x": z(2, T, self.H), "xhat": z(T, self.H), "y": z(T, self.H)}
+        if record:
+            b["xhats"] = z(n, T, self.H)
+            b["ys"] = z(n, T, self.H)
+            b["idx"] = z(n, T, self.k, dt=torch.int32)
+            b["w"] = z(n, T, self.k, dt=torch.float32)
+        return b
+
+    def forward(self, x, bufs, stream=None):
+        """x: torch bf16 [T, H] (device).  Returns the output x_L (a view into bufs)."""
+        cur = 0
+        bufs["x"][0].copy_(x)
+        moe.residual_rmsnorm(bufs["x"][0], None, self.eps, None, bufs["xhat"], stream)
+        for l, layer in enumerate(self.layers):
+            rec = "xhats" in bufs
+            if rec:
+                bufs["xhats"][l].copy_(bufs["xhat"])
+            y = bufs["ys"][l] if rec else bufs["y"]
+            layer.forward(bufs["xhat"], y, bufs["idx"][l] if rec else None, bufs["w"][l] if rec else None,
+                          stream=stream)
+            nxt = 1 - cur
+            # x_{l+1} = bf16(x_l + y_l); its RMSNorm feeds the next layer
+            moe.residual_rmsnorm(bufs["x"][cur], y, self.eps, bufs["x"][nxt], bufs["xhat"], stream)
+            cur = nxt
+        return bufs["x"][cur]
+
+    def stats(self):
+        return [l.stats()[0] for l in self.layers]
+
+    def close(self):
+        for l in self.layers:
+            l.close()
