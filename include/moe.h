@@ -80,7 +80,7 @@ typedef struct {
   int32_t n_shared;        /* 0 or 1 shared expert (weight 1, outside the softmax) */
   int32_t inter;           /* I: multiple of 64, 64..4096 */
   int32_t qblock;          /* quantization block; must be 32 */
-  int32_t max_tokens;      /* largest T a moe_forward call may pass: 1..64 */
+  int32_t max_tokens;      /* largest T a moe_forward call may pass: 1..8192 (above 64: H % 128 == 0) */
   int32_t device;          /* CUDA device ordinal */
   const float* router_w;   /* device, fp32 [E][H] row-major; caller-owned, must outlive the layer */
   const float* router_bias;/* device, fp32 [E] (per-expert logit bias), or NULL for none; caller-owned */
@@ -150,8 +150,16 @@ MOE_API moe_status_t moe_slot_pool_configure(moe_layer_t* layer, int32_t n_slots
  * lower index.  Output: y = sum over the selected experts, in ascending
  * index, of w_j * FFN_j(x), plus FFN_shared(x), accumulated in fp32 and
  * rounded once to bf16 (round to nearest even).
+ * Execution by T: T <= 8 one fused kernel (slot pool or all resident);
+ * 9..64 three kernels (all resident); 65..max_tokens the prefill path
+ * (all resident): grouped GEMMs on the tensor cores with fp16 operands
+ * (dequantized weights d*q and activations) and fp32 accumulation
+ * (halogen-flash-server README, section "Measured": prefill is compute-bound).
+ * A token's y depends only on its own x on the first two paths; the prefill
+ * path meets the same tolerances but not bit-equality with them.
  * Errors (synchronous): INVALID_ARG (T out of 1..max_tokens, NULL x/y),
- * STATE (no pool configured, or a sticky error), CUDA (launch failure).
+ * STATE (no pool configured, or a sticky error), UNSUPPORTED (T > 8 with a
+ * slot pool of fewer than E slots), CUDA (launch failure).
  */
 MOE_API moe_status_t moe_forward(moe_layer_t* layer, const void* x_bf16_dev, int32_t T, void* y_bf16_dev,
                                  int32_t* topk_idx_dev, float* topk_w_dev, void* cuda_stream);

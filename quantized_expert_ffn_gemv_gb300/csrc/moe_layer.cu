@@ -24,6 +24,7 @@
 
 #include "moe.h"
 #include "moe_internal.h"
+#include "moe_prefill.h"
 
 using namespace moe;
 
@@ -172,6 +173,8 @@ struct moe_layer {
   uint8_t* master = nullptr;  // pinned host, GPU layout, E experts
   uint8_t* shared_dev = nullptr;
   void* dev_block = nullptr;
+  void* pf_block = nullptr;  // prefill scratch (max_tokens > 64 only)
+  PrefillArgs pf{};
   HostMapped* hm_host = nullptr;
   HostMapped* hm_dev = nullptr;
   LayerArgs args{};
@@ -345,6 +348,7 @@ void free_layer(moe_layer* L) {
   for (auto& cs : L->copy_stream)
     if (cs) cudaStreamDestroy(cs);
   if (L->dev_block) cudaFree(L->dev_block);
+  if (L->pf_block) cudaFree(L->pf_block);
   if (L->shared_dev) cudaFree(L->shared_dev);
   if (L->hm_host) cudaFreeHost(L->hm_host);
   if (L->master) cudaFreeHost(L->master);
@@ -382,7 +386,8 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
     return MOE_ERR_INVALID_ARG;
   if (d.hidden % 64 || d.inter % 64 || d.hidden > kMaxHidden || d.inter > kMaxInter) return MOE_ERR_UNSUPPORTED;
   if (d.n_experts > kMaxExperts || d.top_k > kMaxTopK || d.top_k > d.n_experts) return MOE_ERR_UNSUPPORTED;
-  if (d.max_tokens > kMaxTokens) return MOE_ERR_UNSUPPORTED;
+  if (d.max_tokens > kMaxPrefillTokens) return MOE_ERR_UNSUPPORTED;
+  if (d.max_tokens > kMaxTokens && d.hidden % 128) return MOE_ERR_UNSUPPORTED;  // prefill M-blocks of 128 rows
   if (d.n_shared != 0 && d.n_shared != 1) return MOE_ERR_UNSUPPORTED;
   if (!d.router_w || !d.experts || (d.n_shared && !d.shared)) return MOE_ERR_INVALID_ARG;
 
@@ -444,8 +449,10 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   if (cudaHostGetDevicePointer((void**)&L->hm_dev, L->hm_host, 0) != cudaSuccess) return fail(MOE_ERR_CUDA);
 
   // device state + scratch, one allocation
-  const int Um = E < Tm * k ? E : Tm * k;
-  const size_t P = (size_t)Tm * k;
+  // the decode and batched paths take T <= kMaxTokens; larger T runs the prefill path
+  const int Tb = Tm < kMaxTokens ? Tm : kMaxTokens;
+  const int Um = E < Tb * k ? E : Tb * k;
+  const size_t P = (size_t)Tb * k;
   size_t off = 0;
   auto carve = [&](size_t bytes) {
     size_t o = off;
@@ -454,11 +461,11 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   };
   const size_t o_st = carve(sizeof(DevState)), o_slot_of = carve(4ull * E), o_owner = carve(4ull * E),
                o_stamp = carve(4ull * E), o_ready = carve(4ull * E), o_logits = carve(4ull * Tm * E),
-               o_x16 = carve(2ull * Tm * H), o_uexp = carve(4ull * Um), o_uslot = carve(4ull * Um),
+               o_x16 = carve(2ull * Tb * H), o_uexp = carve(4ull * Um), o_uslot = carve(4ull * Um),
                o_uwait = carve(4ull * Um), o_uoff = carve(4ull * (Um + 1)), o_ptok = carve(4 * P),
                o_pw = carve(4 * P), o_tku = carve(4 * P), o_tkpos = carve(4 * P),
-               o_h16 = carve(2ull * (P + Tm) * I), o_tki = carve(4 * P), o_tkw = carve(4 * P),
-               o_bar = carve(8ull * Tm * E), o_cnt = carve(8ull * (Um + 2)), o_pool = carve(4ull * 2 * 3 * E);
+               o_h16 = carve(2ull * (P + Tb) * I), o_tki = carve(4ull * Tm * k), o_tkw = carve(4ull * Tm * k),
+               o_bar = carve(8ull * Tb * E), o_cnt = carve(8ull * (Um + 2)), o_pool = carve(4ull * 2 * 3 * E);
   if (cudaMalloc(&L->dev_block, off) != cudaSuccess) {
     L->dev_block = nullptr;
     return fail(MOE_ERR_OUT_OF_MEMORY);
@@ -500,6 +507,15 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.cnt_stride = Um + 2;
   L->pool_state = (int32_t*)(b + o_pool);
   if (decode_configure() != cudaSuccess) return fail(MOE_ERR_CUDA);
+  if (const size_t pfb = prefill_scratch_bytes(H, I, E, k, Tm)) {
+    if (prefill_configure() != cudaSuccess) return fail(MOE_ERR_CUDA);
+    if (cudaMalloc(&L->pf_block, pfb) != cudaSuccess) {
+      L->pf_block = nullptr;
+      return fail(MOE_ERR_OUT_OF_MEMORY);
+    }
+    if (cudaMemset(L->pf_block, 0, pfb) != cudaSuccess) return fail(MOE_ERR_CUDA);
+    L->pf = prefill_carve(L->pf_block, H, I, E, k, Tm);
+  }
   for (auto& cs : L->copy_stream)
     if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
       cs = nullptr;
@@ -582,6 +598,10 @@ moe_status_t moe_forward(moe_layer_t* L, const void* x, int32_t T, void* y, int3
     return MOE_OK;
   }
   if (a.pool) return MOE_ERR_UNSUPPORTED;  // the slot pool runs on the fused path only
+  if (T > kMaxTokens) {
+    if (launch_prefill(a, L->pf, L->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
   const int Um = L->d.n_experts < T * L->d.top_k ? L->d.n_experts : T * L->d.top_k;
   const int max_tasks = (L->d.n_shared + Um) * (L->d.inter / 16);
   int gu_grid = L->sm_count * gateup_max_blocks_per_sm(T);

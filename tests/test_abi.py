@@ -54,8 +54,11 @@ def test_create_rejects_bad_descriptions_before_touching_the_gpu(moe):
     d.hidden = 1000
     assert moe.lib().moe_layer_create(C.byref(d), C.byref(h)) in (1, 2)
     d.hidden = 1024
-    d.max_tokens = 65
+    d.max_tokens = 8193  # above the largest prefill chunk
     assert moe.lib().moe_layer_create(C.byref(d), C.byref(h)) == 2
+    d.max_tokens, d.hidden = 65, 192  # prefill needs H % 128 == 0
+    assert moe.lib().moe_layer_create(C.byref(d), C.byref(h)) == 2
+    d.hidden = 1024
     assert h.value is None
     assert moe.lib().moe_forward(None, None, 1, None, None, None, None) == 1
     assert moe.expert_bytes(2048, 512) == 1_769_472
