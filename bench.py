@@ -4,8 +4,8 @@ Workload (one "step"): 1,000 decode tokens, batch 1, through the MoE layer of
 Qwen3.8-Flash-Next shape (H 2048, 512 routed experts top-10 + 1 shared,
 I 512, 4-bit block-32 weights, Zipf(1.1) router bias), cycling round-robin
 over 8 byte-identical layer replicas (8 x 0.91 GB of expert weights > L2),
-all experts resident.  Each token is one moe_forward call (three chained
-kernels); the 1,000 calls are replayed as one CUDA graph.
+all experts resident.  Each token is one moe_forward call (one fused
+kernel); the 1,000 calls are replayed as one CUDA graph.
 
   value  tokens/s with inputs resident in HBM (CUDA events on the stream)
   e2e    the same through the public API with the step's activations copied
@@ -17,6 +17,11 @@ kernels); the 1,000 calls are replayed as one CUDA graph.
 Under torchrun (N > 1) every rank runs the same workload on its own GPU
 (replicas; the layer does not shard across GPUs here) and rank 0 prints the
 aggregate.  --impl reference times the CPU oracle instead (rank 0 only).
+
+Other workloads (one JSON line each, same keys):
+  --workload stack    48 page-scale layers, residual + RMSNorm, 25% slot pool
+  --workload prefill  one 4,096-token prefill chunk through the page-scale
+                      layer (grouped GEMMs on the tensor cores)
 """
 import argparse
 import hashlib
@@ -294,6 +299,93 @@ def run_stack(args):
     print(json.dumps(line), flush=True)
     st.close()
 
+PREFILL_T = 4096
+PREFILL_PAIRS = PREFILL_T * (K + 1)                   # routed pairs + shared-expert rows
+PREFILL_FLOPS = 2 * PREFILL_PAIRS * 3 * H * I         # gate, up, down: 283.5 GFLOP on the tensor cores
+PREFILL_WEIGHT_BYTES = (E + 1) * EXPERT_BYTES + ROUTER_BYTES
+
+
+def run_prefill(args):
+    """One 4,096-token chunk through the page-scale layer per step: router,
+    top-k, grouping, gate/up and down grouped GEMMs (tcgen05), combine.
+    All experts resident; 0.91 GB of weights per step (> L2)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from quantized_expert_ffn_gemv_gb300 import moe, synth
+    torch.cuda.set_device(0)
+    L = synth.make_layer(synth.PAGE, layer=0)
+    layer = moe.MoeLayer(L.shape, L.W_r, L.bias, L.experts, L.shared, max_tokens=PREFILL_T)
+    x_host = synth.activations(L.shape, L.index, 0, PREFILL_T, stream=11)
+    x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_pin = torch.empty_like(x_pin).pin_memory()
+    xd = x_pin.to("cuda")
+    yd = torch.empty_like(xd)
+    stream = torch.cuda.Stream()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            layer.forward(xd, yd, stream=stream)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", "bench_prefill_clocks.csv")
+                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp/bench_prefill_clocks.csv")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with clocks:
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for _ in range(args.steps):
+                layer.forward(xd, yd, stream=stream)
+            ev[1].record(stream)
+        torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1])
+    e = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    with torch.cuda.stream(stream):
+        e[0].record(stream)
+        for _ in range(args.steps):
+            xd.copy_(x_pin, non_blocking=True)
+            layer.forward(xd, yd, stream=stream)
+            y_pin.copy_(yd, non_blocking=True)
+        e[1].record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e[0].elapsed_time(e[1])
+    st, code = layer.stats()
+    if code != 0:
+        raise RuntimeError(f"layer error {code}")
+    per_call = ms * 1e-3 / args.steps
+    tflops = PREFILL_FLOPS / per_call / 1e12
+    peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) if os.path.exists(
+        os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    tpeak = float(peaks.get("bf16_tflops", 1900.0))
+    hbm_peak, peak_kind = measured_peak()
+    line = {
+        "metric": "MoE prefill tokens/s (one 4096-token chunk per step); tensor-pipe fraction",
+        "value": PREFILL_T * args.steps / (ms * 1e-3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16xf16+f32 (4-bit weights dequantized to f16)", "data": "synthetic",
+        "config": {"workload": "page-scale MoE layer prefill chunk: 4096 tokens, H 2048, 512 routed experts "
+                               "top-10 + 1 shared, I 512, Zipf(1.1) router bias, all experts resident",
+                   "l2": "inputs larger than L2 (0.91 GB of expert weights per step)"},
+        "roofline": {"bound": "tensor", "kernel": "whole moe_forward call (7 kernels)", "achieved": tflops,
+                     "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
+                     "peak_kind": "measured bf16 burst (f16 runs at the bf16 rate)",
+                     "flops_per_unit": PREFILL_FLOPS, "unit_of_work": "4096-token chunk", "traffic": None,
+                     "hbm_frac": PREFILL_WEIGHT_BYTES / per_call / 1e9 / hbm_peak},
+        "e2e": {"value": PREFILL_T * args.steps / (ms_e2e * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(x_pin.numel() * 2), "d2h_bytes_per_step": int(y_pin.numel() * 2)},
+        "gpu_launches": 7 * args.steps,
+        "clocks": clocks.summary(0),
+    }
+    if args.cpu_sample > 0:
+        import oracle
+        n = min(args.cpu_sample, 16)
+        t0 = time.perf_counter()
+        oracle.moe_forward(H, I, E, K, L.W_r, L.bias, L.experts, L.shared, x_host[:n])
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"{n} prefill tokens of the page-scale layer, single-threaded binary64"}
+    print(json.dumps(line), flush=True)
+    layer.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -302,8 +394,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=32, help="oracle tokens timed for cpu_baseline")
     ap.add_argument("--tokens", type=int, default=TOKENS_PER_STEP)
-    ap.add_argument("--workload", default="decode", choices=["decode", "stack"],
-                    help="decode: one page-scale layer, batch 1 (default); stack: 48-layer stack with a 25%% pool")
+    ap.add_argument("--workload", default="decode", choices=["decode", "stack", "prefill"],
+                    help="decode: one page-scale layer, batch 1 (default); stack: 48-layer stack with a 25%% "
+                         "pool; prefill: one 4096-token chunk")
     ap.add_argument("--layers", type=int, default=48, help="stack depth for --workload stack")
     args = ap.parse_args()
     if args.steps is None:
@@ -314,6 +407,8 @@ def main():
         return run_reference(args)
     if args.workload == "stack":
         return run_stack(args)
+    if args.workload == "prefill":
+        return run_prefill(args)
 
     import torch
     import __graft_entry__
@@ -412,13 +507,13 @@ def main():
         "config": {"workload": WORKLOAD, "tokens_per_step": ntok, "replicas": REPLICAS,
                    "l2": "inputs larger than L2 (8 layer replicas, 7.25 GB of expert weights, round-robin)",
                    "parallelism": f"replicas x{ws}"},
-        "roofline": {"bound": "hbm", "kernel": "moe_forward (route + gateup + down, PDL-chained)",
+        "roofline": {"bound": "hbm", "kernel": "moe_decode_kernel (fused route + hit check + gate/up + down)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "bytes_per_unit": STEP_BYTES_PER_TOKEN, "unit_of_work": "token",
                      "traffic": recorded_traffic()},
         "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(x_pin.numel() * 2),
                 "d2h_bytes_per_step": int(y_pin.numel() * 2)},
-        "gpu_launches": 3 * ntok * args.steps,
+        "gpu_launches": ntok * args.steps,  # one fused kernel per token (T = 1)
         "clocks": clocks.summary(local),
     }
     if ws == 1 and args.cpu_sample > 0:

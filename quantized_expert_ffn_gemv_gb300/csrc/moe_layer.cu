@@ -175,6 +175,8 @@ struct moe_layer {
   void* dev_block = nullptr;
   void* pf_block = nullptr;  // prefill scratch (max_tokens > 64 only)
   PrefillArgs pf{};
+  PrefillMaps pf_maps{};
+  TensorMapEncodeFn encode_map = nullptr;
   HostMapped* hm_host = nullptr;
   HostMapped* hm_dev = nullptr;
   LayerArgs args{};
@@ -515,6 +517,13 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
     }
     if (cudaMemset(L->pf_block, 0, pfb) != cudaSuccess) return fail(MOE_ERR_CUDA);
     L->pf = prefill_carve(L->pf_block, H, I, E, k, Tm);
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return fail(MOE_ERR_CUDA);
+    L->encode_map = (TensorMapEncodeFn)fn;
+    if (!prefill_encode_maps(L->encode_map, L->pf, H, I, E, k, Tm, &L->pf_maps)) return fail(MOE_ERR_CUDA);
   }
   for (auto& cs : L->copy_stream)
     if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
@@ -599,7 +608,8 @@ moe_status_t moe_forward(moe_layer_t* L, const void* x, int32_t T, void* y, int3
   }
   if (a.pool) return MOE_ERR_UNSUPPORTED;  // the slot pool runs on the fused path only
   if (T > kMaxTokens) {
-    if (launch_prefill(a, L->pf, L->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (!prefill_encode_x(L->encode_map, x, L->d.hidden, T, &L->pf_maps)) return MOE_ERR_CUDA;
+    if (launch_prefill(a, L->pf, L->pf_maps, L->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
   const int Um = L->d.n_experts < T * L->d.top_k ? L->d.n_experts : T * L->d.top_k;

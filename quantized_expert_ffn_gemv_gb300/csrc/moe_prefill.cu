@@ -1,25 +1,33 @@
-// Prefill path (T > 64 tokens per call): the same layer as two grouped GEMMs
-// on the 5th-generation tensor cores.  Prefill is compute-bound where decode
-// is bandwidth-bound (halogen-flash-server README, section "Measured"), and a
+// Prefill path (T > 64 tokens per call): the layer as three GEMMs on the
+// 5th-generation tensor cores.  Prefill is compute-bound where decode is
+// bandwidth-bound (halogen-flash-server README, section "Measured"), and a
 // chunk's cost per token keeps falling up to a few thousand tokens (Basalt
 // README, section "Prompt chunks").
 //
-//   router     fp32 SIMT tiled GEMM: logits [T][E]; x -> fp16 rows
+//   prep       W_r (fp32) -> three bf16 pieces W0 + W1 + W2 (24 + bits, so
+//              the router keeps fp32 accuracy on bf16 tensor cores: x is
+//              bf16 already, each product is exact, sums are fp32);
+//              x -> fp16 rows for the expert GEMMs
+//   router     tcgen05 GEMM: logits [T][E] = sum of the three pieces' products
 //   top-k      warp per token: the k largest logits (ties to the lower
 //              index), ascending expert order, softmax over the selection;
-//              sets bit t of the expert's token bitmap
+//              bit t of the expert's token bitmap
+//   prefix     warp per expert: set bits before each bitmap word
 //   scan       per-expert counts -> pair offsets and 128-token chunks
-//   group      warp per expert: the expert's tokens in ascending order
-//              (a stable counting sort) -> (token, z row) pairs
-//   gate/up    tcgen05.mma kind::f16, cta_group::1, M = 128 (64 gate rows
-//              and the 64 matching up rows), N = the chunk's tokens (<= 128,
-//              rounded up to 16), K = H in steps of 64.  Eight producer warps
-//              dequantize 4-bit tiles to fp16 d*q and write them with
-//              stmatrix in the no-swizzle K-major core-matrix layout; one
-//              thread issues the MMAs into a double-buffered TMEM
-//              accumulator; four epilogue warps compute h = silu(g) * u.
-//   down       the same engine with M = 128 output rows and K = I; the
-//              epilogue writes each pair's expert output z as fp16.
+//   pairs      thread per (token, rank): its place in the expert's token
+//              list (ascending token: a stable counting sort)
+//   gate/up    grouped GEMM, M = 128 (64 gate rows and the 64 matching up
+//              rows), N = the chunk's tokens (<= 128, rounded up to 16),
+//              K = H in steps of 64.  One TMA warp streams the packed 4-bit
+//              tiles into shared memory (bulk copies) and gathers the
+//              chunk's activation rows (tile::gather4); eight warps
+//              dequantize the tiles to fp16 d*q and write them with stmatrix
+//              in the 128-byte-swizzled K-major layout; one thread issues the
+//              MMAs into a double-buffered TMEM accumulator; four epilogue
+//              warps compute h = silu(g) * u.
+//   down       the same engine, M = 128 output rows, K = I, B = the pairs'
+//              h rows (contiguous, tiled TMA); the epilogue writes each
+//              pair's expert output z as fp16.
 //   combine    y[t] = sum_j w_j z_j (ascending expert) + z_shared in fp32,
 //              rounded once to bf16.
 #include <cfloat>
@@ -42,18 +50,21 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -67,18 +78,6 @@ __device__ __forceinline__ uint4 ld_cg4(const void* p) {
   asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
 }
-__device__ __forceinline__ uint4 ld_nc4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
-               : "l"(p));
-  return r;
-}
-__device__ __forceinline__ uint2 ld_nc_u64(const void* p) {
-  uint2 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
-  return r;
-}
 // Four 8x8 b16 matrices from mma-fragment registers; lane l gives the shared
 // address of row (l & 7) of matrix (l >> 3).
 __device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
@@ -86,10 +85,38 @@ __device__ __forceinline__ void stmatrix_x4(uint32_t addr, uint32_t r0, uint32_t
                "r"(r2), "r"(r3)
                : "memory");
 }
+// 1-D bulk copy global -> shared, completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+// Four rows (r0..r3) x 64 elements at column c0 -> 512 consecutive shared bytes.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int c0, int r0, int r1, int r2,
+                                            int r3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4, %5, %6}], [%7];" ::"r"(dst),
+      "l"((uint64_t)map), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+      : "memory");
+}
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(
@@ -97,11 +124,9 @@ __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(acc)
       : "memory");
 }
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
-
 // 16 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
@@ -115,17 +140,21 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Shared-memory matrix descriptor, no swizzle, K-major: core matrices of
-// 8 rows x 16 bytes, `lbo` bytes apart along K and `sbo` bytes apart along
-// M (or N); bit 46 is the descriptor version.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 B
+// (64 fp16), 8-row atoms 1024 B apart, bit 46 = descriptor version, layout
+// type 2 = 128-byte swizzle.  A K-slice of 16 starts 32 B further.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  return (uint64_t)((saddr >> 4) & 0x3FFFu) | (1ull << 16) | ((uint64_t)(1024 >> 4) << 32) | (1ull << 46) |
+         (2ull << 61);
 }
-// Instruction descriptor of kind::f16: D f32, A and B f16, both K-major, M = 128.
-__device__ __forceinline__ uint32_t instr_desc(int n) {
-  return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+// Instruction descriptor of kind::f16: D f32, M = 128, N; A and B both f16
+// (bf16 = false) or both bf16, K-major.
+__device__ __forceinline__ uint32_t instr_desc(int n, bool bf16) {
+  return (1u << 4) | (bf16 ? ((1u << 7) | (1u << 10)) : 0u) | ((uint32_t)(n >> 3) << 17) |
+         ((uint32_t)(128 >> 4) << 24);
 }
+// Byte offset of 16-byte chunk c (k 8c .. 8c+7) of row r in a swizzled tile.
+__device__ __forceinline__ uint32_t sw128_off(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
 
 __device__ void set_error(const LayerArgs& a, int code) {
   atomicCAS(&a.st->error, 0, code);
@@ -134,7 +163,7 @@ __device__ void set_error(const LayerArgs& a, int code) {
   __threadfence_system();
 }
 
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, const LayerArgs& a, uint64_t deadline,
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const LayerArgs& a, uint64_t deadline,
                                          bool& ok) {
   if (!ok) return false;
   int spins = 0;
@@ -168,63 +197,36 @@ __device__ __forceinline__ void dequant_word(uint32_t w, __half2 (&q)[4]) {
 }
 __device__ __forceinline__ uint32_t h2u(__half2 v) { return *reinterpret_cast<uint32_t*>(&v); }
 
-// Byte offset of core-matrix row (r, k-core c) in a [rows][64] fp16 operand tile:
-// 8-row groups 1024 B apart, k-cores (8 elements) 128 B apart, rows 16 B apart.
-__device__ __forceinline__ uint32_t core_off(int r, int c) {
-  return (uint32_t)((r >> 3) * 1024 + c * 128 + (r & 7) * 16);
-}
+// ------------------------------------------------------------------ prep, top-k, grouping
 
-// ------------------------------------------------------------------ router, top-k, grouping
-
-constexpr int kRtTile = 64, kRtK = 32;
-
-// logits[t][e] = sum_h W_r[e][h] x[t][h] + bias[e]; 64 x 64 tile per CTA.
-__global__ void __launch_bounds__(256) prefill_router_kernel(LayerArgs a, PrefillArgs p) {
-  __shared__ __align__(16) float xs[kRtK][kRtTile + 4];
-  __shared__ __align__(16) float ws[kRtK][kRtTile + 4];
-  const int tid = threadIdx.x;
-  const int t0 = blockIdx.x * kRtTile, e0 = blockIdx.y * kRtTile;
-  const int H = a.H, E = a.E, T = a.T;
-  const int tr = (tid / 16) * 4, ec = (tid % 16) * 4;
-  float acc[4][4] = {};
+// W_r -> bf16 pieces (W = W0 + W1 + W2 up to 2^-27 relative) and x -> fp16.
+__global__ void __launch_bounds__(256) prefill_prep_kernel(LayerArgs a, PrefillArgs p) {
+  const size_t nw = (size_t)a.E * a.H, nx = (size_t)a.T * a.H;
+  const size_t stride = (size_t)gridDim.x * 256;
+  for (size_t i = (size_t)blockIdx.x * 256 + threadIdx.x; i < nw; i += stride) {
+    const float w = a.W_r[i];
+    const __nv_bfloat16 w0 = __float2bfloat16_rn(w);
+    const float r0 = w - __bfloat162float(w0);
+    const __nv_bfloat16 w1 = __float2bfloat16_rn(r0);
+    const __nv_bfloat16 w2 = __float2bfloat16_rn(r0 - __bfloat162float(w1));
+    p.w_split[i] = __bfloat16_as_ushort(w0);
+    p.w_split[nw + i] = __bfloat16_as_ushort(w1);
+    p.w_split[2 * nw + i] = __bfloat16_as_ushort(w2);
+  }
   int bad = 0;
-  for (int k0 = 0; k0 < H; k0 += kRtK) {
-    for (int i = tid; i < kRtTile * kRtK; i += 256) {
-      const int r = i / kRtK, kk = i % kRtK;
-      const int t = t0 + r, e = e0 + r;
-      float xv = 0.f;
-      if (t < T) {
-        const uint16_t bits = a.x[(size_t)t * H + k0 + kk];
-        xv = __uint_as_float((uint32_t)bits << 16);
-        if (blockIdx.y == 0) {
-          bad |= !(fabsf(xv) < 65504.f);
-          p.x16p[(size_t)t * H + k0 + kk] = __float2half_rn(xv);
-        }
-      }
-      xs[kk][r] = xv;
-      ws[kk][r] = (e < E) ? a.W_r[(size_t)e * H + k0 + kk] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kRtK; ++kk) {
-      const float4 xv = *reinterpret_cast<const float4*>(&xs[kk][tr]);
-      const float4 wv = *reinterpret_cast<const float4*>(&ws[kk][ec]);
-      const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+  for (size_t i = ((size_t)blockIdx.x * 256 + threadIdx.x) * 8; i < nx; i += stride * 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(a.x + i);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xa[i], wa[j], acc[i][j]);
+    for (int q = 0; q < 4; ++q) {
+      const float f0 = __uint_as_float(w[q] << 16), f1 = __uint_as_float(w[q] & 0xFFFF0000u);
+      bad |= !(fabsf(f0) < 65504.f) || !(fabsf(f1) < 65504.f);
+      o[q] = h2u(__floats2half2_rn(f0, f1));
     }
-    __syncthreads();
+    *reinterpret_cast<uint4*>(p.x16p + i) = make_uint4(o[0], o[1], o[2], o[3]);
   }
   if (bad) set_error(a, MOE_ERR_DEVICE);
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int t = t0 + tr + i, e = e0 + ec + j;
-      if (t < T && e < E) a.logits[(size_t)t * E + e] = acc[i][j] + (a.bias ? a.bias[e] : 0.f);
-    }
 }
 
 // Warp per token: k rounds of a warp argmax (value desc, index asc).
@@ -243,13 +245,19 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(LayerArgs a, PrefillA
     for (int e = lane, i = 0; e < E; e += 32, ++i) {
       if ((taken[i >> 5] >> (i & 31)) & 1u) continue;
       const float v = lt[e];
-      if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
+      if (v > bv || (v == bv && e < bi)) {
+        bv = v;
+        bi = e;
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
       const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
       const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+      if (ov > bv || (ov == bv && oi < bi)) {
+        bv = ov;
+        bi = oi;
+      }
     }
     if (bi == INT_MAX) {  // fewer than k comparable logits (NaN): flagged; keep the indices distinct
       if (lane == 0) set_error(a, MOE_ERR_DEVICE);
@@ -275,13 +283,35 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(LayerArgs a, PrefillA
     }
     float z = 0.f;
     for (int j = 0; j < k; ++j) z += expf(selv[j] - m);
-    const int words = (a.T + 31) >> 5;
     for (int j = 0; j < k; ++j) {
       a.topk_idx[t * k + j] = sel[j];
       a.topk_w[t * k + j] = expf(selv[j] - m) / z;
       atomicAdd(&p.counts[sel[j]], 1);
-      atomicOr(&p.bitmap[(size_t)sel[j] * words + (t >> 5)], 1u << (t & 31));
+      atomicOr(&p.bitmap[(size_t)sel[j] * p.words + (t >> 5)], 1u << (t & 31));
     }
+  }
+}
+
+// Warp per routed expert: prefix[e][w] = set bits of bitmap row e before word w.
+__global__ void __launch_bounds__(256) prefill_prefix_kernel(LayerArgs a, PrefillArgs p) {
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (e >= a.E) return;
+  const int words = (a.T + 31) >> 5;
+  const uint32_t* row = p.bitmap + (size_t)e * p.words;
+  int32_t* pre = p.prefix + (size_t)e * p.words;
+  int run = 0;
+  for (int w0 = 0; w0 < words; w0 += 32) {
+    const int w = w0 + lane;
+    const int c = (w < words) ? __popc(row[w]) : 0;
+    int incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (w < words) pre[w] = run + incl - c;
+    run += __shfl_sync(0xffffffffu, incl, 31);
   }
 }
 
@@ -349,72 +379,58 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(LayerArgs a, Prefill
   }
 }
 
-// Warp per expert list entry: its tokens in ascending order (a stable
-// counting sort of the (token, rank) pairs by expert).  Pair -> token and z
-// row t*(k+1) + rank; the shared expert's rank is k.  Clears the bitmap row.
-__global__ void __launch_bounds__(256) prefill_group_kernel(LayerArgs a, PrefillArgs p) {
-  const int lane = threadIdx.x & 31;
-  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int E = a.E, k = a.k, T = a.T;
-  if (e >= E + a.n_shared) return;
-  const int base = p.offsets[e];
-  if (e == E) {
-    for (int t = lane; t < T; t += 32) {
-      p.pair_token[base + t] = t;
-      p.pair_z[base + t] = t * (k + 1) + k;
-    }
-    return;
-  }
-  const int words = (T + 31) >> 5;
-  uint32_t* row = p.bitmap + (size_t)e * words;
-  int run = 0;
-  for (int w0 = 0; w0 < words; w0 += 32) {
-    const int w = w0 + lane;
-    const uint32_t bits = (w < words) ? row[w] : 0u;
-    if (bits) row[w] = 0u;
-    const int c = __popc(bits);
-    int incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int v = __shfl_up_sync(0xffffffffu, incl, o);
-      if (lane >= o) incl += v;
-    }
-    int pos = base + run + incl - c;
-    for (uint32_t b = bits; b; b &= b - 1) {
-      const int t = (w << 5) + __ffs(b) - 1;
-      int j = 0;
-      while (j < k - 1 && a.topk_idx[t * k + j] != e) ++j;
-      p.pair_token[pos] = t;
-      p.pair_z[pos] = t * (k + 1) + j;
-      ++pos;
-    }
-    run += __shfl_sync(0xffffffffu, incl, 31);
+// Thread per (t, rank j): place t in expert e's ascending token list.  The
+// shared expert's pairs are token t at offsets[E] + t, rank k.
+__global__ void __launch_bounds__(256) prefill_pairs_kernel(LayerArgs a, PrefillArgs p) {
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  const int T = a.T, k = a.k;
+  if (i < T * k) {
+    const int t = i / k, j = i - t * k;
+    const int e = a.topk_idx[i];
+    const size_t w = (size_t)e * p.words + (t >> 5);
+    const int pos = p.offsets[e] + p.prefix[w] + __popc(p.bitmap[w] & ((1u << (t & 31)) - 1u));
+    p.pair_token[pos] = t;
+    p.pair_z[pos] = t * (k + 1) + j;
+  } else if (a.n_shared && i < T * k + T) {
+    const int t = i - T * k;
+    const int pos = p.offsets[a.E] + t;
+    p.pair_token[pos] = t;
+    p.pair_z[pos] = t * (k + 1) + k;
   }
 }
 
-// ------------------------------------------------------------------ grouped GEMM on tcgen05
+// ------------------------------------------------------------------ GEMMs on tcgen05
 
-constexpr int kPfStages = 4;
-constexpr int kProducers = 8;  // warps 0-7: one 16-row weight strip each
-constexpr int kMmaWarp = 8;    // warp 8: allocates TMEM; lane 0 issues the MMAs
-constexpr int kEpi0 = 9;       // warps 9-12: epilogue, TMEM lane quadrant warp % 4
-constexpr int kPfThreads = (kEpi0 + 4) * 32;
-constexpr int kTileBytes = 128 * 64 * 2;  // one fp16 operand tile: 128 rows x 64 k
+constexpr int kTile = 128 * 128;  // one operand tile: 128 rows x 64 fp16/bf16 (128-byte rows)
+constexpr int kRaw = 8 * 512 + 8 * 64;  // packed 4-bit tile of 128 rows x 64 k: 8 strips of nibbles + scales
+constexpr int kTmaWarp = 0;
+constexpr int kDeq0 = 1;     // warps 1-8: dequantize one 16-row strip each
+constexpr int kMmaWarp = 9;  // allocates TMEM; lane 0 issues the MMAs
+constexpr int kEpi0 = 10;    // warps 10-13: epilogue; TMEM lane quadrant = warp % 4
+constexpr int kGemmThreads = (kEpi0 + 4) * 32;
 
-struct PfSmem {
-  unsigned char a[kPfStages][kTileBytes];
-  unsigned char b[kPfStages][kTileBytes];
-  uint64_t full[kPfStages], empty[kPfStages], acc_full[2], acc_empty[2], drain;
-  uint32_t tmem;
+// MODE 0 gate/up, 1 down: stages of [A tile][B tile][raw packed tile]
+// MODE 2 router: stages of [3 A tiles (weight pieces)][B tile]
+template <int MODE>
+struct Cfg {
+  static constexpr int kStages = MODE == 2 ? 3 : 5;
+  static constexpr int kA = MODE == 2 ? 3 * kTile : kTile;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kStages * kA;
+  static constexpr int kOffRaw = kOffB + kStages * kTile;
+  static constexpr int kOffBar = kOffRaw + (MODE == 2 ? 0 : kStages * kRaw);
+  // barriers: raw_full[S], b_full[S], a_full[S], empty[S], acc_full[2], acc_empty[2], drain
+  static constexpr int kOffTmem = kOffBar + 8 * (4 * kStages + 5);
+  static constexpr int kBytes = kOffTmem + 16 + 1024;  // + alignment slack
 };
 
 struct Task {
   int e, n0, nt, mb;
 };
 
-// Task t -> expert list entry e, first pair n0 of the chunk within e, its
-// tokens nt and the M-block.  M-blocks of one chunk are consecutive tasks,
-// so CTAs running them at once share the chunk's activation rows in L2.
+// Tasks of the grouped GEMMs: t -> expert list entry e, first pair n0 of the
+// chunk within e, its tokens nt and the M-block.  M-blocks of one chunk are
+// consecutive tasks, so CTAs running them at once share the chunk's rows in L2.
 __device__ __forceinline__ Task task_decode(const PrefillArgs& p, int NE, int MB, int t) {
   Task r;
   r.mb = t % MB;
@@ -433,147 +449,214 @@ __device__ __forceinline__ Task task_decode(const PrefillArgs& p, int NE, int MB
   r.nt = min(kPfN, cnt - r.n0);
   return r;
 }
+// Router tasks: t -> (M-block of 128 experts, 128-token block).
+__device__ __forceinline__ Task router_task(int E, int T, int t) {
+  const int MB = (E + 127) / 128;
+  Task r;
+  r.e = 0;
+  r.mb = t % MB;
+  r.n0 = (t / MB) * 128;
+  r.nt = min(128, T - r.n0);
+  return r;
+}
 
 // MODE 0: gate/up; M-block mb = intermediate rows 64 mb .. 64 mb + 63 of gate
 //   and of up, K = H.  Tile row of local gate row i: 16 (i / 8) + i % 8; the
 //   matching up row is 8 further, so an epilogue lane pairs with lane + 8.
 // MODE 1: down; M-block mb = output rows 128 mb .. 128 mb + 127, K = I.
+// MODE 2: router; M-block = 128 experts, N = 128 tokens, K = H, bf16 pieces.
 template <int MODE>
-__global__ void __launch_bounds__(kPfThreads, 1) prefill_gemm_kernel(LayerArgs a, PrefillArgs p) {
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    prefill_gemm_kernel(LayerArgs a, PrefillArgs p, const __grid_constant__ CUtensorMap mapA,
+                        const __grid_constant__ CUtensorMap mapB) {
+  using C = Cfg<MODE>;
+  constexpr int S = C::kStages;
   extern __shared__ __align__(1024) unsigned char smraw[];
-  PfSmem& S = *reinterpret_cast<PfSmem*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar0 = sbase + C::kOffBar;
+  auto raw_full = [&](int s) { return bar0 + 8u * s; };
+  auto b_full = [&](int s) { return bar0 + 8u * (S + s); };
+  auto a_full = [&](int s) { return bar0 + 8u * (2 * S + s); };
+  auto empty = [&](int s) { return bar0 + 8u * (3 * S + s); };
+  auto acc_full = [&](int b) { return bar0 + 8u * (4 * S + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (4 * S + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (4 * S + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmem);
+
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H, I = a.I, E = a.E;
   const int NE = E + a.n_shared;
-  const int MB = (MODE == 0) ? I / 64 : H / 128;
-  const int KS = (MODE == 0) ? H / 64 : I / 64;
-  const int n_tasks = ld_cg_i32(&p.n_chunks[0]) * MB;
+  const int MB = MODE == 0 ? I / 64 : MODE == 1 ? H / 128 : (E + 127) / 128;
+  const int KS = MODE == 1 ? I / 64 : H / 64;
+  const int n_tasks = MODE == 2 ? MB * ((a.T + 127) / 128) : ld_cg_i32(&p.n_chunks[0]) * MB;
   const uint64_t deadline = global_ns() + kPipeTimeoutNs;
   bool ok = true;
 
   if (tid == 0) {
-    for (int s = 0; s < kPfStages; ++s) {
-      mbar_init(&S.full[s], kProducers);
-      mbar_init(&S.empty[s], 1);
+    for (int s = 0; s < S; ++s) {
+      mbar_init(raw_full(s), 1);
+      mbar_init(b_full(s), 1);
+      mbar_init(a_full(s), 8);
+      mbar_init(empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(&S.acc_full[b], 1);
-      mbar_init(&S.acc_empty[b], 4);
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 4);
     }
-    mbar_init(&S.drain, 1);
+    mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kMmaWarp) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(&S.tmem)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(tmem_slot)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = S.tmem;
+  const uint32_t tmem = *tmem_slot;
 
-  if (warp < kProducers) {
-    // ---- producers: warp w dequantizes weight strip w of the A tile; all
-    //      eight gather the B tile
-    const int gg = lane >> 2;
-    const int Kdim = (MODE == 0) ? H : I;
-    const int R0 = (MODE == 0) ? 32 * (warp & 3) + 8 * (warp >> 2) : 16 * warp;  // tile row of strip row 0
-    const int rstep = (MODE == 0) ? 16 : 8;                                       // tile rows from g to g + 8
-    // stmatrix: matrix mi = lane >> 3 is (row g | g + 8) x (k-core 2 kt | 2 kt + 1)
-    const int mi = lane >> 3;
-    const uint32_t st_off = core_off(R0 + (lane & 7) + ((mi & 1) ? rstep : 0), mi >> 1);
-    int g = 0;  // k-steps produced so far
+  if (warp == kTmaWarp) {
+    // ---- loads: packed weight tiles (bulk copies) and B rows (tensor maps)
+    int g = 0;
     for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x) {
-      const Task tk = task_decode(p, NE, MB, t);
-      const uint8_t* base = (tk.e < E) ? a.arena + (int64_t)tk.e * a.blob : a.shared;
-      const uint8_t* sp;
-      if (MODE == 0)
-        sp = base + (int64_t)(tk.mb * 4 + (warp & 3)) * gu_strip_bytes(H) + ((warp >> 2) ? 9ll * H : 0);
-      else
-        sp = base + down_base(H, I) + (int64_t)(tk.mb * 8 + warp) * down_strip_bytes(I);
-      const int poff = ld_cg_i32(&p.offsets[tk.e]) + tk.n0;
-      const int nt = tk.nt;
-      for (int ks = 0; ks < KS; ++ks, ++g) {
-        const int s = g % kPfStages, use = g / kPfStages;
-        const uint4 nib = ld_nc4(sp + ks * 512 + lane * 16);
-        const uint2 sc = ld_nc_u64(sp + 8 * Kdim + ks * 64 + gg * 8);
-        if (use > 0 && !wait_bar(&S.empty[s], (use - 1) & 1, a, deadline, ok)) break;
-        const uint32_t sa = smem_u32(S.a[s]);
-        unsigned char* sb = S.b[s];
-        const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
+      const Task tk = MODE == 2 ? router_task(E, a.T, t) : task_decode(p, NE, MB, t);
+      const int nn = (tk.nt + 15) & ~15;
+      const uint8_t* src = nullptr;  // this lane's packed source (lanes 0-7 nibbles, 8-15 scales of strip lane % 8)
+      int tok[4] = {0, 0, 0, 0};
+      int poff = 0;
+      if (MODE != 2) {
+        const uint8_t* base = (tk.e < E) ? a.arena + (int64_t)tk.e * a.blob : a.shared;
+        const int strip = lane & 7;
+        const uint8_t* sp;
+        if (MODE == 0)
+          sp = base + (int64_t)(tk.mb * 4 + (strip & 3)) * gu_strip_bytes(H) + ((strip >> 2) ? 9ll * H : 0);
+        else
+          sp = base + down_base(H, I) + (int64_t)(tk.mb * 8 + strip) * down_strip_bytes(I);
+        src = (lane < 8) ? sp : sp + 8 * (MODE == 0 ? H : I);
+        poff = ld_cg_i32(&p.offsets[tk.e]) + tk.n0;
+        if (MODE == 0 && 4 * lane < nn) {
 #pragma unroll
-        for (int kt = 0; kt < 4; ++kt) {
-          const uint32_t scw = (kt < 2) ? sc.x : sc.y;  // k-tiles 0, 1: block 2 ks; 2, 3: block 2 ks + 1
-          const __half2 dg = __half2half2(__ushort_as_half((uint16_t)(scw & 0xFFFFu)));
-          const __half2 dg8 = __half2half2(__ushort_as_half((uint16_t)(scw >> 16)));
-          __half2 q[4];
-          dequant_word(words[kt], q);
-          stmatrix_x4(sa + st_off + (uint32_t)(kt * 256), h2u(__hmul2(q[0], dg)), h2u(__hmul2(q[1], dg8)),
-                      h2u(__hmul2(q[2], dg)), h2u(__hmul2(q[3], dg8)));
-        }
-        // B: rows n < nt in 16-byte k-cores; lanes 0-7 of a phase take 8 rows of one k-core
-        const int nrow8 = (nt + 7) >> 3;
-        for (int i = tid; i < nrow8 * 64; i += kProducers * 32) {
-          const int n = (i & 7) + 8 * (i >> 6), c = (i >> 3) & 7;
-          if (n < nt) {
-            const __half* src;
-            if (MODE == 0) {
-              const int tok = ld_cg_i32(&p.pair_token[poff + n]);
-              src = p.x16p + (size_t)tok * H + ks * 64 + c * 8;
-            } else {
-              src = p.h16p + (size_t)(poff + n) * I + ks * 64 + c * 8;
-            }
-            *reinterpret_cast<uint4*>(sb + core_off(n, c)) = ld_cg4(src);
+          for (int q = 0; q < 4; ++q) {
+            const int n = min(4 * lane + q, tk.nt - 1);
+            tok[q] = ld_cg_i32(&p.pair_token[poff + n]);
           }
         }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.full[s]);
       }
+      for (int ks = 0; ks < KS; ++ks, ++g) {
+        const int s = g % S, use = g / S;
+        if (lane == 0 && use > 0) wait_bar(empty(s), (use - 1) & 1, a, deadline, ok);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t sA = sbase + C::kOffA + s * C::kA, sB = sbase + C::kOffB + s * kTile;
+        if (MODE == 2) {
+          if (lane == 0) {
+            mbar_expect_tx(b_full(s), 4 * kTile);
+#pragma unroll
+            for (int pc = 0; pc < 3; ++pc) tma_3d(sA + pc * kTile, &mapA, ks * 64, tk.mb * 128, pc, b_full(s));
+            tma_2d(sB, &mapB, ks * 64, tk.n0, b_full(s));
+          }
+        } else {
+          if (lane == 0) {
+            mbar_expect_tx(raw_full(s), kRaw);
+            mbar_expect_tx(b_full(s), (uint32_t)nn * 128);
+          }
+          __syncwarp();
+          const uint32_t sRaw = sbase + C::kOffRaw + s * kRaw;
+          if (lane < 8)
+            bulk_g2s(sRaw + lane * 512, src + ks * 512, 512, raw_full(s));
+          else if (lane < 16)
+            bulk_g2s(sRaw + 4096 + (lane - 8) * 64, src + ks * 64, 64, raw_full(s));
+          if (MODE == 0) {
+            if (4 * lane < nn) tma_gather4(sB + lane * 512, &mapB, ks * 64, tok[0], tok[1], tok[2], tok[3], b_full(s));
+          } else {
+            if (16 * lane < nn) tma_2d(sB + lane * 2048, &mapB, ks * 64, poff + 16 * lane, b_full(s));
+          }
+        }
+      }
+    }
+  } else if (MODE != 2 && warp >= kDeq0 && warp < kDeq0 + 8) {
+    // ---- dequantize strip w of the packed tile into the swizzled fp16 A tile
+    const int w = warp - kDeq0;
+    const int gg = lane >> 2;
+    const int R0 = (MODE == 0) ? 32 * (w & 3) + 8 * (w >> 2) : 16 * w;  // tile row of strip row 0
+    const int rstep = (MODE == 0) ? 16 : 8;                              // tile rows from g to g + 8
+    // stmatrix: matrix mi = lane >> 3 is (row g | g + 8) x (low | high 8 k of the k-tile)
+    const int mi = lane >> 3;
+    const int st_row = R0 + (lane & 7) + ((mi & 1) ? rstep : 0);
+    int my_tasks = 0;
+    for (int t = blockIdx.x; t < n_tasks; t += gridDim.x) ++my_tasks;
+    const int steps = my_tasks * KS;
+    for (int g = 0; g < steps && ok; ++g) {
+      const int s = g % S, use = g / S;
+      if (!wait_bar(raw_full(s), use & 1, a, deadline, ok)) break;
+      const unsigned char* raw = sm + C::kOffRaw + s * kRaw;
+      const uint4 nib = *reinterpret_cast<const uint4*>(raw + w * 512 + lane * 16);
+      const uint2 sc = *reinterpret_cast<const uint2*>(raw + 4096 + w * 64 + gg * 8);
+      const uint32_t sA = sbase + C::kOffA + s * C::kA;
+      const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
+#pragma unroll
+      for (int kt = 0; kt < 4; ++kt) {
+        const uint32_t scw = (kt < 2) ? sc.x : sc.y;  // k-tiles 0, 1: first block of 32; 2, 3: second
+        const __half2 dg = __half2half2(__ushort_as_half((uint16_t)(scw & 0xFFFFu)));
+        const __half2 dg8 = __half2half2(__ushort_as_half((uint16_t)(scw >> 16)));
+        __half2 q[4];
+        dequant_word(words[kt], q);
+        stmatrix_x4(sA + sw128_off(st_row, 2 * kt + (mi >> 1)), h2u(__hmul2(q[0], dg)), h2u(__hmul2(q[1], dg8)),
+                    h2u(__hmul2(q[2], dg)), h2u(__hmul2(q[3], dg8)));
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(a_full(s));
     }
   } else if (warp == kMmaWarp) {
     // ---- MMA issue: one thread, double-buffered accumulator (2 x 128 columns)
     if (lane == 0) {
       int g = 0, i = 0;
       for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x, ++i) {
-        const Task tk = task_decode(p, NE, MB, t);
-        const uint32_t idesc = instr_desc((tk.nt + 15) & ~15);
+        const Task tk = MODE == 2 ? router_task(E, a.T, t) : task_decode(p, NE, MB, t);
+        const uint32_t idesc = instr_desc((tk.nt + 15) & ~15, MODE == 2);
         const int b = i & 1, ub = i >> 1;
-        if (ub > 0 && !wait_bar(&S.acc_empty[b], (ub - 1) & 1, a, deadline, ok)) break;
+        if (ub > 0 && !wait_bar(acc_empty(b), (ub - 1) & 1, a, deadline, ok)) break;
         tc_fence_after();
         const uint32_t dt = tmem + (uint32_t)(b * 128);
         for (int ks = 0; ks < KS; ++ks, ++g) {
-          const int s = g % kPfStages, use = g / kPfStages;
-          if (!wait_bar(&S.full[s], use & 1, a, deadline, ok)) break;
+          const int s = g % S, use = g / S;
+          if (!wait_bar(b_full(s), use & 1, a, deadline, ok)) break;
+          if (MODE != 2 && !wait_bar(a_full(s), use & 1, a, deadline, ok)) break;
           tc_fence_after();
-          const uint32_t sa = smem_u32(S.a[s]), sb = smem_u32(S.b[s]);
+          const uint32_t sA = sbase + C::kOffA + s * C::kA, sB = sbase + C::kOffB + s * kTile;
 #pragma unroll
-          for (int j = 0; j < 4; ++j)
-            tc_mma(dt, smem_desc(sa + j * 256, 128, 1024), smem_desc(sb + j * 256, 128, 1024), idesc,
-                   (ks > 0 || j > 0) ? 1u : 0u);
-          tc_commit(&S.empty[s]);
+          for (int pc = 0; pc < (MODE == 2 ? 3 : 1); ++pc)
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              tc_mma(dt, desc_sw128(sA + pc * kTile + j * 32), desc_sw128(sB + j * 32), idesc,
+                     (ks > 0 || j > 0 || pc > 0) ? 1u : 0u);
+          tc_commit(empty(s));
         }
         if (!ok) break;
-        tc_commit(&S.acc_full[b]);
+        tc_commit(acc_full(b));
       }
       // every MMA this thread issued completes before TMEM is released
-      tc_commit(&S.drain);
+      tc_commit(drain);
       bool dok = true;
-      wait_bar(&S.drain, 0, a, deadline + kPipeTimeoutNs, dok);
+      wait_bar(drain, 0, a, deadline + kPipeTimeoutNs, dok);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= kEpi0) {
     // ---- epilogue: TMEM lanes 32 (warp % 4) .. + 31 are tile rows
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     int i = 0;
     for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x, ++i) {
-      const Task tk = task_decode(p, NE, MB, t);
+      const Task tk = MODE == 2 ? router_task(E, a.T, t) : task_decode(p, NE, MB, t);
       const int b = i & 1, ub = i >> 1;
-      if (!wait_bar(&S.acc_full[b], ub & 1, a, deadline, ok)) break;
+      if (!wait_bar(acc_full(b), ub & 1, a, deadline, ok)) break;
       tc_fence_after();
-      const int poff = ld_cg_i32(&p.offsets[tk.e]) + tk.n0;
+      const int poff = MODE == 2 ? 0 : ld_cg_i32(&p.offsets[tk.e]) + tk.n0;
       const uint32_t taddr = tmem + (uint32_t)(b * 128) + ((uint32_t)(quad * 32) << 16);
+      const int e = tk.mb * 128 + row;
+      const float bias = (MODE == 2 && a.bias && e < E) ? a.bias[e] : 0.f;
       for (int c0 = 0; c0 < tk.nt; c0 += 16) {
         float v[16];
         tc_ld16(taddr + (uint32_t)c0, v);
@@ -588,19 +671,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_gemm_kernel(LayerArgs a
               p.h16p[(size_t)(poff + c0 + j) * I + fi] = __float2half_rn(gv / (1.0f + expf(-gv)) * u);
             }
           }
-        } else {
-          const int orow = tk.mb * 128 + row;
+        } else if (MODE == 1) {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
             if (c0 + j < tk.nt) {
               const int zr = ld_cg_i32(&p.pair_z[poff + c0 + j]);
-              p.z16[(size_t)zr * H + orow] = __float2half_rn(v[j]);
+              p.z16[(size_t)zr * H + e] = __float2half_rn(v[j]);
             }
+        } else {
+          if (e < E) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < tk.nt) a.logits[(size_t)(tk.n0 + c0 + j) * E + e] = v[j] + bias;
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&S.acc_empty[b]);
+      if (lane == 0) mbar_arrive(acc_empty(b));
     }
   }
   tc_fence_before();
@@ -645,9 +733,15 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(LayerArgs a, Prefi
   *reinterpret_cast<uint4*>(a.y + (size_t)t * H + c8) = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-constexpr size_t kGemmSmem = sizeof(PfSmem) + 1024;
-
 size_t pf_align(size_t b) { return (b + 255) & ~size_t(255); }
+
+bool encode(TensorMapEncodeFn enc, CUtensorMap* m, CUtensorMapDataType dt, int rank, const void* base,
+            const cuuint64_t* dims, const cuuint64_t* strides, const cuuint32_t* box) {
+  const cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, dt, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 }  // namespace
 
@@ -655,7 +749,8 @@ size_t prefill_scratch_bytes(int H, int I, int E, int k, int Tm) {
   if (Tm <= kMaxTokens) return 0;
   const size_t P = (size_t)Tm * (k + 1), words = (size_t)(Tm + 31) / 32;
   return pf_align(4ull * (E + 1)) + 2 * pf_align(4ull * (E + 2)) + pf_align(4) + 2 * pf_align(4 * P) +
-         pf_align(2ull * Tm * H) + pf_align(2 * P * I) + pf_align(2 * P * H) + pf_align(4ull * E * words);
+         2 * pf_align(4ull * E * words) + pf_align(6ull * E * H) + pf_align(2ull * Tm * H) + pf_align(2 * P * I) +
+         pf_align(2 * P * H);
 }
 
 PrefillArgs prefill_carve(void* block, int H, int I, int E, int k, int Tm) {
@@ -674,29 +769,71 @@ PrefillArgs prefill_carve(void* block, int H, int I, int E, int k, int Tm) {
   p.n_chunks = (int32_t*)carve(4);
   p.pair_token = (int32_t*)carve(4 * P);
   p.pair_z = (int32_t*)carve(4 * P);
+  p.bitmap = (uint32_t*)carve(4ull * E * words);
+  p.prefix = (int32_t*)carve(4ull * E * words);
+  p.w_split = (uint16_t*)carve(6ull * E * H);
   p.x16p = (__half*)carve(2ull * Tm * H);
   p.h16p = (__half*)carve(2 * P * I);
   p.z16 = (__half*)carve(2 * P * H);
-  p.bitmap = (uint32_t*)carve(4ull * E * words);
+  p.words = (int)words;
   return p;
 }
 
-cudaError_t prefill_configure() {
-  cudaError_t e =
-      cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+bool prefill_encode_maps(TensorMapEncodeFn enc, const PrefillArgs& p, int H, int I, int E, int k, int Tm,
+                         PrefillMaps* m) {
+  const cuuint64_t P = (cuuint64_t)Tm * (k + 1);
+  {
+    const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)E, 3};
+    const cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)E * H * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    if (!encode(enc, &m->w_split, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.w_split, dims, strides, box)) return false;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)Tm};
+    const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+    const cuuint32_t box[2] = {64, 1};
+    if (!encode(enc, &m->x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x16p, dims, strides, box)) return false;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)I, P};
+    const cuuint64_t strides[1] = {(cuuint64_t)I * 2};
+    const cuuint32_t box[2] = {64, 16};
+    if (!encode(enc, &m->h16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.h16p, dims, strides, box)) return false;
+  }
+  return true;
 }
 
-cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, int sm_count, cudaStream_t s) {
+bool prefill_encode_x(TensorMapEncodeFn enc, const void* x, int H, int T, PrefillMaps* m) {
+  const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T};
+  const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
+  const cuuint32_t box[2] = {64, 128};
+  return encode(enc, &m->x_bf16, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, dims, strides, box);
+}
+
+cudaError_t prefill_configure() {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<0>::kBytes)))
+    return e;
+  if ((e = cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<1>::kBytes)))
+    return e;
+  return cudaFuncSetAttribute(prefill_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<2>::kBytes);
+}
+
+cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, const PrefillMaps& m, int sm_count,
+                           cudaStream_t s) {
   cudaError_t e;
   if ((e = cudaMemsetAsync(p.counts, 0, sizeof(int32_t) * (size_t)(a.E + 1), s)) != cudaSuccess) return e;
-  prefill_router_kernel<<<dim3((a.T + kRtTile - 1) / kRtTile, (a.E + kRtTile - 1) / kRtTile), 256, 0, s>>>(a, p);
+  if ((e = cudaMemsetAsync(p.bitmap, 0, sizeof(uint32_t) * (size_t)a.E * p.words, s)) != cudaSuccess) return e;
+  prefill_prep_kernel<<<sm_count * 4, 256, 0, s>>>(a, p);
+  const int router_tasks = ((a.E + 127) / 128) * ((a.T + 127) / 128);
+  prefill_gemm_kernel<2><<<router_tasks < sm_count ? router_tasks : sm_count, kGemmThreads, Cfg<2>::kBytes, s>>>(
+      a, p, m.w_split, m.x_bf16);
   prefill_topk_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a, p);
+  prefill_prefix_kernel<<<(a.E + 7) / 8, 256, 0, s>>>(a, p);
   prefill_scan_kernel<<<1, 1024, 0, s>>>(a, p);
-  prefill_group_kernel<<<(a.E + a.n_shared + 7) / 8, 256, 0, s>>>(a, p);
-  prefill_gemm_kernel<0><<<sm_count, kPfThreads, kGemmSmem, s>>>(a, p);
-  prefill_gemm_kernel<1><<<sm_count, kPfThreads, kGemmSmem, s>>>(a, p);
+  prefill_pairs_kernel<<<(a.T * (a.k + 1) + 255) / 256, 256, 0, s>>>(a, p);
+  prefill_gemm_kernel<0><<<sm_count, kGemmThreads, Cfg<0>::kBytes, s>>>(a, p, m.x16, m.x16);
+  prefill_gemm_kernel<1><<<sm_count, kGemmThreads, Cfg<1>::kBytes, s>>>(a, p, m.h16, m.h16);
   const long long n = (long long)a.T * (a.H / 8);
   prefill_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, p);
   return cudaGetLastError();

@@ -1,11 +1,13 @@
-// Prefill path (T > 64): per-call scratch and launch entry (moe_prefill.cu).
+// Prefill path (T > 64): per-call scratch, tensor maps and launch entry (moe_prefill.cu).
 #pragma once
+
+#include <cuda.h>
 
 #include "moe_internal.h"
 
 namespace moe {
 
-constexpr int kPfN = 128;               // tokens per GEMM chunk (the MMA's N, at most)
+constexpr int kPfN = 128;                // tokens per GEMM chunk (the MMA's N, at most)
 constexpr int kMaxPrefillTokens = 8192;  // largest T of one prefill call
 
 // Scratch of the prefill kernels.  Pairs are (token, rank) assignments; the
@@ -15,19 +17,39 @@ struct PrefillArgs {
   int32_t* offsets;     // [E + 2] first pair of each expert list entry; [NE] = total
   int32_t* chunk_off;   // [E + 2] first 128-token chunk of each entry; [NE] = total
   int32_t* n_chunks;    // [1]
-  int32_t* pair_token;  // [T*k + T] token of each pair, grouped by expert
+  int32_t* pair_token;  // [T*k + T] token of each pair, grouped by expert, ascending token
   int32_t* pair_z;      // [T*k + T] z row of each pair: t*(k+1) + rank (rank k = shared)
-  __half* x16p;         // [T][H] fp16 activations, natural order
-  __half* h16p;         // [T*k + T][I] fp16 h of each pair, natural order
+  uint32_t* bitmap;     // [E][ceil(T/32)] bit t of row e: token t selected e (zeroed each call)
+  int32_t* prefix;      // [E][ceil(T/32)] set bits of row e in the words before each word
+  uint16_t* w_split;    // [3][E][H] bf16 pieces of the router weights: W = W0 + W1 + W2
+  __half* x16p;         // [T][H] fp16 activations
+  __half* h16p;         // [T*k + T][I] fp16 h of each pair
   __half* z16;          // [T*(k+1)][H] fp16 expert outputs before the weighting
-  uint32_t* bitmap;     // [E][ceil(T/32)] bit t of row e: token t selected e (cleared after use)
+  int words;            // ceil(max_tokens / 32): row stride of bitmap and prefix
 };
+
+// TMA descriptors (128-byte swizzle, fp16/bf16, 64-element boxes along K).
+struct PrefillMaps {
+  CUtensorMap w_split;  // [3][E][H] bf16, box 64 x 128 x 1
+  CUtensorMap x16;      // [Tmax][H] fp16, box 64 x 1 (row gathers)
+  CUtensorMap h16;      // [pairs max][I] fp16, box 64 x 16
+  CUtensorMap x_bf16;   // the call's x [T][H] bf16, box 64 x 128 (encoded per call)
+};
+
+typedef CUresult (*TensorMapEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                      const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                      CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 // Bytes of prefill scratch for up to Tm tokens (0 when Tm <= kMaxTokens).
 size_t prefill_scratch_bytes(int H, int I, int E, int k, int Tm);
 // Carve PrefillArgs from a device block of prefill_scratch_bytes() bytes.
 PrefillArgs prefill_carve(void* block, int H, int I, int E, int k, int Tm);
+// The fixed tensor maps of the scratch buffers (x_bf16 is left for the call).
+bool prefill_encode_maps(TensorMapEncodeFn enc, const PrefillArgs& p, int H, int I, int E, int k, int Tm,
+                         PrefillMaps* m);
+bool prefill_encode_x(TensorMapEncodeFn enc, const void* x, int H, int T, PrefillMaps* m);
 cudaError_t prefill_configure();
-cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, int sm_count, cudaStream_t s);
+cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, const PrefillMaps& m, int sm_count,
+                           cudaStream_t s);
 
 }  // namespace moe

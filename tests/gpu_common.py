@@ -7,6 +7,12 @@ from quantized_expert_ffn_gemv_gb300 import synth
 REL_L2 = 2e-3   # per token row
 MAX_ABS = 5e-3  # every element
 W_RTOL = 1e-5   # routing weights (fp32 softmax vs binary64)
+# Routing weights when the router runs on the tensor cores (prefill): the
+# logits are sums of 2048 exact bf16 x bf16 products accumulated by the MMA
+# unit in fp32 without IEEE round-to-nearest at every step; the logit error
+# is about 1e-5 (100x inside the 1e-3 near-tie gap), so a weight may move
+# by twice that relative.
+W_RTOL_TC = 1e-4
 
 
 def to_torch_bf16(x_u16, device="cuda"):
@@ -48,12 +54,12 @@ def run(layer, x_u16, T=None):
     return y, idx, w
 
 
-def check_against_oracle(L, x_u16, y, idx, w, rows=None):
+def check_against_oracle(L, x_u16, y, idx, w, rows=None, w_rtol=W_RTOL):
     sh = L.shape
     rows = np.arange(x_u16.shape[0]) if rows is None else np.asarray(rows)
     ref = oracle.moe_forward(sh.H, sh.I, sh.E, sh.k, L.W_r, L.bias, L.experts, L.shared, x_u16[rows])
     assert np.array_equal(idx[rows], ref["idx"]), "routing differs from the oracle"
-    assert np.allclose(w[rows], ref["w"], rtol=W_RTOL, atol=1e-7)
+    assert np.allclose(w[rows], ref["w"], rtol=w_rtol, atol=1e-7)
     yg = synth.bf16_to_f32(y[rows]).astype(np.float64)
     r = ref["y"]
     err = yg - r
