@@ -398,6 +398,8 @@ def main():
                     help="decode: one page-scale layer, batch 1 (default); stack: 48-layer stack with a 25%% "
                          "pool; prefill: one 4096-token chunk")
     ap.add_argument("--layers", type=int, default=48, help="stack depth for --workload stack")
+    ap.add_argument("--replicas", type=int, default=REPLICAS,
+                    help="decode: identical layer copies cycled round-robin (8 keeps every reuse out of L2)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 256 if args.workload == "stack" else 10
@@ -425,7 +427,7 @@ def main():
 
     L = synth.make_layer(synth.PAGE, layer=0)
     layers = [moe.MoeLayer(L.shape, L.W_r, L.bias, L.experts, L.shared, max_tokens=1, device=local)
-              for _ in range(REPLICAS)]
+              for _ in range(args.replicas)]
     ntok = args.tokens
     x_host = L_tokens(L, 0, ntok)
     x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
@@ -436,7 +438,7 @@ def main():
 
     def step():
         for t in range(ntok):
-            layers[t % REPLICAS].forward(xd[t:t + 1], yd[t:t + 1])
+            layers[t % len(layers)].forward(xd[t:t + 1], yd[t:t + 1])
 
     with torch.cuda.stream(stream):
         step()
@@ -504,8 +506,9 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16xf16+f32 (4-bit weights)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens_per_step": ntok, "replicas": REPLICAS,
-                   "l2": "inputs larger than L2 (8 layer replicas, 7.25 GB of expert weights, round-robin)",
+        "config": {"workload": WORKLOAD, "tokens_per_step": ntok, "replicas": len(layers),
+                   "l2": f"inputs larger than L2 ({len(layers)} layer replicas, "
+                         f"{len(layers) * E * EXPERT_BYTES / 2**30:.2f} GiB of expert weights, round-robin)",
                    "parallelism": f"replicas x{ws}"},
         "roofline": {"bound": "hbm", "kernel": "moe_decode_kernel (fused route + hit check + gate/up + down)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,

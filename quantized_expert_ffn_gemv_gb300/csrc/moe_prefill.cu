@@ -18,16 +18,16 @@
 //              list (ascending token: a stable counting sort)
 //   gate/up    grouped GEMM, M = 128 (64 gate rows and the 64 matching up
 //              rows), N = the chunk's tokens (<= 128, rounded up to 16),
-//              K = H in steps of 64.  One TMA warp streams the packed 4-bit
-//              tiles into shared memory (bulk copies) and gathers the
-//              chunk's activation rows (tile::gather4); eight warps
-//              dequantize the tiles to fp16 d*q and write them with stmatrix
-//              in the 128-byte-swizzled K-major layout; one thread issues the
-//              MMAs into a double-buffered TMEM accumulator; four epilogue
-//              warps compute h = silu(g) * u.
+//              K = H in steps of 64.  One warp streams the packed 4-bit
+//              tiles into shared memory (bulk copies, four k-steps each);
+//              eight warps dequantize them to fp16 d*q, written with stmatrix
+//              in the 128-byte-swizzled K-major layout, and gather the
+//              chunk's activation rows with cp.async two k-steps ahead; one
+//              thread issues the MMAs into a double-buffered TMEM
+//              accumulator; four epilogue warps compute h = silu(g) * u.
 //   down       the same engine, M = 128 output rows, K = I, B = the pairs'
-//              h rows (contiguous, tiled TMA); the epilogue writes each
-//              pair's expert output z as fp16.
+//              h rows; the epilogue writes each pair's expert output z as
+//              fp16.
 //   combine    y[t] = sum_j w_j z_j (ascending expert) + z_shared in fp32,
 //              rounded once to bf16.
 #include <cfloat>
@@ -105,16 +105,6 @@ __device__ __forceinline__ void tma_3d(uint32_t dst, const CUtensorMap* map, int
       "l"((uint64_t)map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
-// Four rows (r0..r3) x 64 elements at column c0 -> 512 consecutive shared bytes.
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int c0, int r0, int r1, int r2,
-                                            int r3, uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
-      "%4, %5, %6}], [%7];" ::"r"(dst),
-      "l"((uint64_t)map), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
-      : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t acc) {
@@ -366,6 +356,7 @@ __global__ void __launch_bounds__(1024) prefill_scan_kernel(LayerArgs a, Prefill
       const int cnt = (e < E) ? p.counts[e] : a.T;
       p.offsets[e] = oa;
       p.chunk_off[e] = ob;
+      for (int c = 0; c * kPfN < cnt; ++c) p.chunk_rec[ob + c] = make_int4(e, oa + c * kPfN, min(kPfN, cnt - c * kPfN), 0);
       oa += cnt;
       ob += (cnt + kPfN - 1) / kPfN;
     }
@@ -402,102 +393,55 @@ __global__ void __launch_bounds__(256) prefill_pairs_kernel(LayerArgs a, Prefill
 // ------------------------------------------------------------------ GEMMs on tcgen05
 
 constexpr int kTile = 128 * 128;  // one operand tile: 128 rows x 64 fp16/bf16 (128-byte rows)
-constexpr int kRaw = 8 * 512 + 8 * 64;  // packed 4-bit tile of 128 rows x 64 k: 8 strips of nibbles + scales
-constexpr int kTmaWarp = 0;
-constexpr int kDeq0 = 1;     // warps 1-8: dequantize one 16-row strip each
-constexpr int kMmaWarp = 9;  // allocates TMEM; lane 0 issues the MMAs
-constexpr int kEpi0 = 10;    // warps 10-13: epilogue; TMEM lane quadrant = warp % 4
+constexpr int kMmaWarp = 9;       // allocates TMEM; lane 0 issues the MMAs
+constexpr int kEpi0 = 10;         // warps 10-13: epilogue; TMEM lane quadrant = warp % 4
 constexpr int kGemmThreads = (kEpi0 + 4) * 32;
 
-// MODE 0 gate/up, 1 down: stages of [A tile][B tile][raw packed tile]
-// MODE 2 router: stages of [3 A tiles (weight pieces)][B tile]
-template <int MODE>
-struct Cfg {
-  static constexpr int kStages = MODE == 2 ? 3 : 5;
-  static constexpr int kA = MODE == 2 ? 3 * kTile : kTile;
-  static constexpr int kOffA = 0;
-  static constexpr int kOffB = kStages * kA;
-  static constexpr int kOffRaw = kOffB + kStages * kTile;
-  static constexpr int kOffBar = kOffRaw + (MODE == 2 ? 0 : kStages * kRaw);
-  // barriers: raw_full[S], b_full[S], a_full[S], empty[S], acc_full[2], acc_empty[2], drain
-  static constexpr int kOffTmem = kOffBar + 8 * (4 * kStages + 5);
-  static constexpr int kBytes = kOffTmem + 16 + 1024;  // + alignment slack
-};
-
-struct Task {
-  int e, n0, nt, mb;
-};
-
-// Tasks of the grouped GEMMs: t -> expert list entry e, first pair n0 of the
-// chunk within e, its tokens nt and the M-block.  M-blocks of one chunk are
-// consecutive tasks, so CTAs running them at once share the chunk's rows in L2.
-__device__ __forceinline__ Task task_decode(const PrefillArgs& p, int NE, int MB, int t) {
-  Task r;
-  r.mb = t % MB;
-  const int ch = t / MB;
-  int lo = 0, hi = NE;  // the largest e with chunk_off[e] <= ch
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (ld_cg_i32(&p.chunk_off[mid]) <= ch)
-      lo = mid;
-    else
-      hi = mid;
-  }
-  r.e = lo;
-  r.n0 = (ch - ld_cg_i32(&p.chunk_off[lo])) * kPfN;
-  const int cnt = ld_cg_i32(&p.offsets[lo + 1]) - ld_cg_i32(&p.offsets[lo]);
-  r.nt = min(kPfN, cnt - r.n0);
+__device__ __forceinline__ int4 ld_cg_int4(const int4* p) {
+  int4 r;
+  asm volatile("ld.global.cg.v4.s32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
 }
-// Router tasks: t -> (M-block of 128 experts, 128-token block).
-__device__ __forceinline__ Task router_task(int E, int T, int t) {
-  const int MB = (E + 127) / 128;
-  Task r;
-  r.e = 0;
-  r.mb = t % MB;
-  r.n0 = (t / MB) * 128;
-  r.nt = min(128, T - r.n0);
-  return r;
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+// Arrive on `bar` once every cp.async this thread issued so far has landed
+// (the barrier's expected count includes these arrivals).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-// MODE 0: gate/up; M-block mb = intermediate rows 64 mb .. 64 mb + 63 of gate
-//   and of up, K = H.  Tile row of local gate row i: 16 (i / 8) + i % 8; the
-//   matching up row is 8 further, so an epilogue lane pairs with lane + 8.
-// MODE 1: down; M-block mb = output rows 128 mb .. 128 mb + 127, K = I.
-// MODE 2: router; M-block = 128 experts, N = 128 tokens, K = H, bf16 pieces.
-template <int MODE>
+// ---- router GEMM: M-block = 128 experts, N = 128 tokens, K = H; A = the
+//      three bf16 pieces of W_r, B = x, both by TMA; logits = acc + bias.
+//      Warp 0 loads, warp 9 issues, warps 10-13 drain.
+constexpr int kRtStages = 3;
+constexpr int kRtOffB = kRtStages * 3 * kTile;
+constexpr int kRtOffBar = kRtOffB + kRtStages * kTile;
+constexpr int kRtOffTmem = kRtOffBar + 8 * (2 * kRtStages + 5);
+constexpr int kRtSmem = kRtOffTmem + 16 + 1024;
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
-    prefill_gemm_kernel(LayerArgs a, PrefillArgs p, const __grid_constant__ CUtensorMap mapA,
-                        const __grid_constant__ CUtensorMap mapB) {
-  using C = Cfg<MODE>;
-  constexpr int S = C::kStages;
+    prefill_router_kernel(LayerArgs a, const __grid_constant__ CUtensorMap mapW, const __grid_constant__ CUtensorMap mapX) {
+  constexpr int S = kRtStages;
   extern __shared__ __align__(1024) unsigned char smraw[];
   unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(sm);
-  const uint32_t bar0 = sbase + C::kOffBar;
-  auto raw_full = [&](int s) { return bar0 + 8u * s; };
-  auto b_full = [&](int s) { return bar0 + 8u * (S + s); };
-  auto a_full = [&](int s) { return bar0 + 8u * (2 * S + s); };
-  auto empty = [&](int s) { return bar0 + 8u * (3 * S + s); };
-  auto acc_full = [&](int b) { return bar0 + 8u * (4 * S + b); };
-  auto acc_empty = [&](int b) { return bar0 + 8u * (4 * S + 2 + b); };
-  const uint32_t drain = bar0 + 8u * (4 * S + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + C::kOffTmem);
-
+  const uint32_t bar0 = sbase + kRtOffBar;
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (S + s); };
+  auto acc_full = [&](int b) { return bar0 + 8u * (2 * S + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (2 * S + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (2 * S + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kRtOffTmem);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int H = a.H, I = a.I, E = a.E;
-  const int NE = E + a.n_shared;
-  const int MB = MODE == 0 ? I / 64 : MODE == 1 ? H / 128 : (E + 127) / 128;
-  const int KS = MODE == 1 ? I / 64 : H / 64;
-  const int n_tasks = MODE == 2 ? MB * ((a.T + 127) / 128) : ld_cg_i32(&p.n_chunks[0]) * MB;
+  const int E = a.E, T = a.T;
+  const int MB = (E + 127) / 128, KS = a.H / 64;
+  const int n_tasks = MB * ((T + 127) / 128);
   const uint64_t deadline = global_ns() + kPipeTimeoutNs;
   bool ok = true;
-
   if (tid == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(raw_full(s), 1);
-      mbar_init(b_full(s), 1);
-      mbar_init(a_full(s), 8);
+      mbar_init(full(s), 1);
       mbar_init(empty(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -516,118 +460,39 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == kTmaWarp) {
-    // ---- loads: packed weight tiles (bulk copies) and B rows (tensor maps)
-    int g = 0;
-    for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x) {
-      const Task tk = MODE == 2 ? router_task(E, a.T, t) : task_decode(p, NE, MB, t);
-      const int nn = (tk.nt + 15) & ~15;
-      const uint8_t* src = nullptr;  // this lane's packed source (lanes 0-7 nibbles, 8-15 scales of strip lane % 8)
-      int tok[4] = {0, 0, 0, 0};
-      int poff = 0;
-      if (MODE != 2) {
-        const uint8_t* base = (tk.e < E) ? a.arena + (int64_t)tk.e * a.blob : a.shared;
-        const int strip = lane & 7;
-        const uint8_t* sp;
-        if (MODE == 0)
-          sp = base + (int64_t)(tk.mb * 4 + (strip & 3)) * gu_strip_bytes(H) + ((strip >> 2) ? 9ll * H : 0);
-        else
-          sp = base + down_base(H, I) + (int64_t)(tk.mb * 8 + strip) * down_strip_bytes(I);
-        src = (lane < 8) ? sp : sp + 8 * (MODE == 0 ? H : I);
-        poff = ld_cg_i32(&p.offsets[tk.e]) + tk.n0;
-        if (MODE == 0 && 4 * lane < nn) {
+  if (warp == 0) {
+    if (lane == 0) {
+      int g = 0;
+      for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x) {
+        const int mb = t % MB, n0 = (t / MB) * 128;
+        for (int ks = 0; ks < KS; ++ks, ++g) {
+          const int s = g % S, use = g / S;
+          if (use > 0 && !wait_bar(empty(s), (use - 1) & 1, a, deadline, ok)) break;
+          const uint32_t sA = sbase + s * 3 * kTile, sB = sbase + kRtOffB + s * kTile;
+          mbar_expect_tx(full(s), 4 * kTile);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int n = min(4 * lane + q, tk.nt - 1);
-            tok[q] = ld_cg_i32(&p.pair_token[poff + n]);
-          }
+          for (int pc = 0; pc < 3; ++pc) tma_3d(sA + pc * kTile, &mapW, ks * 64, mb * 128, pc, full(s));
+          tma_2d(sB, &mapX, ks * 64, n0, full(s));
         }
       }
-      for (int ks = 0; ks < KS; ++ks, ++g) {
-        const int s = g % S, use = g / S;
-        if (lane == 0 && use > 0) wait_bar(empty(s), (use - 1) & 1, a, deadline, ok);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const uint32_t sA = sbase + C::kOffA + s * C::kA, sB = sbase + C::kOffB + s * kTile;
-        if (MODE == 2) {
-          if (lane == 0) {
-            mbar_expect_tx(b_full(s), 4 * kTile);
-#pragma unroll
-            for (int pc = 0; pc < 3; ++pc) tma_3d(sA + pc * kTile, &mapA, ks * 64, tk.mb * 128, pc, b_full(s));
-            tma_2d(sB, &mapB, ks * 64, tk.n0, b_full(s));
-          }
-        } else {
-          if (lane == 0) {
-            mbar_expect_tx(raw_full(s), kRaw);
-            mbar_expect_tx(b_full(s), (uint32_t)nn * 128);
-          }
-          __syncwarp();
-          const uint32_t sRaw = sbase + C::kOffRaw + s * kRaw;
-          if (lane < 8)
-            bulk_g2s(sRaw + lane * 512, src + ks * 512, 512, raw_full(s));
-          else if (lane < 16)
-            bulk_g2s(sRaw + 4096 + (lane - 8) * 64, src + ks * 64, 64, raw_full(s));
-          if (MODE == 0) {
-            if (4 * lane < nn) tma_gather4(sB + lane * 512, &mapB, ks * 64, tok[0], tok[1], tok[2], tok[3], b_full(s));
-          } else {
-            if (16 * lane < nn) tma_2d(sB + lane * 2048, &mapB, ks * 64, poff + 16 * lane, b_full(s));
-          }
-        }
-      }
-    }
-  } else if (MODE != 2 && warp >= kDeq0 && warp < kDeq0 + 8) {
-    // ---- dequantize strip w of the packed tile into the swizzled fp16 A tile
-    const int w = warp - kDeq0;
-    const int gg = lane >> 2;
-    const int R0 = (MODE == 0) ? 32 * (w & 3) + 8 * (w >> 2) : 16 * w;  // tile row of strip row 0
-    const int rstep = (MODE == 0) ? 16 : 8;                              // tile rows from g to g + 8
-    // stmatrix: matrix mi = lane >> 3 is (row g | g + 8) x (low | high 8 k of the k-tile)
-    const int mi = lane >> 3;
-    const int st_row = R0 + (lane & 7) + ((mi & 1) ? rstep : 0);
-    int my_tasks = 0;
-    for (int t = blockIdx.x; t < n_tasks; t += gridDim.x) ++my_tasks;
-    const int steps = my_tasks * KS;
-    for (int g = 0; g < steps && ok; ++g) {
-      const int s = g % S, use = g / S;
-      if (!wait_bar(raw_full(s), use & 1, a, deadline, ok)) break;
-      const unsigned char* raw = sm + C::kOffRaw + s * kRaw;
-      const uint4 nib = *reinterpret_cast<const uint4*>(raw + w * 512 + lane * 16);
-      const uint2 sc = *reinterpret_cast<const uint2*>(raw + 4096 + w * 64 + gg * 8);
-      const uint32_t sA = sbase + C::kOffA + s * C::kA;
-      const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
-#pragma unroll
-      for (int kt = 0; kt < 4; ++kt) {
-        const uint32_t scw = (kt < 2) ? sc.x : sc.y;  // k-tiles 0, 1: first block of 32; 2, 3: second
-        const __half2 dg = __half2half2(__ushort_as_half((uint16_t)(scw & 0xFFFFu)));
-        const __half2 dg8 = __half2half2(__ushort_as_half((uint16_t)(scw >> 16)));
-        __half2 q[4];
-        dequant_word(words[kt], q);
-        stmatrix_x4(sA + sw128_off(st_row, 2 * kt + (mi >> 1)), h2u(__hmul2(q[0], dg)), h2u(__hmul2(q[1], dg8)),
-                    h2u(__hmul2(q[2], dg)), h2u(__hmul2(q[3], dg8)));
-      }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(a_full(s));
     }
   } else if (warp == kMmaWarp) {
-    // ---- MMA issue: one thread, double-buffered accumulator (2 x 128 columns)
     if (lane == 0) {
       int g = 0, i = 0;
       for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x, ++i) {
-        const Task tk = MODE == 2 ? router_task(E, a.T, t) : task_decode(p, NE, MB, t);
-        const uint32_t idesc = instr_desc((tk.nt + 15) & ~15, MODE == 2);
+        const int nt = min(128, T - (t / MB) * 128);
+        const uint32_t idesc = instr_desc((nt + 15) & ~15, true);
         const int b = i & 1, ub = i >> 1;
         if (ub > 0 && !wait_bar(acc_empty(b), (ub - 1) & 1, a, deadline, ok)) break;
         tc_fence_after();
         const uint32_t dt = tmem + (uint32_t)(b * 128);
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int s = g % S, use = g / S;
-          if (!wait_bar(b_full(s), use & 1, a, deadline, ok)) break;
-          if (MODE != 2 && !wait_bar(a_full(s), use & 1, a, deadline, ok)) break;
+          if (!wait_bar(full(s), use & 1, a, deadline, ok)) break;
           tc_fence_after();
-          const uint32_t sA = sbase + C::kOffA + s * C::kA, sB = sbase + C::kOffB + s * kTile;
+          const uint32_t sA = sbase + s * 3 * kTile, sB = sbase + kRtOffB + s * kTile;
 #pragma unroll
-          for (int pc = 0; pc < (MODE == 2 ? 3 : 1); ++pc)
+          for (int pc = 0; pc < 3; ++pc)
 #pragma unroll
             for (int j = 0; j < 4; ++j)
               tc_mma(dt, desc_sw128(sA + pc * kTile + j * 32), desc_sw128(sB + j * 32), idesc,
@@ -637,53 +502,30 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ok) break;
         tc_commit(acc_full(b));
       }
-      // every MMA this thread issued completes before TMEM is released
       tc_commit(drain);
       bool dok = true;
       wait_bar(drain, 0, a, deadline + kPipeTimeoutNs, dok);
     }
     __syncwarp();
   } else if (warp >= kEpi0) {
-    // ---- epilogue: TMEM lanes 32 (warp % 4) .. + 31 are tile rows
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     int i = 0;
     for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x, ++i) {
-      const Task tk = MODE == 2 ? router_task(E, a.T, t) : task_decode(p, NE, MB, t);
+      const int mb = t % MB, n0 = (t / MB) * 128, nt = min(128, T - n0);
       const int b = i & 1, ub = i >> 1;
       if (!wait_bar(acc_full(b), ub & 1, a, deadline, ok)) break;
       tc_fence_after();
-      const int poff = MODE == 2 ? 0 : ld_cg_i32(&p.offsets[tk.e]) + tk.n0;
       const uint32_t taddr = tmem + (uint32_t)(b * 128) + ((uint32_t)(quad * 32) << 16);
-      const int e = tk.mb * 128 + row;
-      const float bias = (MODE == 2 && a.bias && e < E) ? a.bias[e] : 0.f;
-      for (int c0 = 0; c0 < tk.nt; c0 += 16) {
+      const int e = mb * 128 + row;
+      const float bias = (a.bias && e < E) ? a.bias[e] : 0.f;
+      for (int c0 = 0; c0 < nt; c0 += 16) {
         float v[16];
         tc_ld16(taddr + (uint32_t)c0, v);
-        if (MODE == 0) {
-          const bool gate = (row & 8) == 0;
-          const int fi = tk.mb * 64 + 8 * (row >> 4) + (row & 7);
-#pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float u = __shfl_xor_sync(0xffffffffu, v[j], 8);
-            if (gate && c0 + j < tk.nt) {
-              const float gv = v[j];
-              p.h16p[(size_t)(poff + c0 + j) * I + fi] = __float2half_rn(gv / (1.0f + expf(-gv)) * u);
-            }
-          }
-        } else if (MODE == 1) {
+        if (e < E) {
 #pragma unroll
           for (int j = 0; j < 16; ++j)
-            if (c0 + j < tk.nt) {
-              const int zr = ld_cg_i32(&p.pair_z[poff + c0 + j]);
-              p.z16[(size_t)zr * H + e] = __float2half_rn(v[j]);
-            }
-        } else {
-          if (e < E) {
-#pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < tk.nt) a.logits[(size_t)(tk.n0 + c0 + j) * E + e] = v[j] + bias;
-          }
+            if (c0 + j < nt) a.logits[(size_t)(n0 + c0 + j) * E + e] = v[j] + bias;
         }
       }
       tc_fence_before();
@@ -695,6 +537,325 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == kMmaWarp) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+}
+
+// ---- grouped expert GEMMs.
+// Warp 0 (lanes 0-15): bulk copies of the packed 4-bit tiles, kRawR k-steps
+//   per copy and strip, into a ring of kRawStages raw stages.
+// Warps 1-16 (producers): warp pw dequantizes k-tiles 2 (pw / 8) and
+//   2 (pw / 8) + 1 of strip pw % 8 into the swizzled fp16 A tile (stmatrix)
+//   and signals a_full; all 512 threads gather the chunk's B rows with
+//   cp.async kLook k-steps ahead, each signalling b_full when its copies
+//   land.  A and B have rings of their own (kAStages, kBStages): the B ring
+//   is deep to cover the gather latency, the A ring only the MMA's lag.  The
+//   MMA thread orders both (generic-proxy writes) before its tensor-core
+//   reads with one proxy fence after its waits.
+// Warp 17: TMEM allocation; lane 0 issues the MMAs (2 x 128 TMEM columns).
+// Warps 18-21: epilogue (TMEM lane quadrant warp % 4).
+constexpr int kAStages = 3;
+constexpr int kBStages = 8;
+constexpr int kLook = 5;
+constexpr int kRawR = 4;
+constexpr int kRawStages = 2;
+constexpr int kProd = 16;
+constexpr int kXMmaWarp = 1 + kProd;
+constexpr int kXEpi0 = kXMmaWarp + 1;
+constexpr int kExpThreads = (kXEpi0 + 4) * 32;
+constexpr int kRawBytes = 8 * kRawR * (512 + 64);
+constexpr int kOffB = kAStages * kTile;
+constexpr int kOffRaw = kOffB + kBStages * kTile;
+constexpr int kNumBars = 2 * kRawStages + 2 * kAStages + 2 * kBStages + 5;
+constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
+constexpr int kOffTmem = kOffBar + 8 * kNumBars;
+constexpr int kGemmSmem = kOffTmem + 16 + 1024;
+static_assert(kLook + kAStages <= kBStages, "a B stage is refilled only after the MMA released it");
+
+struct Task {
+  int e, poff, nt, mb;
+};
+// Task t: chunk t / MB (its record: expert list entry, first pair, tokens)
+// and M-block t % MB.  The M-blocks of one chunk are consecutive tasks, so
+// CTAs running them at once share the chunk's B rows in L2.
+__device__ __forceinline__ Task load_task(const PrefillArgs& p, int MB, int t) {
+  const int4 r = ld_cg_int4(&p.chunk_rec[t / MB]);
+  return Task{r.x, r.y, r.z, t % MB};
+}
+
+// MODE 0: gate/up; M-block mb = intermediate rows 64 mb .. 64 mb + 63 of gate
+//   and of up, K = H.  Tile row of local gate row i: 16 (i / 8) + i % 8; the
+//   matching up row is 8 further, so an epilogue lane pairs with lane ^ 8.
+// MODE 1: down; M-block mb = output rows 128 mb .. 128 mb + 127, K = I.
+template <int MODE>
+__global__ void __launch_bounds__(kExpThreads, 1) prefill_expert_kernel(LayerArgs a, PrefillArgs p) {
+  extern __shared__ __align__(1024) unsigned char smraw[];
+  unsigned char* sm = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar0 = sbase + kOffBar;
+  auto raw_full = [&](int r) { return bar0 + 8u * r; };
+  auto raw_empty = [&](int r) { return bar0 + 8u * (kRawStages + r); };
+  auto a_full = [&](int s) { return bar0 + 8u * (2 * kRawStages + s); };
+  auto a_empty = [&](int s) { return bar0 + 8u * (2 * kRawStages + kAStages + s); };
+  auto b_empty = [&](int s) { return bar0 + 8u * (2 * kRawStages + 2 * kAStages + s); };
+  auto b_full = [&](int s) { return bar0 + 8u * (2 * kRawStages + 2 * kAStages + kBStages + s); };
+  const int acc0 = 2 * kRawStages + 2 * kAStages + 2 * kBStages;
+  auto acc_full = [&](int b) { return bar0 + 8u * (acc0 + b); };
+  auto acc_empty = [&](int b) { return bar0 + 8u * (acc0 + 2 + b); };
+  const uint32_t drain = bar0 + 8u * (acc0 + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kOffTmem);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int H = a.H, I = a.I, E = a.E;
+  const int MB = MODE == 0 ? I / 64 : H / 128;
+  const int KS = MODE == 0 ? H / 64 : I / 64;
+  const int Kdim = MODE == 0 ? H : I;
+  const int n_tasks = ld_cg_i32(&p.n_chunks[0]) * MB;
+  const uint64_t deadline = global_ns() + kPipeTimeoutNs;
+  bool ok = true;
+
+  if (tid == 0) {
+    for (int r = 0; r < kRawStages; ++r) {
+      mbar_init(raw_full(r), 1);
+      mbar_init(raw_empty(r), kProd);
+    }
+    for (int s = 0; s < kAStages; ++s) {
+      mbar_init(a_full(s), kProd);
+      mbar_init(a_empty(s), 1);
+    }
+    for (int s = 0; s < kBStages; ++s) {
+      mbar_init(b_empty(s), 1);
+      mbar_init(b_full(s), kProd * 32);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(acc_full(b), 1);
+      mbar_init(acc_empty(b), 4);
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == kXMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(tmem_slot)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ---- packed tiles: lanes 0-7 the nibbles of strip lane, 8-15 its scales
+    int rb = 0;
+    for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x) {
+      const Task tk = load_task(p, MB, t);
+      const uint8_t* base = (tk.e < E) ? a.arena + (int64_t)tk.e * a.blob : a.shared;
+      const int strip = lane & 7;
+      const uint8_t* sp;
+      if (MODE == 0)
+        sp = base + (int64_t)(tk.mb * 4 + (strip & 3)) * gu_strip_bytes(H) + ((strip >> 2) ? 9ll * H : 0);
+      else
+        sp = base + down_base(H, I) + (int64_t)(tk.mb * 8 + strip) * down_strip_bytes(I);
+      for (int ks0 = 0; ks0 < KS; ks0 += kRawR, ++rb) {
+        const int len = min(kRawR, KS - ks0);
+        const int r = rb % kRawStages, use = rb / kRawStages;
+        if (lane == 0 && use > 0) wait_bar(raw_empty(r), (use - 1) & 1, a, deadline, ok);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        if (lane == 0) mbar_expect_tx(raw_full(r), (uint32_t)(8 * len * (512 + 64)));
+        __syncwarp();
+        const uint32_t sRaw = sbase + kOffRaw + r * kRawBytes;
+        if (lane < 8)
+          bulk_g2s(sRaw + lane * (kRawR * 512), sp + ks0 * 512, len * 512, raw_full(r));
+        else if (lane < 16)
+          bulk_g2s(sRaw + 8 * kRawR * 512 + strip * (kRawR * 64), sp + 8 * Kdim + ks0 * 64, len * 64, raw_full(r));
+      }
+    }
+  } else if (warp <= kProd) {
+    // ---- producers
+    const int pw = warp - 1, pt = tid - 32;
+    const int strip = pw & 7, half = pw >> 3;  // k-tiles 2 half, 2 half + 1 of the strip
+    const int gg = lane >> 2;
+    const int R0 = (MODE == 0) ? 32 * (strip & 3) + 8 * (strip >> 2) : 16 * strip;  // tile row of strip row 0
+    const int rstep = (MODE == 0) ? 16 : 8;  // tile rows from g to g + 8
+    const int mi = lane >> 3;  // stmatrix matrix: (row g | g + 8) x (low | high 8 k of the k-tile)
+    const int st_row = R0 + (lane & 7) + ((mi & 1) ? rstep : 0);
+    const uint32_t st_off0 = sw128_off(st_row, 4 * half + (mi >> 1)), st_off1 = sw128_off(st_row, 4 * half + 2 + (mi >> 1));
+    const int bc = pt & 7;  // B: 16-byte chunk of rows (pt >> 3) + 64 q
+    // B cursor, kLook k-steps ahead of the A cursor: task bt, k-step bks; the
+    // next task's record and token ids are fetched half a task early
+    int bt = blockIdx.x, bks = 0, gb = 0;
+    Task ntk{};
+    const __half* brow[2] = {nullptr, nullptr};
+    int ntok[2] = {0, 0};
+    auto fetch_tokens = [&](const Task& tk, int (&tok)[2]) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int n = (pt >> 3) + 64 * q;
+        tok[q] = (MODE == 0 && n < tk.nt) ? ld_cg_i32(&p.pair_token[tk.poff + n]) : 0;
+      }
+    };
+    auto set_rows = [&](const Task& tk, const int (&tok)[2]) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int n = (pt >> 3) + 64 * q;
+        brow[q] = n >= tk.nt ? nullptr
+                             : (MODE == 0 ? p.x16p + (size_t)tok[q] * H : p.h16p + (size_t)(tk.poff + n) * I);
+      }
+    };
+    if (bt < n_tasks) {
+      const Task btk = load_task(p, MB, bt);
+      int tok[2];
+      fetch_tokens(btk, tok);
+      set_rows(btk, tok);
+      if (bt + (int)gridDim.x < n_tasks) ntk = load_task(p, MB, bt + gridDim.x);
+    }
+    auto issue_b = [&]() {
+      if (bt < n_tasks && ok) {
+        const int s = gb % kBStages;
+        if (gb >= kBStages) wait_bar(b_empty(s), (gb / kBStages - 1) & 1, a, deadline, ok);
+        const uint32_t sB = sbase + kOffB + s * kTile;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (brow[q]) cp_async16(sB + sw128_off((pt >> 3) + 64 * q, bc), brow[q] + bks * 64 + bc * 8);
+        cp_async_arrive_noinc(b_full(s));
+        ++gb;
+        if (bks == KS / 2 && bt + (int)gridDim.x < n_tasks) fetch_tokens(ntk, ntok);
+        if (++bks == KS) {
+          bks = 0;
+          bt += gridDim.x;
+          if (bt < n_tasks) {
+            set_rows(ntk, ntok);  // token ids fetched at k-step KS / 2 of the task before
+            if (bt + (int)gridDim.x < n_tasks) ntk = load_task(p, MB, bt + gridDim.x);
+          }
+        }
+      }
+    };
+#pragma unroll
+    for (int i = 0; i < kLook; ++i) issue_b();
+    int rb = 0, g = 0;
+    for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x) {
+      for (int ks = 0; ks < KS && ok; ++ks, ++g) {
+        issue_b();  // k-step g + kLook
+        const int j = ks % kRawR;
+        const int r = rb % kRawStages;
+        if (j == 0 && !wait_bar(raw_full(r), (rb / kRawStages) & 1, a, deadline, ok)) break;
+        const unsigned char* raw = sm + kOffRaw + r * kRawBytes;
+        const uint2 nib = *reinterpret_cast<const uint2*>(raw + (strip * kRawR + j) * 512 + lane * 16 + half * 8);
+        const uint32_t scw =
+            *reinterpret_cast<const uint32_t*>(raw + 8 * kRawR * 512 + (strip * kRawR + j) * 64 + gg * 8 + half * 4);
+        const int len = min(kRawR, KS - (ks - j));
+        if (j == len - 1) {  // the raw stage is consumed (this warp's part is in registers)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(raw_empty(r));
+          ++rb;
+        }
+        const int s = g % kAStages;
+        if (g >= kAStages && !wait_bar(a_empty(s), (g / kAStages - 1) & 1, a, deadline, ok)) break;
+        const uint32_t sA = sbase + s * kTile;
+        // both k-tiles share this lane's block scales (k-tiles 0, 1: block 2 ks; 2, 3: block 2 ks + 1)
+        const __half2 dg = __half2half2(__ushort_as_half((uint16_t)(scw & 0xFFFFu)));
+        const __half2 dg8 = __half2half2(__ushort_as_half((uint16_t)(scw >> 16)));
+        __half2 q0[4], q1[4];
+        dequant_word(nib.x, q0);
+        dequant_word(nib.y, q1);
+        stmatrix_x4(sA + st_off0, h2u(__hmul2(q0[0], dg)), h2u(__hmul2(q0[1], dg8)), h2u(__hmul2(q0[2], dg)),
+                    h2u(__hmul2(q0[3], dg8)));
+        stmatrix_x4(sA + st_off1, h2u(__hmul2(q1[0], dg)), h2u(__hmul2(q1[1], dg8)), h2u(__hmul2(q1[2], dg)),
+                    h2u(__hmul2(q1[3], dg8)));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(a_full(s));
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == kXMmaWarp) {
+    // ---- MMA issue: one thread, double-buffered accumulator (2 x 128 columns)
+    if (lane == 0) {
+      int g = 0, i = 0;
+      Task nxt = blockIdx.x < n_tasks ? load_task(p, MB, blockIdx.x) : Task{};
+      for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x, ++i) {
+        const Task tk = nxt;
+        if (t + (int)gridDim.x < n_tasks) nxt = load_task(p, MB, t + gridDim.x);
+        const uint32_t idesc = instr_desc((tk.nt + 15) & ~15, false);
+        const int b = i & 1, ub = i >> 1;
+        if (ub > 0 && !wait_bar(acc_empty(b), (ub - 1) & 1, a, deadline, ok)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem + (uint32_t)(b * 128);
+        for (int ks = 0; ks < KS; ++ks, ++g) {
+          const int sa = g % kAStages, sb = g % kBStages;
+          if (!wait_bar(a_full(sa), (g / kAStages) & 1, a, deadline, ok)) break;
+          if (!wait_bar(b_full(sb), (g / kBStages) & 1, a, deadline, ok)) break;
+          // the stage was written through the generic proxy (stmatrix, cp.async)
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          tc_fence_after();
+          const uint32_t sA = sbase + sa * kTile, sB = sbase + kOffB + sb * kTile;
+#pragma unroll
+          for (int j = 0; j < 4; ++j)
+            tc_mma(dt, desc_sw128(sA + j * 32), desc_sw128(sB + j * 32), idesc, (ks > 0 || j > 0) ? 1u : 0u);
+          tc_commit(a_empty(sa));
+          tc_commit(b_empty(sb));
+        }
+        if (!ok) break;
+        tc_commit(acc_full(b));
+      }
+      // every MMA this thread issued completes before TMEM is released
+      tc_commit(drain);
+      bool dok = true;
+      wait_bar(drain, 0, a, deadline + kPipeTimeoutNs, dok);
+    }
+    __syncwarp();
+  } else {
+    // ---- epilogue: TMEM lanes 32 (warp % 4) .. + 31 are tile rows
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    int i = 0;
+    Task nxt = blockIdx.x < n_tasks ? load_task(p, MB, blockIdx.x) : Task{};
+    for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x, ++i) {
+      const Task tk = nxt;
+      if (t + (int)gridDim.x < n_tasks) nxt = load_task(p, MB, t + gridDim.x);
+      int zq[4];  // MODE 1: z rows of the chunk's pairs lane + 32 q
+      if (MODE == 1) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) zq[q] = (lane + 32 * q < tk.nt) ? ld_cg_i32(&p.pair_z[tk.poff + lane + 32 * q]) : 0;
+      }
+      const int b = i & 1, ub = i >> 1;
+      if (!wait_bar(acc_full(b), ub & 1, a, deadline, ok)) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem + (uint32_t)(b * 128) + ((uint32_t)(quad * 32) << 16);
+      for (int c0 = 0; c0 < tk.nt; c0 += 16) {
+        float v[16];
+        tc_ld16(taddr + (uint32_t)c0, v);
+        if (MODE == 0) {
+          // lanes l (gate row) and l ^ 8 (its up row) swap values; the gate lane
+          // finishes the even columns, the up lane the odd ones
+          const bool up = (row & 8) != 0;
+          const int fi = tk.mb * 64 + 8 * (row >> 4) + (row & 7);
+          __half* hrow = p.h16p + (size_t)(tk.poff + c0) * I + fi;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float o = __shfl_xor_sync(0xffffffffu, v[j], 8);
+            if ((j & 1) == (up ? 1 : 0) && c0 + j < tk.nt) {
+              const float gv = up ? o : v[j], uv = up ? v[j] : o;
+              hrow[(size_t)j * I] = __float2half_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
+            }
+          }
+        } else {
+          const int orow = tk.mb * 128 + row;
+          const int zsrc = (c0 >> 5);
+          const int zsel = zsrc == 0 ? zq[0] : zsrc == 1 ? zq[1] : zsrc == 2 ? zq[2] : zq[3];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int zr = __shfl_sync(0xffffffffu, zsel, (c0 + j) & 31);
+            if (c0 + j < tk.nt) p.z16[(size_t)zr * H + orow] = __float2half_rn(v[j]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(b));
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kXMmaWarp) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
 }
 
 // y[t][r] = sum_j w_tj z[t][j][r] in ascending expert order, + z[t][k][r]; 8 outputs per thread.
@@ -748,7 +909,9 @@ bool encode(TensorMapEncodeFn enc, CUtensorMap* m, CUtensorMapDataType dt, int r
 size_t prefill_scratch_bytes(int H, int I, int E, int k, int Tm) {
   if (Tm <= kMaxTokens) return 0;
   const size_t P = (size_t)Tm * (k + 1), words = (size_t)(Tm + 31) / 32;
-  return pf_align(4ull * (E + 1)) + 2 * pf_align(4ull * (E + 2)) + pf_align(4) + 2 * pf_align(4 * P) +
+  const size_t chunks = (size_t)E + 2 + P / kPfN;
+  return pf_align(4ull * (E + 1)) + 2 * pf_align(4ull * (E + 2)) + pf_align(4) + pf_align(16 * chunks) +
+         2 * pf_align(4 * P) +
          2 * pf_align(4ull * E * words) + pf_align(6ull * E * H) + pf_align(2ull * Tm * H) + pf_align(2 * P * I) +
          pf_align(2 * P * H);
 }
@@ -767,6 +930,7 @@ PrefillArgs prefill_carve(void* block, int H, int I, int E, int k, int Tm) {
   p.offsets = (int32_t*)carve(4ull * (E + 2));
   p.chunk_off = (int32_t*)carve(4ull * (E + 2));
   p.n_chunks = (int32_t*)carve(4);
+  p.chunk_rec = (int4*)carve(16 * ((size_t)E + 2 + P / kPfN));
   p.pair_token = (int32_t*)carve(4 * P);
   p.pair_z = (int32_t*)carve(4 * P);
   p.bitmap = (uint32_t*)carve(4ull * E * words);
@@ -781,26 +945,13 @@ PrefillArgs prefill_carve(void* block, int H, int I, int E, int k, int Tm) {
 
 bool prefill_encode_maps(TensorMapEncodeFn enc, const PrefillArgs& p, int H, int I, int E, int k, int Tm,
                          PrefillMaps* m) {
-  const cuuint64_t P = (cuuint64_t)Tm * (k + 1);
-  {
-    const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)E, 3};
-    const cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)E * H * 2};
-    const cuuint32_t box[3] = {64, 128, 1};
-    if (!encode(enc, &m->w_split, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.w_split, dims, strides, box)) return false;
-  }
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)Tm};
-    const cuuint64_t strides[1] = {(cuuint64_t)H * 2};
-    const cuuint32_t box[2] = {64, 1};
-    if (!encode(enc, &m->x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.x16p, dims, strides, box)) return false;
-  }
-  {
-    const cuuint64_t dims[2] = {(cuuint64_t)I, P};
-    const cuuint64_t strides[1] = {(cuuint64_t)I * 2};
-    const cuuint32_t box[2] = {64, 16};
-    if (!encode(enc, &m->h16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p.h16p, dims, strides, box)) return false;
-  }
-  return true;
+  (void)I;
+  (void)k;
+  (void)Tm;
+  const cuuint64_t dims[3] = {(cuuint64_t)H, (cuuint64_t)E, 3};
+  const cuuint64_t strides[2] = {(cuuint64_t)H * 2, (cuuint64_t)E * H * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  return encode(enc, &m->w_split, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, p.w_split, dims, strides, box);
 }
 
 bool prefill_encode_x(TensorMapEncodeFn enc, const void* x, int H, int T, PrefillMaps* m) {
@@ -812,11 +963,11 @@ bool prefill_encode_x(TensorMapEncodeFn enc, const void* x, int H, int T, Prefil
 
 cudaError_t prefill_configure() {
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(prefill_gemm_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<0>::kBytes)))
+  if ((e = cudaFuncSetAttribute(prefill_expert_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem)))
     return e;
-  if ((e = cudaFuncSetAttribute(prefill_gemm_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<1>::kBytes)))
+  if ((e = cudaFuncSetAttribute(prefill_expert_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem)))
     return e;
-  return cudaFuncSetAttribute(prefill_gemm_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<2>::kBytes);
+  return cudaFuncSetAttribute(prefill_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
 }
 
 cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, const PrefillMaps& m, int sm_count,
@@ -826,14 +977,14 @@ cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, const Prefi
   if ((e = cudaMemsetAsync(p.bitmap, 0, sizeof(uint32_t) * (size_t)a.E * p.words, s)) != cudaSuccess) return e;
   prefill_prep_kernel<<<sm_count * 4, 256, 0, s>>>(a, p);
   const int router_tasks = ((a.E + 127) / 128) * ((a.T + 127) / 128);
-  prefill_gemm_kernel<2><<<router_tasks < sm_count ? router_tasks : sm_count, kGemmThreads, Cfg<2>::kBytes, s>>>(
-      a, p, m.w_split, m.x_bf16);
+  prefill_router_kernel<<<router_tasks < sm_count ? router_tasks : sm_count, kGemmThreads, kRtSmem, s>>>(
+      a, m.w_split, m.x_bf16);
   prefill_topk_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a, p);
   prefill_prefix_kernel<<<(a.E + 7) / 8, 256, 0, s>>>(a, p);
   prefill_scan_kernel<<<1, 1024, 0, s>>>(a, p);
   prefill_pairs_kernel<<<(a.T * (a.k + 1) + 255) / 256, 256, 0, s>>>(a, p);
-  prefill_gemm_kernel<0><<<sm_count, kGemmThreads, Cfg<0>::kBytes, s>>>(a, p, m.x16, m.x16);
-  prefill_gemm_kernel<1><<<sm_count, kGemmThreads, Cfg<1>::kBytes, s>>>(a, p, m.h16, m.h16);
+  prefill_expert_kernel<0><<<sm_count, kExpThreads, kGemmSmem, s>>>(a, p);
+  prefill_expert_kernel<1><<<sm_count, kExpThreads, kGemmSmem, s>>>(a, p);
   const long long n = (long long)a.T * (a.H / 8);
   prefill_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, p);
   return cudaGetLastError();

@@ -17,6 +17,7 @@ struct PrefillArgs {
   int32_t* offsets;     // [E + 2] first pair of each expert list entry; [NE] = total
   int32_t* chunk_off;   // [E + 2] first 128-token chunk of each entry; [NE] = total
   int32_t* n_chunks;    // [1]
+  int4* chunk_rec;      // [max chunks] per 128-token chunk: {expert list entry, first pair, tokens, 0}
   int32_t* pair_token;  // [T*k + T] token of each pair, grouped by expert, ascending token
   int32_t* pair_z;      // [T*k + T] z row of each pair: t*(k+1) + rank (rank k = shared)
   uint32_t* bitmap;     // [E][ceil(T/32)] bit t of row e: token t selected e (zeroed each call)
@@ -28,12 +29,10 @@ struct PrefillArgs {
   int words;            // ceil(max_tokens / 32): row stride of bitmap and prefix
 };
 
-// TMA descriptors (128-byte swizzle, fp16/bf16, 64-element boxes along K).
+// TMA descriptors of the router GEMM (128-byte swizzle, bf16, 64-element boxes along K).
 struct PrefillMaps {
-  CUtensorMap w_split;  // [3][E][H] bf16, box 64 x 128 x 1
-  CUtensorMap x16;      // [Tmax][H] fp16, box 64 x 1 (row gathers)
-  CUtensorMap h16;      // [pairs max][I] fp16, box 64 x 16
-  CUtensorMap x_bf16;   // the call's x [T][H] bf16, box 64 x 128 (encoded per call)
+  CUtensorMap w_split;  // [3][E][H], box 64 x 128 x 1
+  CUtensorMap x_bf16;   // the call's x [T][H], box 64 x 128 (encoded per call)
 };
 
 typedef CUresult (*TensorMapEncodeFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
