@@ -59,12 +59,15 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+// Potentially blocking test: the thread sleeps (up to the hint, 20 us)
+// until the phase completes instead of spinning on issue slots that the
+// MMA thread and the epilogue need.
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(20000u)
       : "memory");
   return ok != 0;
 }
@@ -158,7 +161,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const La
   if (!ok) return false;
   int spins = 0;
   while (!mbar_try_wait(bar, parity)) {
-    if (((++spins) & 255) == 0 && global_ns() > deadline) {
+    if (((++spins) & 15) == 0 && global_ns() > deadline) {
       set_error(a, MOE_ERR_TIMEOUT);
       ok = false;
       return false;
