@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -327,8 +328,7 @@ def run_prefill(args):
         for _ in range(args.warmup):
             layer.forward(xd, yd, stream=stream)
     torch.cuda.synchronize()
-    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", "bench_prefill_clocks.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else "/tmp/bench_prefill_clocks.csv")
+    clocks = ClockSampler(os.path.join(tempfile.gettempdir(), "bench_prefill_clocks.csv"))
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
     with clocks:
         with torch.cuda.stream(stream):
@@ -459,8 +459,7 @@ def main():
         for _ in range(args.warmup):
             graph.replay()
     barrier()
-    clocks = ClockSampler(os.path.join(ROOT, "gpurun_out", f"bench_clocks_{rank}.csv")
-                          if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/bench_clocks_{rank}.csv")
+    clocks = ClockSampler(os.path.join(tempfile.gettempdir(), f"bench_clocks_{rank}.csv"))
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with clocks:
         with torch.cuda.stream(stream):
