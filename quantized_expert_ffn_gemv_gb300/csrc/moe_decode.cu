@@ -10,8 +10,8 @@
 //   router     fp32 dot products -> logits, each stored with the step number
 //              in one 64-bit word; readers poll for the tag (no grid barrier).
 //   routing    every CTA redundantly: top-k per token as a warp tournament
-//              (redux max over order-preserving keys) and a merge of the
-//              warps' lists, ascending expert order, softmax
+//              (redux max over order-preserving keys) over each warp's range,
+//              a k-way merge of the warps' lists, ascending expert order, softmax
 //              weights renormalised over the k, the union of selected experts
 //              and the (expert, token) pair lists, the slot hit check and LRU
 //              victims (double-buffered pool state; CTA 0 writes the next
@@ -80,11 +80,6 @@ __device__ __forceinline__ uint64_t global_ns() {
 __device__ __forceinline__ int ld_cg_i32(const int* p) {
   int r;
   asm volatile("ld.global.cg.s32 %0, [%1];" : "=r"(r) : "l"(p));
-  return r;
-}
-__device__ __forceinline__ uint4 ld_cg4(const void* p) {
-  uint4 r;
-  asm volatile("ld.global.cg.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
   return r;
 }
 __device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t* p) {
@@ -450,100 +445,58 @@ __device__ void warp_topk(const unsigned long long* logits, int E, int k, int ba
   }
 }
 
-// Merge one token's nl rank-ordered lists (nl <= 16, k entries each): the
-// k-th largest list head is a lower bound of the token's k-th largest key, so
-// only entries at or above it can be selected; those are ranked exactly.
-// Writes the selection in ascending expert order with renormalised softmax
-// weights, and marks the token in tokmask.
-__device__ void merge_topk(const uint2* lists, int nl, int k, const Lists& L, unsigned long long* tokmask, int t,
-                           bool write_out, const LayerArgs& a) {
+// One warp per token: a k-way merge of the token's nl rank-ordered lists
+// (lane l < nl owns list l; key 0 = none).  Each round takes the best head
+// (larger key, then lower expert) and advances that list.  sel gets the
+// token's k largest logits in rank order.
+__device__ void merge_lists(const uint2* lists, int nl, int k, uint2* sel) {
   const int lane = threadIdx.x & 31;
-  // threshold: k-th largest of the list heads (k <= nl); else take everything
-  uint2 hd = (lane < nl) ? lists[lane * kMaxTopK] : make_uint2(0u, 0u);
-  uint32_t thr = 0u;
-  if (k <= nl) {
-    int r = 0;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const uint32_t ki = __shfl_sync(0xffffffffu, hd.x, i);
-      const int ei = (int)__shfl_sync(0xffffffffu, hd.y, i);
-      r += (i < nl) && (ki != 0u) && before(ki, ei, hd.x, (int)hd.y);
-    }
-    const unsigned b = __ballot_sync(0xffffffffu, lane < nl && hd.x != 0u && r == k - 1);
-    thr = b ? __shfl_sync(0xffffffffu, hd.x, __ffs(b) - 1) : 0u;
-  }
-  // gather the entries >= thr (each list is sorted: a prefix of it)
-  int cnt = 0;
-  if (lane < nl) {
-    uint32_t kk[kMaxTopK];
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) kk[j] = (j < k) ? lists[lane * kMaxTopK + j].x : 0u;
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) cnt += (kk[j] != 0u && kk[j] >= thr);
-  }
-  int inc = cnt;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int v = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += v;
-  }
-  const int total = __shfl_sync(0xffffffffu, inc, 31);
-  uint2* cand = const_cast<uint2*>(lists) + 16 * kMaxTopK;  // scratch after the lists
-  for (int j = 0; j < cnt; ++j) cand[inc - cnt + j] = lists[lane * kMaxTopK + j];
-  __syncwarp();
-  // exact ranks of the candidates, scattered by rank into cand_sel
-  uint2* cand_sel = cand + 16 * kMaxTopK;
-  if (total <= 32) {
-    const uint2 me = (lane < total) ? cand[lane] : make_uint2(0u, 0xFFFFFFFFu);
-    int r = 0;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const uint32_t xj = __shfl_sync(0xffffffffu, me.x, j), yj = __shfl_sync(0xffffffffu, me.y, j);
-      r += (j < total) && before(xj, (int)yj, me.x, (int)me.y);
-    }
-    if (lane < total && r < k) cand_sel[r] = me;
-  } else {
-    for (int i = lane; i < total; i += 32) {
-      const uint2 me = cand[i];
-      int r = 0;
-      for (int j = 0; j < total; ++j) r += before(cand[j].x, (int)cand[j].y, me.x, (int)me.y);
-      if (r < k) cand_sel[r] = me;
+  int ptr = 0;
+  uint2 head = (lane < nl) ? lists[lane * kMaxTopK] : make_uint2(0u, 0xFFFFFFFFu);
+  if (head.x == 0u) head.y = 0xFFFFFFFFu;
+  for (int r = 0; r < k; ++r) {
+    const uint32_t mx = __reduce_max_sync(0xffffffffu, head.x);
+    const uint32_t emin = __reduce_min_sync(0xffffffffu, head.x == mx ? head.y : 0xFFFFFFFFu);
+    if (lane == 0) sel[r] = make_uint2(mx, emin);
+    if (mx != 0u && head.x == mx && head.y == emin) {
+      ++ptr;
+      head = (ptr < k) ? lists[lane * kMaxTopK + ptr] : make_uint2(0u, 0xFFFFFFFFu);
+      if (head.x == 0u) head.y = 0xFFFFFFFFu;
     }
   }
   __syncwarp();
-  const uint2 sel = (lane < k) ? cand_sel[lane] : make_uint2(0u, 0u);
-  // ascending expert order; softmax over the k renormalised (max = rank 0)
-  const int my_e = (lane < k) ? (int)sel.y : INT_MAX;
-  const float v = (lane < k) ? fkey_value(sel.x) : 0.f;
+}
+
+// One warp per token: the k selected (in rank order in sel) reported in
+// ascending expert order with softmax weights renormalised over the k (the
+// sum taken in ascending expert order, as on the batched path); marks the
+// token in tokmask.  sel is reused as scratch.
+__device__ void finish_topk(uint2* sel, int k, const Lists& L, unsigned long long* tokmask, int t, bool write_out,
+                            const LayerArgs& a) {
+  const int lane = threadIdx.x & 31;
+  const uint2 me = (lane < k) ? sel[lane] : make_uint2(0u, 0u);
+  const int my_e = (lane < k) ? (int)me.y : INT_MAX;
+  const float v = (lane < k) ? fkey_value(me.x) : 0.f;
+  const float m = __shfl_sync(0xffffffffu, v, 0);  // rank 0 holds the largest logit
   int pos = 0;
 #pragma unroll
   for (int j = 0; j < kMaxTopK; ++j) pos += (j < k) && (__shfl_sync(0xffffffffu, my_e, j) < my_e);
-  const float m = __shfl_sync(0xffffffffu, v, 0);
-  float vs = 0.f;
-  int es = 0;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) {
-    const int pj = __shfl_sync(0xffffffffu, pos, j);
-    const float vj = __shfl_sync(0xffffffffu, v, j);
-    const int ej = __shfl_sync(0xffffffffu, my_e, j);
-    if (j < k && lane == pj) { vs = vj; es = ej; }
-  }
-  float ex[kMaxTopK];
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) ex[j] = expf(__shfl_sync(0xffffffffu, vs, j) - m);
+  const float ex = (lane < k) ? expf(v - m) : 0.f;
+  float* ex_sorted = reinterpret_cast<float*>(sel);
+  __syncwarp();
+  if (lane < k) ex_sorted[pos] = ex;
+  __syncwarp();
   float z = 0.f;
-#pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j)
-    if (j < k) z += ex[j];
+  for (int j = 0; j < k; ++j) z += ex_sorted[j];
   if (lane < k) {
-    const float wj = expf(vs - m) / z;
-    L.s_idx[t * k + lane] = es;
-    L.s_w[t * k + lane] = wj;
+    const float wj = ex / z;
+    L.s_idx[t * k + pos] = my_e;
+    L.s_w[t * k + pos] = wj;
     if (write_out) {
-      a.topk_idx[t * k + lane] = es;
-      a.topk_w[t * k + lane] = wj;
+      a.topk_idx[t * k + pos] = my_e;
+      a.topk_w[t * k + pos] = wj;
     }
-    atomicOr(&tokmask[es], 1ull << t);
+    atomicOr(&tokmask[my_e], 1ull << t);
   }
 }
 
@@ -595,17 +548,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   const bool has_dn = c < H / 16;
   const bool pre_gu = NSh && c < NS;  // task 0 of this CTA is a shared-expert strip, loaded early
 
+  // loads whose latency overlaps the prologue: the step counter and this
+  // thread's router bias (used only once the router rows have arrived)
+  const uint32_t step0 = (tid == 0) ? (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.st->step)) : 0u;
+  const float bias_v = (a.bias && tid < nrows * T) ? __ldg(a.bias + r0 + tid / T) : 0.f;
   if (tid == 0) {
     for (int s = 0; s < R.gs; ++s) { mbar_init(&R.full_gu[s], 1); mbar_init(&R.empty_gu[s], kGroupWarps); }
     for (int s = 0; s < R.ds; ++s) { mbar_init(&R.full_dn[s], 1); mbar_init(&R.empty_dn[s], 1); }
     mbar_init(full_rt, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    s_seq = (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.st->step)) + 1u;
   }
   __syncthreads();
-  const uint32_t seq = s_seq;
-  uint32_t* cnt_cur = a.counters + (size_t)(seq & 1u) * a.cnt_stride;
-  uint32_t* cnt_next = a.counters + (size_t)((seq + 1u) & 1u) * a.cnt_stride;
 
   // ---- prologue: weights that do not depend on this call's input
   if (is_prod) {
@@ -641,7 +594,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     }
     if (bad) set_error(a, MOE_ERR_DEVICE);
   }
+  if (tid == 0) s_seq = step0 + 1u;
   __syncthreads();
+  const uint32_t seq = s_seq;
+  uint32_t* cnt_cur = a.counters + (size_t)(seq & 1u) * a.cnt_stride;
+  uint32_t* cnt_next = a.counters + (size_t)((seq + 1u) & 1u) * a.cnt_stride;
 
   // ---- router: two warps per row (one per half), the same summation order
   // as the batched path's router; bf16 x read exactly (shared-memory copy)
@@ -685,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     if (tid < nrows * T) {
       const int rr = tid / T, t = tid % T, e = r0 + rr;
       const float l = part[(2 * rr) * kMaxT + t] + part[(2 * rr + 1) * kMaxT + t];
-      const float v = l + (a.bias ? __ldg(a.bias + e) : 0.f);
+      const float v = l + bias_v;
       // value and step number in one 64-bit word: a reader that sees this
       // step's tag sees this step's value (no fence, no grid barrier)
       st_relaxed_u64(&tagged_logits[(size_t)t * E + e], ((unsigned long long)seq << 32) | __float_as_uint(v));
@@ -775,7 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         warp_topk<16>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
     }
     __syncthreads();
-    if (warp < T) merge_topk(wlist + warp * wpt * kMaxTopK, wpt, k, L, tokmask, warp, c == 0, a);
+    uint2* sel = wlist + kWarps * kMaxTopK;  // [T][kMaxTopK]
+    if (warp < T) {
+      merge_lists(wlist + warp * wpt * kMaxTopK, wpt, k, sel + warp * kMaxTopK);
+      finish_topk(sel + warp * kMaxTopK, k, L, tokmask, warp, c == 0, a);
+    }
   }
   __syncthreads();
   // union of the selected experts (ascending) and pair offsets, from the
@@ -844,32 +805,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   if (!a.pool) {
     if (tid == 0) s_nmiss = 0;
   } else {
-    // pool scratch in region A after tokmask: per slot owner, stamp and
-    // candidate key; per union entry its miss number; the ranked victims
+    // pool scratch in region A after the routing lists: per slot owner, stamp
+    // and candidate key; per union entry its miss number; the ranked victims
     int* own_s = reinterpret_cast<int*>(sm + PL.regA + al128((size_t)E * 8) + (size_t)4 * kWarps * kMaxTopK * 8);
     uint32_t* stp_s = reinterpret_cast<uint32_t*>(own_s + S);
     unsigned long long* key_s = reinterpret_cast<unsigned long long*>(stp_s + S);  // 8-byte aligned: 8S bytes precede it
     int* miss_no = reinterpret_cast<int*>(key_s + S);
     int* victim = miss_no + PL.umax + 2;
     __shared__ int s_ncand;
-    if (tid == 0) s_ncand = 0;
-    __syncthreads();
-    // candidates: empty slots first (ascending), then slots whose expert this
-    // call does not use, least recently used first, ties to the lower slot
-    for (int q = tid; q < S; q += kThreads) {
-      const int ow = ld_cg_i32(&pre_owner[q]);
-      const uint32_t stp = (uint32_t)ld_cg_i32((const int*)&pre_stamp[q]);
-      own_s[q] = ow;
-      stp_s[q] = stp;
-      const bool elig = ow < 0 || tokmask[ow] == 0ull;
-      key_s[q] = elig ? (((unsigned long long)(ow >= 0) << 44) | ((unsigned long long)stp << 12) | (unsigned long long)q)
-                      : ~0ull;
-      if (elig) atomicAdd(&s_ncand, 1);
-    }
+    // this CTA's slice of the next state starts as a copy of the current one
+    // (loads issued now, stored after the decision)
+    const int e0 = (int)((long long)c * E / G), e1 = (int)((long long)(c + 1) * E / G);
+    const int q0 = (int)((long long)c * S / G), q1 = (int)((long long)(c + 1) * S / G);
+    const int ce = e0 + tid, cq = q0 + tid;
+    const int cp_slot = ce < e1 ? ld_cg_i32(&pre_slot[ce]) : 0;
+    const int cp_owner = cq < q1 ? ld_cg_i32(&pre_owner[cq]) : 0;
+    const int cp_stamp = cq < q1 ? ld_cg_i32((const int*)&pre_stamp[cq]) : 0;
     for (int u = tid; u < n_union; u += kThreads) {
       L.u_slot[u] = ld_cg_i32(&pre_slot[L.u_expert[u]]);
       L.u_wait[u] = 0u;
     }
+    if (tid == 0) s_ncand = 0;
     __syncthreads();
     // misses in ascending expert order (the union order) get numbers 0, 1, ...
     if (warp == 0) {
@@ -883,43 +839,41 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       }
       if (lane == 0) s_nmiss = base;
     }
-    // the i-th best candidate slot is the i-th miss's victim
-    for (int q = tid; q < S; q += kThreads) {
-      const unsigned long long kq = key_s[q];
-      if (kq == ~0ull) continue;
-      int r = 0;
-      for (int j = 0; j < S; ++j) r += key_s[j] < kq;
-      if (r < PL.umax) victim[r] = q;
-    }
     __syncthreads();
     const int nm = s_nmiss;
-    if (nm > s_ncand && tid == 0) set_error(a, MOE_ERR_STATE);  // configure forbids this
-    for (int u = tid; u < n_union; u += kThreads)
-      if (L.u_slot[u] < 0) {
-        const int i = miss_no[u];
-        L.u_slot[u] = (i < s_ncand) ? victim[i] : 0;  // 0 keeps addresses in bounds on error
-        L.u_wait[u] = seq;
-      }
-    __syncthreads();
-    // CTA 0 writes the next state and rings the host doorbell
-    if (c == 0) {
-      for (int e = tid; e < E; e += kThreads) nxt_slot[e] = ld_cg_i32(&pre_slot[e]);
+    if (nm > 0) {
+      // candidates: empty slots first (ascending), then slots whose expert this
+      // call does not use, least recently used first, ties to the lower slot
       for (int q = tid; q < S; q += kThreads) {
-        nxt_owner[q] = own_s[q];
-        nxt_stamp[q] = stp_s[q];
+        const int ow = ld_cg_i32(&pre_owner[q]);
+        const uint32_t stp = (uint32_t)ld_cg_i32((const int*)&pre_stamp[q]);
+        own_s[q] = ow;
+        stp_s[q] = stp;
+        const bool elig = ow < 0 || tokmask[ow] == 0ull;
+        key_s[q] = elig ? (((unsigned long long)(ow >= 0) << 44) | ((unsigned long long)stp << 12) | (unsigned long long)q)
+                        : ~0ull;
+        if (elig) atomicAdd(&s_ncand, 1);
       }
       __syncthreads();
-      for (int u = tid; u < n_union; u += kThreads) {
-        const int e = L.u_expert[u], q = L.u_slot[u];
-        if (L.u_wait[u] != 0u) {
-          const int old = own_s[q];
-          if (old >= 0) nxt_slot[old] = -1;  // an evicted expert is never selected now
-          nxt_owner[q] = e;
-          nxt_slot[e] = q;
-        }
-        nxt_stamp[q] = seq;
+      // the i-th best candidate slot is the i-th miss's victim
+      for (int q = tid; q < S; q += kThreads) {
+        const unsigned long long kq = key_s[q];
+        if (kq == ~0ull) continue;
+        int r = 0;
+        for (int j = 0; j < S; ++j) r += key_s[j] < kq;
+        if (r < PL.umax) victim[r] = q;
       }
-      if (tid == 0 && nm > 0) {
+      __syncthreads();
+      if (nm > s_ncand && tid == 0) set_error(a, MOE_ERR_STATE);  // configure forbids this
+      for (int u = tid; u < n_union; u += kThreads)
+        if (L.u_slot[u] < 0) {
+          const int i = miss_no[u];
+          L.u_slot[u] = (i < s_ncand) ? victim[i] : 0;  // 0 keeps addresses in bounds on error
+          L.u_wait[u] = seq;
+        }
+      __syncthreads();
+      // CTA 0 rings the host doorbell as soon as the misses are placed
+      if (c == 0 && tid == 0) {
         int i = 0;
         const uint32_t head0 = a.st->ring_head;
         for (int u = 0; u < n_union; ++u)
@@ -936,14 +890,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         __threadfence_system();
       }
     }
+    // next state: every CTA writes its slice (copy, then this step's changes)
+    if (ce < e1) nxt_slot[ce] = cp_slot;
+    if (cq < q1) {
+      nxt_owner[cq] = cp_owner;
+      nxt_stamp[cq] = (uint32_t)cp_stamp;
+    }
+    __syncthreads();
+    for (int u = tid; u < n_union; u += kThreads) {
+      const int e = L.u_expert[u], q = L.u_slot[u];
+      if (q >= q0 && q < q1) nxt_stamp[q] = seq;
+      if (L.u_wait[u] != 0u) {
+        const int old = own_s[q];  // an evicted expert is never selected now
+        if (old >= e0 && old < e1) nxt_slot[old] = -1;
+        if (q >= q0 && q < q1) nxt_owner[q] = e;
+        if (e >= e0 && e < e1) nxt_slot[e] = q;
+      }
+    }
   }
   if (c == 0 && tid == 0) {
+    // stores and reductions only: nothing here waits for the (possibly cold) counters
     a.st->step = seq;
     a.st->n_union = n_union;
     a.st->n_miss = s_nmiss;
-    a.st->forwards += 1ull;
-    a.st->hits += (unsigned long long)(n_union - s_nmiss);
-    a.st->misses += (unsigned long long)s_nmiss;
+    atomicAdd(&a.st->forwards, 1ull);
+    atomicAdd(&a.st->hits, (unsigned long long)(n_union - s_nmiss));
+    atomicAdd(&a.st->misses, (unsigned long long)s_nmiss);
   }
   __syncthreads();
 
@@ -1000,9 +972,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       if (ok) {
         const unsigned char* sb = R.dn + s * R.dn_pitch;
         const int hrow = tk.poff + ((g < tk.cnt) ? g : 0);
+#pragma unroll 2
         for (int st = 0; st < nst; ++st) {
           const __half* hr = a.h16 + (size_t)hrow * I + st * 64 + t4 * 16;
-          const uint4 b01 = ld_cg4(hr), b23 = ld_cg4(hr + 8);
+          const uint4 b01 = __ldcg(reinterpret_cast<const uint4*>(hr)), b23 = __ldcg(reinterpret_cast<const uint4*>(hr + 8));
           const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
           const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
           supertile_mma(acc, nb, scv, b01, b23);
