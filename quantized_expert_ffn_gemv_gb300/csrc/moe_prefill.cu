@@ -156,11 +156,18 @@ __device__ void set_error(const LayerArgs& a, int code) {
   __threadfence_system();
 }
 
+// Bounded wait on an mbarrier phase.  backoff_ns > 0 puts the warp to sleep
+// between tests so that waiting warps leave the issue slots to the ones
+// doing work (the MMA thread waits without it).
+#ifndef PF_BACKOFF_NS
+#define PF_BACKOFF_NS 64
+#endif
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const LayerArgs& a, uint64_t deadline,
-                                         bool& ok) {
+                                         bool& ok, unsigned backoff_ns = PF_BACKOFF_NS) {
   if (!ok) return false;
   int spins = 0;
   while (!mbar_try_wait(bar, parity)) {
+    if (backoff_ns) __nanosleep(backoff_ns);
     if (((++spins) & 15) == 0 && global_ns() > deadline) {
       set_error(a, MOE_ERR_TIMEOUT);
       ok = false;
@@ -491,7 +498,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         const uint32_t dt = tmem + (uint32_t)(b * 128);
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int s = g % S, use = g / S;
-          if (!wait_bar(full(s), use & 1, a, deadline, ok)) break;
+          if (!wait_bar(full(s), use & 1, a, deadline, ok, 0)) break;
           tc_fence_after();
           const uint32_t sA = sbase + s * 3 * kTile, sB = sbase + kRtOffB + s * kTile;
 #pragma unroll
@@ -543,35 +550,42 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 // ---- grouped expert GEMMs.
+// A tcgen05.mma costs the issuing thread about as long as the tensor core
+// needs for 128 x 256 x 16, so chunks are up to 256 tokens (N = 256) and a
+// k-step issues its four MMAs and one commit.
 // Warp 0 (lanes 0-15): bulk copies of the packed 4-bit tiles, kRawR k-steps
 //   per copy and strip, into a ring of kRawStages raw stages.
-// Warps 1-16 (producers): warp pw dequantizes k-tiles 2 (pw / 8) and
-//   2 (pw / 8) + 1 of strip pw % 8 into the swizzled fp16 A tile (stmatrix)
-//   and signals a_full; all 512 threads gather the chunk's B rows with
-//   cp.async kLook k-steps ahead, each signalling b_full when its copies
-//   land.  A and B have rings of their own (kAStages, kBStages): the B ring
-//   is deep to cover the gather latency, the A ring only the MMA's lag.  The
-//   MMA thread orders both (generic-proxy writes) before its tensor-core
+// Warps 1-8 (dequant): warp w dequantizes strip w of each k-step's packed
+//   tile into the swizzled fp16 A tile (stmatrix) and signals a_full.
+// Warps 9-16 (gather): their 256 threads copy the chunk's B rows with
+//   cp.async as far ahead as the B ring allows, each signalling b_full when
+//   its copies land.  A k-step's commit arrives on its B stage's empty barrier; the A
+//   ring (kAStages < kBStages) is reused once the MMA of k-step g - kAStages
+//   has completed, i.e. when that k-step's B stage is released.  The MMA
+//   thread orders both halves (generic-proxy writes) before its tensor-core
 //   reads with one proxy fence after its waits.
-// Warp 17: TMEM allocation; lane 0 issues the MMAs (2 x 128 TMEM columns).
-// Warps 18-21: epilogue (TMEM lane quadrant warp % 4).
+// Warp 17: TMEM allocation (2 x 256 columns); lane 0 issues the MMAs.
+// Warps 18-25: epilogue, two per TMEM lane quadrant (warp % 4), each taking
+//   half of the chunk's columns.
 constexpr int kAStages = 3;
-constexpr int kBStages = 8;
-constexpr int kLook = 5;
-constexpr int kRawR = 4;
+constexpr int kBStages = 4;
+constexpr int kRawR = 2;
 constexpr int kRawStages = 2;
-constexpr int kProd = 16;
-constexpr int kXMmaWarp = 1 + kProd;
+constexpr int kProd = 8;    // dequant warps
+constexpr int kGather = 8;  // gather warps
+constexpr int kXMmaWarp = 1 + kProd + kGather;
 constexpr int kXEpi0 = kXMmaWarp + 1;
-constexpr int kExpThreads = (kXEpi0 + 4) * 32;
+constexpr int kXEpiWarps = 8;
+constexpr int kExpThreads = (kXEpi0 + kXEpiWarps) * 32;
+constexpr int kBTile = kPfN * 128;  // B tile: kPfN rows x 64 fp16
 constexpr int kRawBytes = 8 * kRawR * (512 + 64);
 constexpr int kOffB = kAStages * kTile;
-constexpr int kOffRaw = kOffB + kBStages * kTile;
-constexpr int kNumBars = 2 * kRawStages + 2 * kAStages + 2 * kBStages + 5;
+constexpr int kOffRaw = kOffB + kBStages * kBTile;
+constexpr int kNumBars = 2 * kRawStages + kAStages + 2 * kBStages + 5;
 constexpr int kOffBar = kOffRaw + kRawStages * kRawBytes;
 constexpr int kOffTmem = kOffBar + 8 * kNumBars;
 constexpr int kGemmSmem = kOffTmem + 16 + 1024;
-static_assert(kLook + kAStages <= kBStages, "a B stage is refilled only after the MMA released it");
+static_assert(kGemmSmem <= 232448, "shared memory");
 
 struct Task {
   int e, poff, nt, mb;
@@ -582,6 +596,22 @@ struct Task {
 __device__ __forceinline__ Task load_task(const PrefillArgs& p, int MB, int t) {
   const int4 r = ld_cg_int4(&p.chunk_rec[t / MB]);
   return Task{r.x, r.y, r.z, t % MB};
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 // MODE 0: gate/up; M-block mb = intermediate rows 64 mb .. 64 mb + 63 of gate
@@ -597,10 +627,9 @@ __global__ void __launch_bounds__(kExpThreads, 1) prefill_expert_kernel(LayerArg
   auto raw_full = [&](int r) { return bar0 + 8u * r; };
   auto raw_empty = [&](int r) { return bar0 + 8u * (kRawStages + r); };
   auto a_full = [&](int s) { return bar0 + 8u * (2 * kRawStages + s); };
-  auto a_empty = [&](int s) { return bar0 + 8u * (2 * kRawStages + kAStages + s); };
-  auto b_empty = [&](int s) { return bar0 + 8u * (2 * kRawStages + 2 * kAStages + s); };
-  auto b_full = [&](int s) { return bar0 + 8u * (2 * kRawStages + 2 * kAStages + kBStages + s); };
-  const int acc0 = 2 * kRawStages + 2 * kAStages + 2 * kBStages;
+  auto b_empty = [&](int s) { return bar0 + 8u * (2 * kRawStages + kAStages + s); };
+  auto b_full = [&](int s) { return bar0 + 8u * (2 * kRawStages + kAStages + kBStages + s); };
+  const int acc0 = 2 * kRawStages + kAStages + 2 * kBStages;
   auto acc_full = [&](int b) { return bar0 + 8u * (acc0 + b); };
   auto acc_empty = [&](int b) { return bar0 + 8u * (acc0 + 2 + b); };
   const uint32_t drain = bar0 + 8u * (acc0 + 4);
@@ -620,23 +649,20 @@ __global__ void __launch_bounds__(kExpThreads, 1) prefill_expert_kernel(LayerArg
       mbar_init(raw_full(r), 1);
       mbar_init(raw_empty(r), kProd);
     }
-    for (int s = 0; s < kAStages; ++s) {
-      mbar_init(a_full(s), kProd);
-      mbar_init(a_empty(s), 1);
-    }
+    for (int s = 0; s < kAStages; ++s) mbar_init(a_full(s), kProd);
     for (int s = 0; s < kBStages; ++s) {
       mbar_init(b_empty(s), 1);
-      mbar_init(b_full(s), kProd * 32);
+      mbar_init(b_full(s), kGather * 32);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(acc_full(b), 1);
-      mbar_init(acc_empty(b), 4);
+      mbar_init(acc_empty(b), kXEpiWarps);
     }
     mbar_init(drain, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == kXMmaWarp) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(tmem_slot)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(tmem_slot)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   tc_fence_before();
@@ -672,104 +698,80 @@ __global__ void __launch_bounds__(kExpThreads, 1) prefill_expert_kernel(LayerArg
       }
     }
   } else if (warp <= kProd) {
-    // ---- producers
-    const int pw = warp - 1, pt = tid - 32;
-    const int strip = pw & 7, half = pw >> 3;  // k-tiles 2 half, 2 half + 1 of the strip
+    // ---- dequant: warp w, strip w, all four k-tiles of each k-step
+    const int w = warp - 1;
     const int gg = lane >> 2;
-    const int R0 = (MODE == 0) ? 32 * (strip & 3) + 8 * (strip >> 2) : 16 * strip;  // tile row of strip row 0
-    const int rstep = (MODE == 0) ? 16 : 8;  // tile rows from g to g + 8
+    const int R0 = (MODE == 0) ? 32 * (w & 3) + 8 * (w >> 2) : 16 * w;  // tile row of strip row 0
+    const int rstep = (MODE == 0) ? 16 : 8;                              // tile rows from g to g + 8
     const int mi = lane >> 3;  // stmatrix matrix: (row g | g + 8) x (low | high 8 k of the k-tile)
     const int st_row = R0 + (lane & 7) + ((mi & 1) ? rstep : 0);
-    const uint32_t st_off0 = sw128_off(st_row, 4 * half + (mi >> 1)), st_off1 = sw128_off(st_row, 4 * half + 2 + (mi >> 1));
-    const int bc = pt & 7;  // B: 16-byte chunk of rows (pt >> 3) + 64 q
-    // B cursor, kLook k-steps ahead of the A cursor: task bt, k-step bks; the
-    // next task's record and token ids are fetched half a task early
-    int bt = blockIdx.x, bks = 0, gb = 0;
-    Task ntk{};
-    const __half* brow[2] = {nullptr, nullptr};
-    int ntok[2] = {0, 0};
-    auto fetch_tokens = [&](const Task& tk, int (&tok)[2]) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int n = (pt >> 3) + 64 * q;
-        tok[q] = (MODE == 0 && n < tk.nt) ? ld_cg_i32(&p.pair_token[tk.poff + n]) : 0;
-      }
-    };
-    auto set_rows = [&](const Task& tk, const int (&tok)[2]) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int n = (pt >> 3) + 64 * q;
-        brow[q] = n >= tk.nt ? nullptr
-                             : (MODE == 0 ? p.x16p + (size_t)tok[q] * H : p.h16p + (size_t)(tk.poff + n) * I);
-      }
-    };
-    if (bt < n_tasks) {
-      const Task btk = load_task(p, MB, bt);
-      int tok[2];
-      fetch_tokens(btk, tok);
-      set_rows(btk, tok);
-      if (bt + (int)gridDim.x < n_tasks) ntk = load_task(p, MB, bt + gridDim.x);
-    }
-    auto issue_b = [&]() {
-      if (bt < n_tasks && ok) {
-        const int s = gb % kBStages;
-        if (gb >= kBStages) wait_bar(b_empty(s), (gb / kBStages - 1) & 1, a, deadline, ok);
-        const uint32_t sB = sbase + kOffB + s * kTile;
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-          if (brow[q]) cp_async16(sB + sw128_off((pt >> 3) + 64 * q, bc), brow[q] + bks * 64 + bc * 8);
-        cp_async_arrive_noinc(b_full(s));
-        ++gb;
-        if (bks == KS / 2 && bt + (int)gridDim.x < n_tasks) fetch_tokens(ntk, ntok);
-        if (++bks == KS) {
-          bks = 0;
-          bt += gridDim.x;
-          if (bt < n_tasks) {
-            set_rows(ntk, ntok);  // token ids fetched at k-step KS / 2 of the task before
-            if (bt + (int)gridDim.x < n_tasks) ntk = load_task(p, MB, bt + gridDim.x);
-          }
-        }
-      }
-    };
-#pragma unroll
-    for (int i = 0; i < kLook; ++i) issue_b();
     int rb = 0, g = 0;
     for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x) {
       for (int ks = 0; ks < KS && ok; ++ks, ++g) {
-        issue_b();  // k-step g + kLook
         const int j = ks % kRawR;
         const int r = rb % kRawStages;
         if (j == 0 && !wait_bar(raw_full(r), (rb / kRawStages) & 1, a, deadline, ok)) break;
         const unsigned char* raw = sm + kOffRaw + r * kRawBytes;
-        const uint2 nib = *reinterpret_cast<const uint2*>(raw + (strip * kRawR + j) * 512 + lane * 16 + half * 8);
-        const uint32_t scw =
-            *reinterpret_cast<const uint32_t*>(raw + 8 * kRawR * 512 + (strip * kRawR + j) * 64 + gg * 8 + half * 4);
+        const uint4 nib = *reinterpret_cast<const uint4*>(raw + (w * kRawR + j) * 512 + lane * 16);
+        const uint2 sc = *reinterpret_cast<const uint2*>(raw + 8 * kRawR * 512 + (w * kRawR + j) * 64 + gg * 8);
         const int len = min(kRawR, KS - (ks - j));
         if (j == len - 1) {  // the raw stage is consumed (this warp's part is in registers)
           __syncwarp();
           if (lane == 0) mbar_arrive(raw_empty(r));
           ++rb;
         }
+        // A stage g % kAStages is free once the MMA of k-step g - kAStages completed
         const int s = g % kAStages;
-        if (g >= kAStages && !wait_bar(a_empty(s), (g / kAStages - 1) & 1, a, deadline, ok)) break;
+        if (g >= kAStages) {
+          const int gp = g - kAStages;
+          if (!wait_bar(b_empty(gp % kBStages), (gp / kBStages) & 1, a, deadline, ok)) break;
+        }
         const uint32_t sA = sbase + s * kTile;
-        // both k-tiles share this lane's block scales (k-tiles 0, 1: block 2 ks; 2, 3: block 2 ks + 1)
-        const __half2 dg = __half2half2(__ushort_as_half((uint16_t)(scw & 0xFFFFu)));
-        const __half2 dg8 = __half2half2(__ushort_as_half((uint16_t)(scw >> 16)));
-        __half2 q0[4], q1[4];
-        dequant_word(nib.x, q0);
-        dequant_word(nib.y, q1);
-        stmatrix_x4(sA + st_off0, h2u(__hmul2(q0[0], dg)), h2u(__hmul2(q0[1], dg8)), h2u(__hmul2(q0[2], dg)),
-                    h2u(__hmul2(q0[3], dg8)));
-        stmatrix_x4(sA + st_off1, h2u(__hmul2(q1[0], dg)), h2u(__hmul2(q1[1], dg8)), h2u(__hmul2(q1[2], dg)),
-                    h2u(__hmul2(q1[3], dg8)));
+        const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
+#pragma unroll
+        for (int kt = 0; kt < 4; ++kt) {
+          const uint32_t scw = (kt < 2) ? sc.x : sc.y;  // k-tiles 0, 1: first block of 32; 2, 3: second
+          const __half2 dg = __half2half2(__ushort_as_half((uint16_t)(scw & 0xFFFFu)));
+          const __half2 dg8 = __half2half2(__ushort_as_half((uint16_t)(scw >> 16)));
+          __half2 q[4];
+          dequant_word(words[kt], q);
+          stmatrix_x4(sA + sw128_off(st_row, 2 * kt + (mi >> 1)), h2u(__hmul2(q[0], dg)), h2u(__hmul2(q[1], dg8)),
+                      h2u(__hmul2(q[2], dg)), h2u(__hmul2(q[3], dg8)));
+        }
         __syncwarp();
         if (lane == 0) mbar_arrive(a_full(s));
       }
     }
+  } else if (warp <= kProd + kGather) {
+    // ---- gather: B rows of k-step gb into B stage gb % kBStages, running up
+    //      to kBStages - kAStages k-steps ahead of the MMA
+    const int gt = tid - 32 * (1 + kProd);  // 0 .. 255
+    const int bc = gt & 7;                  // 16-byte chunk of rows (gt >> 3) + 32 q
+    constexpr int kRows = kPfN / 32;
+    int gb = 0;
+    for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x) {
+      const Task tk = load_task(p, MB, t);
+      const __half* brow[kRows];
+#pragma unroll
+      for (int q = 0; q < kRows; ++q) {
+        const int n = (gt >> 3) + 32 * q;
+        brow[q] = (n >= tk.nt) ? nullptr
+                               : (MODE == 0 ? p.x16p + (size_t)ld_cg_i32(&p.pair_token[tk.poff + n]) * H
+                                            : p.h16p + (size_t)(tk.poff + n) * I);
+      }
+      for (int ks = 0; ks < KS && ok; ++ks, ++gb) {
+        const int s = gb % kBStages;
+        if (gb >= kBStages && !wait_bar(b_empty(s), (gb / kBStages - 1) & 1, a, deadline, ok)) break;
+        const uint32_t sB = sbase + kOffB + s * kBTile;
+#pragma unroll
+        for (int q = 0; q < kRows; ++q)
+          if (brow[q]) cp_async16(sB + sw128_off((gt >> 3) + 32 * q, bc), brow[q] + ks * 64 + bc * 8);
+        cp_async_arrive_noinc(b_full(s));
+      }
+    }
     asm volatile("cp.async.wait_all;" ::: "memory");
   } else if (warp == kXMmaWarp) {
-    // ---- MMA issue: one thread, double-buffered accumulator (2 x 128 columns)
+    // ---- MMA issue: one thread, double-buffered accumulator (2 x 256 columns)
     if (lane == 0) {
       int g = 0, i = 0;
       Task nxt = blockIdx.x < n_tasks ? load_task(p, MB, blockIdx.x) : Task{};
@@ -778,21 +780,20 @@ __global__ void __launch_bounds__(kExpThreads, 1) prefill_expert_kernel(LayerArg
         if (t + (int)gridDim.x < n_tasks) nxt = load_task(p, MB, t + gridDim.x);
         const uint32_t idesc = instr_desc((tk.nt + 15) & ~15, false);
         const int b = i & 1, ub = i >> 1;
-        if (ub > 0 && !wait_bar(acc_empty(b), (ub - 1) & 1, a, deadline, ok)) break;
+        if (ub > 0 && !wait_bar(acc_empty(b), (ub - 1) & 1, a, deadline, ok, 0)) break;
         tc_fence_after();
-        const uint32_t dt = tmem + (uint32_t)(b * 128);
+        const uint32_t dt = tmem + (uint32_t)(b * kPfN);
         for (int ks = 0; ks < KS; ++ks, ++g) {
           const int sa = g % kAStages, sb = g % kBStages;
-          if (!wait_bar(a_full(sa), (g / kAStages) & 1, a, deadline, ok)) break;
-          if (!wait_bar(b_full(sb), (g / kBStages) & 1, a, deadline, ok)) break;
+          if (!wait_bar(a_full(sa), (g / kAStages) & 1, a, deadline, ok, 0)) break;
+          if (!wait_bar(b_full(sb), (g / kBStages) & 1, a, deadline, ok, 0)) break;
           // the stage was written through the generic proxy (stmatrix, cp.async)
           asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           tc_fence_after();
-          const uint32_t sA = sbase + sa * kTile, sB = sbase + kOffB + sb * kTile;
+          const uint32_t sA = sbase + sa * kTile, sB = sbase + kOffB + sb * kBTile;
 #pragma unroll
           for (int j = 0; j < 4; ++j)
             tc_mma(dt, desc_sw128(sA + j * 32), desc_sw128(sB + j * 32), idesc, (ks > 0 || j > 0) ? 1u : 0u);
-          tc_commit(a_empty(sa));
           tc_commit(b_empty(sb));
         }
         if (!ok) break;
@@ -805,48 +806,53 @@ __global__ void __launch_bounds__(kExpThreads, 1) prefill_expert_kernel(LayerArg
     }
     __syncwarp();
   } else {
-    // ---- epilogue: TMEM lanes 32 (warp % 4) .. + 31 are tile rows
-    const int quad = warp & 3;
+    // ---- epilogue: TMEM lanes 32 (warp % 4) .. + 31 are tile rows; two warps
+    //      per quadrant, each half of the columns
+    const int quad = warp & 3, ehalf = (warp - kXEpi0) >> 2;
     const int row = quad * 32 + lane;
     int i = 0;
     Task nxt = blockIdx.x < n_tasks ? load_task(p, MB, blockIdx.x) : Task{};
     for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x, ++i) {
       const Task tk = nxt;
       if (t + (int)gridDim.x < n_tasks) nxt = load_task(p, MB, t + gridDim.x);
-      int zq[4];  // MODE 1: z rows of the chunk's pairs lane + 32 q
+      const int cbeg = ehalf * (kPfN / 2), cend = min(tk.nt, cbeg + kPfN / 2);
+      int zq[kPfN / 64];  // MODE 1: z rows of the pairs cbeg + lane + 32 q
       if (MODE == 1) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) zq[q] = (lane + 32 * q < tk.nt) ? ld_cg_i32(&p.pair_z[tk.poff + lane + 32 * q]) : 0;
+        for (int q = 0; q < kPfN / 64; ++q) {
+          const int n = cbeg + lane + 32 * q;
+          zq[q] = n < cend ? ld_cg_i32(&p.pair_z[tk.poff + n]) : 0;
+        }
       }
       const int b = i & 1, ub = i >> 1;
       if (!wait_bar(acc_full(b), ub & 1, a, deadline, ok)) break;
       tc_fence_after();
-      const uint32_t taddr = tmem + (uint32_t)(b * 128) + ((uint32_t)(quad * 32) << 16);
-      for (int c0 = 0; c0 < tk.nt; c0 += 16) {
-        float v[16];
-        tc_ld16(taddr + (uint32_t)c0, v);
+      const uint32_t taddr = tmem + (uint32_t)(b * kPfN) + ((uint32_t)(quad * 32) << 16);
+      for (int c0 = cbeg; c0 < cend; c0 += 32) {
+        float v[32];
+        tc_ld32(taddr + (uint32_t)c0, v);
         if (MODE == 0) {
-          // lanes l (gate row) and l ^ 8 (its up row) swap values; the gate lane
-          // finishes the even columns, the up lane the odd ones
+          // lanes l (gate row) and l ^ 8 (its up row): the gate lane finishes the
+          // even columns, the up lane the odd ones, without divergence
           const bool up = (row & 8) != 0;
           const int fi = tk.mb * 64 + 8 * (row >> 4) + (row & 7);
-          __half* hrow = p.h16p + (size_t)(tk.poff + c0) * I + fi;
+          __half* hbase = p.h16p + (size_t)(tk.poff + c0 + (up ? 1 : 0)) * I + fi;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float o = __shfl_xor_sync(0xffffffffu, v[j], 8);
-            if ((j & 1) == (up ? 1 : 0) && c0 + j < tk.nt) {
-              const float gv = up ? o : v[j], uv = up ? v[j] : o;
-              hrow[(size_t)j * I] = __float2half_rn(__fdividef(gv, 1.0f + __expf(-gv)) * uv);
-            }
+          for (int q = 0; q < 16; ++q) {
+            const float send = up ? v[2 * q] : v[2 * q + 1];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 8);
+            const float gv = up ? recv : v[2 * q], uv = up ? v[2 * q + 1] : recv;
+            const float h = __fdividef(gv, 1.0f + __expf(-gv)) * uv;
+            if (c0 + 2 * q + (up ? 1 : 0) < cend) hbase[(size_t)(2 * q) * I] = __float2half_rn(h);
           }
         } else {
           const int orow = tk.mb * 128 + row;
-          const int zsrc = (c0 >> 5);
-          const int zsel = zsrc == 0 ? zq[0] : zsrc == 1 ? zq[1] : zsrc == 2 ? zq[2] : zq[3];
+          const int zb = (c0 - cbeg) >> 5;
+          const int zsel = zb == 0 ? zq[0] : zb == 1 ? zq[1] : zb == 2 ? zq[2] : zq[3];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const int zr = __shfl_sync(0xffffffffu, zsel, (c0 + j) & 31);
-            if (c0 + j < tk.nt) p.z16[(size_t)zr * H + orow] = __float2half_rn(v[j]);
+          for (int j = 0; j < 32; ++j) {
+            const int zr = __shfl_sync(0xffffffffu, zsel, j);
+            if (c0 + j < cend) p.z16[(size_t)zr * H + orow] = __float2half_rn(v[j]);
           }
         }
       }
@@ -858,7 +864,7 @@ __global__ void __launch_bounds__(kExpThreads, 1) prefill_expert_kernel(LayerArg
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kXMmaWarp) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+  if (warp == kXMmaWarp) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
 }
 
 // y[t][r] = sum_j w_tj z[t][j][r] in ascending expert order, + z[t][k][r]; 8 outputs per thread.
