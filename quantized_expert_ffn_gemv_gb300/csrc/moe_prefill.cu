@@ -229,25 +229,45 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(LayerArgs a, PrefillA
   if (bad) set_error(a, MOE_ERR_DEVICE);
 }
 
-// Warp per token: k rounds of a warp argmax (value desc, index asc).
+// Warp per token: k rounds of a warp argmax (value desc, index asc) over the
+// token's logits, held in registers (CPL per lane; CPL = 0: read from
+// memory each round, for very large E).  Sets bit t of each selected
+// expert's bitmap row; the per-expert counts come from the bitmap.
+template <int CPL>
 __global__ void __launch_bounds__(256) prefill_topk_kernel(LayerArgs a, PrefillArgs p) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int E = a.E, k = a.k;
   if (t >= a.T) return;
   const float* lt = a.logits + (size_t)t * E;
+  constexpr int kRegs = CPL > 0 ? CPL : 1;
+  float lv[kRegs];
+#pragma unroll
+  for (int i = 0; i < kRegs; ++i) lv[i] = (CPL > 0 && lane + 32 * i < E) ? lt[lane + 32 * i] : -FLT_MAX;
   int sel[kMaxTopK];
   float selv[kMaxTopK];
   uint32_t taken[kMaxExperts / 1024] = {};  // bit i: logit lane + 32 i already selected
   for (int r = 0; r < k; ++r) {
     float bv = -FLT_MAX;
     int bi = INT_MAX;
-    for (int e = lane, i = 0; e < E; e += 32, ++i) {
-      if ((taken[i >> 5] >> (i & 31)) & 1u) continue;
-      const float v = lt[e];
-      if (v > bv || (v == bv && e < bi)) {
-        bv = v;
-        bi = e;
+    if (CPL > 0) {
+#pragma unroll
+      for (int i = 0; i < kRegs; ++i) {
+        const int e = lane + 32 * i;
+        const bool free = e < E && !((taken[0] >> i) & 1u);
+        if (free && (lv[i] > bv || (lv[i] == bv && e < bi))) {
+          bv = lv[i];
+          bi = e;
+        }
+      }
+    } else {
+      for (int e = lane, i = 0; e < E; e += 32, ++i) {
+        if ((taken[i >> 5] >> (i & 31)) & 1u) continue;
+        const float v = lt[e];
+        if (v > bv || (v == bv && e < bi)) {
+          bv = v;
+          bi = e;
+        }
       }
     }
 #pragma unroll
@@ -286,13 +306,13 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(LayerArgs a, PrefillA
     for (int j = 0; j < k; ++j) {
       a.topk_idx[t * k + j] = sel[j];
       a.topk_w[t * k + j] = expf(selv[j] - m) / z;
-      atomicAdd(&p.counts[sel[j]], 1);
       atomicOr(&p.bitmap[(size_t)sel[j] * p.words + (t >> 5)], 1u << (t & 31));
     }
   }
 }
 
-// Warp per routed expert: prefix[e][w] = set bits of bitmap row e before word w.
+// Warp per routed expert: prefix[e][w] = set bits of bitmap row e before
+// word w; counts[e] = all of them.
 __global__ void __launch_bounds__(256) prefill_prefix_kernel(LayerArgs a, PrefillArgs p) {
   const int lane = threadIdx.x & 31;
   const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -313,6 +333,7 @@ __global__ void __launch_bounds__(256) prefill_prefix_kernel(LayerArgs a, Prefil
     if (w < words) pre[w] = run + incl - c;
     run += __shfl_sync(0xffffffffu, incl, 31);
   }
+  if (lane == 0) p.counts[e] = run;
 }
 
 // One CTA: offsets and chunk offsets of the E routed experts and the shared
@@ -988,7 +1009,21 @@ cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, const Prefi
   const int router_tasks = ((a.E + 127) / 128) * ((a.T + 127) / 128);
   prefill_router_kernel<<<router_tasks < sm_count ? router_tasks : sm_count, kGemmThreads, kRtSmem, s>>>(
       a, m.w_split, m.x_bf16);
-  prefill_topk_kernel<<<(a.T + 7) / 8, 256, 0, s>>>(a, p);
+  const int tk_grid = (a.T + 7) / 8;
+  if (a.E <= 32)
+    prefill_topk_kernel<1><<<tk_grid, 256, 0, s>>>(a, p);
+  else if (a.E <= 64)
+    prefill_topk_kernel<2><<<tk_grid, 256, 0, s>>>(a, p);
+  else if (a.E <= 128)
+    prefill_topk_kernel<4><<<tk_grid, 256, 0, s>>>(a, p);
+  else if (a.E <= 256)
+    prefill_topk_kernel<8><<<tk_grid, 256, 0, s>>>(a, p);
+  else if (a.E <= 512)
+    prefill_topk_kernel<16><<<tk_grid, 256, 0, s>>>(a, p);
+  else if (a.E <= 1024)
+    prefill_topk_kernel<32><<<tk_grid, 256, 0, s>>>(a, p);
+  else
+    prefill_topk_kernel<0><<<tk_grid, 256, 0, s>>>(a, p);
   prefill_prefix_kernel<<<(a.E + 7) / 8, 256, 0, s>>>(a, p);
   prefill_scan_kernel<<<1, 1024, 0, s>>>(a, p);
   prefill_pairs_kernel<<<(a.T * (a.k + 1) + 255) / 256, 256, 0, s>>>(a, p);
