@@ -236,11 +236,13 @@ def run_stack(args):
 
     def totals():
         ss = [l.stats() for l in st.layers]
-        return (sum(s["misses"] for s, _ in ss), sum(s["h2d_bytes"] for s, _ in ss), [c for _, c in ss])
+        return (sum(s["misses"] for s, _ in ss), sum(s["h2d_bytes"] for s, _ in ss), [c for _, c in ss],
+                sum(s["wait_ns"] for s, _ in ss))
 
-    def run(n_slots):
+    def run(n_slots, service=0):
         for l in st.layers:
             l.configure(n_slots)
+            l.set_miss_service(service)
         outs = torch.empty((ntok, synth.PAGE.H), dtype=torch.bfloat16, device="cuda")
         with torch.cuda.stream(stream):
             xin.copy_(x_pin[0:1], non_blocking=True)
@@ -257,7 +259,7 @@ def run_stack(args):
                 graph.replay()
                 outs[t:t + 1].copy_(o)
         torch.cuda.synchronize()
-        m0, b0, _ = totals()
+        m0, b0, _, w0 = totals()
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
         with torch.cuda.stream(stream):
             ev[0].record(stream)
@@ -267,12 +269,14 @@ def run_stack(args):
                 outs[t:t + 1].copy_(o)
             ev[1].record(stream)
         torch.cuda.synchronize()
-        m1, b1, codes = totals()
-        return ev[0].elapsed_time(ev[1]), outs, m1 - m0, b1 - b0, codes
+        m1, b1, codes, w1 = totals()
+        return ev[0].elapsed_time(ev[1]), outs, m1 - m0, b1 - b0, codes, w1 - w0
 
-    ms_pool, out_pool, misses, h2d_bytes, codes = run(slots)
-    ms_res, out_res, _, _, codes_res = run(synth.PAGE.E)
+    ms_pool, out_pool, misses, h2d_bytes, codes, wait_ns = run(slots)
+    ms_pull, out_pull, misses_pull, _, codes_pull, _ = run(slots, service=1)
+    ms_res, out_res, _, _, codes_res, _ = run(synth.PAGE.E)
     identical = bool(torch.equal(out_pool.view(torch.int16), out_res.view(torch.int16)))
+    identical_pull = bool(torch.equal(out_pull.view(torch.int16), out_res.view(torch.int16)))
     peak_small = h2d_peak_gbs(torch, synth.PAGE.expert_bytes, 256)
     peak_large = h2d_peak_gbs(torch, 64 << 20, 16)
     hbm_peak, peak_kind = measured_peak()
@@ -291,7 +295,10 @@ def run_stack(args):
         "pool": {"tokens_per_s": pool_tps, "misses": misses, "h2d_bytes": h2d_bytes,
                  "h2d_bytes_per_token": h2d_bytes / meas, "h2d_gbs": h2d_gbs,
                  "h2d_peak_gbs_expert_copies": peak_small, "h2d_peak_gbs_64MB_copies": peak_large,
-                 "h2d_frac_of_expert_copy_peak": h2d_gbs / peak_small, "status": codes},
+                 "h2d_frac_of_expert_copy_peak": h2d_gbs / peak_small,
+                 "kernel_wait_us_per_miss": wait_ns / 1e3 / max(1, misses), "status": codes},
+        "pool_sm_pull": {"tokens_per_s": meas / (ms_pull * 1e-3), "misses": misses_pull, "status": codes_pull,
+                         "bit_identical_vs_resident": identical_pull},
         "resident": {"tokens_per_s": res_tps, "status": codes_res, "roofline": {
             "bound": "hbm", "achieved": step_bytes * res_tps / 1e9, "peak": hbm_peak, "unit": "GB/s",
             "frac": step_bytes * res_tps / 1e9 / hbm_peak, "peak_kind": peak_kind, "bytes_per_token": step_bytes}},

@@ -188,14 +188,31 @@ typedef struct {
 MOE_API moe_status_t moe_get_stats(moe_layer_t* layer, moe_stats_t* out);
 
 /*
- * Copy the miss log (one (step, expert, slot) int32 triple per copy the
- * copy server issued, step counted from 1 per layer) into out[0 .. 3*max).
+ * Copy the miss log (one (step, expert, slot) int32 triple per miss, in the
+ * order served, step counted from 1 per layer) into out[0 .. 3*max).
  * *n receives the total number logged.  Synchronizes like moe_get_stats.
  */
 MOE_API moe_status_t moe_get_miss_log(moe_layer_t* layer, int32_t* out, int64_t max, int64_t* n);
 
 /* Device-side wait limit for a slot copy (default 2 s); 0 restores the default. */
 MOE_API moe_status_t moe_set_wait_timeout_ns(moe_layer_t* layer, uint64_t ns);
+
+/*
+ * How a pooled layer serves a miss (T <= 8 calls).
+ *  MOE_MISS_COPY_ENGINE (default): the kernel rings the host doorbell and
+ *    waits; the copy server copies the expert from the pinned master copy
+ *    into its slot (cudaMemcpyAsync) and publishes the slot's ready flag
+ *    (Betelgeuse news page, section 机制, rows 调度 and 内存/盘).
+ *  MOE_MISS_SM_PULL: the kernel's own threads read the missed expert from
+ *    the pinned master copy over the coherent host link, use it at once and
+ *    write it into its slot for later calls; the doorbell entry is only
+ *    logged.  Results are bit-identical to the default mode.
+ * Applies to calls launched afterwards; a CUDA graph captured earlier keeps
+ * the mode it was captured with.  Synchronizes the device.
+ * Errors: INVALID_ARG (null layer or unknown mode), CUDA.
+ */
+enum { MOE_MISS_COPY_ENGINE = 0, MOE_MISS_SM_PULL = 1 };
+MOE_API moe_status_t moe_set_miss_service(moe_layer_t* layer, int32_t mode);
 
 /*
  * Host-side fault injection for tests (no GPU fault is ever raised):

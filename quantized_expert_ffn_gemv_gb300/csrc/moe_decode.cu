@@ -266,13 +266,15 @@ __device__ inline Lists carve_lists(unsigned char* base, int T, int k, int umax)
 
 // Expert list index xi: 0 = shared expert (when present), then routed u.
 struct Task {
-  const uint8_t* base;
+  const uint8_t* base;  // the expert in its slot
+  const uint8_t* src;   // pulled misses: the expert in the host master copy, else null
   int cnt, poff, slot;
   uint32_t wait_seq;
 };
 
 __device__ __forceinline__ Task task_of(const LayerArgs& a, const Lists& L, int xi, int n_shared) {
   Task t;
+  t.src = nullptr;
   if (xi < n_shared) {
     t.base = a.shared;
     t.cnt = a.T;
@@ -286,6 +288,10 @@ __device__ __forceinline__ Task task_of(const LayerArgs& a, const Lists& L, int 
     t.poff = L.u_off[u];
     t.cnt = L.u_off[u + 1] - t.poff;
     t.wait_seq = L.u_wait[u];
+    if (t.wait_seq && a.pull) {  // a miss the kernel reads from host memory itself
+      t.src = a.master + (int64_t)L.u_expert[u] * a.blob;
+      t.wait_seq = 0u;
+    }
   }
   return t;
 }
@@ -329,9 +335,13 @@ __device__ void pump(Producer& P, const Ctx& x) {
   const Ring& R = *x.R;
   while (P.m < P.n_gu) {
     const int s = P.m % R.gs;
-    if (P.m >= R.gs && !mbar_try_wait(&R.empty_gu[s], ((P.m / R.gs) - 1) & 1)) break;
     const int t = x.c + x.G * P.m;
     const Task tk = task_of(a, *x.L, t / x.NS, x.NSh);
+    if (tk.src) {  // pulled by the consuming group itself
+      ++P.m;
+      continue;
+    }
+    if (P.m >= R.gs && !mbar_try_wait(&R.empty_gu[s], ((P.m / R.gs) - 1) & 1)) break;
     if (tk.wait_seq) {
       const uint32_t v = ld_acquire_sys(&a.ready[tk.slot]);
       if (v == (tk.wait_seq | kReadyError)) { set_error(a, MOE_ERR_COPY); P.m = P.n_gu; P.d = P.n_dn; return; }
@@ -347,8 +357,12 @@ __device__ void pump(Producer& P, const Ctx& x) {
   }
   while (P.d < P.n_dn) {
     const int s = P.d % R.ds;
-    if (P.d >= R.ds && !mbar_try_wait(&R.empty_dn[s], ((P.d / R.ds) - 1) & 1)) break;
     const Task tk = task_of(a, *x.L, P.d, x.NSh);
+    if (tk.src) {  // pulled by the consuming warp itself
+      ++P.d;
+      continue;
+    }
+    if (P.d >= R.ds && !mbar_try_wait(&R.empty_dn[s], ((P.d / R.ds) - 1) & 1)) break;
     if (tk.wait_seq) {
       const uint32_t v = ld_acquire_sys(&a.ready[tk.slot]);
       if (v == (tk.wait_seq | kReadyError)) { set_error(a, MOE_ERR_COPY); P.m = P.n_gu; P.d = P.n_dn; return; }
@@ -362,6 +376,19 @@ __device__ void pump(Producer& P, const Ctx& x) {
     bulk_g2s(R.dn + s * R.dn_pitch, tk.base + down_base(x.H, x.I) + (size_t)x.c * R.dn_bytes, (uint32_t)R.dn_bytes,
              &R.full_dn[s]);
     ++P.d;
+  }
+}
+
+// A missed expert's strip read by the threads that need it, straight from the
+// pinned host master copy (coherent over the host link), into the ring
+// stage, and written back to the expert's slot for later calls.  16 bytes
+// per thread and step; the caller then completes the stage's full phase.
+__device__ __forceinline__ void pull_strip(const uint8_t* src, uint8_t* slot_dst, unsigned char* stage, size_t bytes,
+                                           int tid, int nthreads) {
+  for (size_t o = (size_t)tid * 16; o < bytes; o += (size_t)nthreads * 16) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + o));
+    *reinterpret_cast<uint4*>(stage + o) = v;
+    *reinterpret_cast<uint4*>(slot_dst + o) = v;
   }
 }
 
@@ -666,6 +693,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     const int xi = t_gu / NS, strip = t_gu % NS;
     const Task tk = task_of(a, L, xi, NSh);
     const int col_tok = (g < tk.cnt) ? (xi < NSh ? g : L.pair_token[tk.poff + g]) : 0;
+    if (tk.src) {  // a missed expert read from host memory by this group
+      const size_t off = (size_t)strip * R.gu_bytes;
+      pull_strip(tk.src + off, const_cast<uint8_t*>(tk.base) + off, R.gu + s * R.gu_pitch, R.gu_bytes,
+                 wg * 32 + lane, kGroupWarps * 32);
+      named_sync(1 + grp, kGroupWarps * 32);
+      if (wg == 0 && lane == 0) mbar_arrive(&R.full_gu[s]);
+    }
     const bool ok = wait_full(&R.full_gu[s], (m / R.gs) & 1, deadline, is_prod, P, X);
     float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
     const int nst = H / 64;
@@ -891,6 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
             re->seq = seq;
             re->expert = L.u_expert[u];
             re->slot = L.u_slot[u];
+            re->served = a.pull ? 1u : 0u;
             ++i;
           }
         __threadfence_system();
@@ -976,6 +1011,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         }
       }
       __syncwarp();
+      if (tk.src) {  // a missed expert read from host memory by this warp
+        const size_t off = (size_t)down_base(H, I) + (size_t)c * R.dn_bytes;
+        pull_strip(tk.src + off, const_cast<uint8_t*>(tk.base) + off, R.dn + s * R.dn_pitch, R.dn_bytes, lane, 32);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&R.full_dn[s]);
+      }
       const bool ok = wait_full(&R.full_dn[s], (xi / R.ds) & 1, deadline, is_prod, P, X);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       if (ok) {

@@ -72,7 +72,7 @@ struct RingEntry {
   uint32_t seq;
   int32_t expert;
   int32_t slot;
-  uint32_t pad;
+  uint32_t served;  // 1: the kernel read the expert from host memory itself (log only, no copy)
 };
 
 // Pinned host memory mapped into the device address space.
@@ -88,6 +88,8 @@ struct HostMapped {
 struct LayerArgs {
   int H, E, k, I, n_shared, T;
   int n_slots, pool;  // pool = 0: every expert resident at slot == expert index
+  int pull;           // pooled misses: 0 = host copy server, 1 = read by the kernel from the mapped master copy
+  const uint8_t* master;  // device address of the pinned host master copy (GPU layout, expert e at e * blob)
   const float* W_r;
   const float* bias;
   const uint8_t* arena;   // slot s at arena + s * blob

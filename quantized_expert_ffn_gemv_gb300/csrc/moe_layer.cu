@@ -202,6 +202,14 @@ struct moe_layer {
 namespace {
 
 void serve_entry(moe_layer* L, const RingEntry& e) {
+  if (e.served) {  // the kernel read this expert from host memory itself
+    L->h2d_bytes += (uint64_t)L->blob;
+    std::lock_guard<std::mutex> g(L->log_mu);
+    L->miss_log.push_back((int32_t)e.seq);
+    L->miss_log.push_back(e.expert);
+    L->miss_log.push_back(e.slot);
+    return;
+  }
   bool fail = false;
   const int64_t n = L->fail_copy_n.load();
   if (n > 0 && ++L->copies_since_arm == n) fail = true;
@@ -256,7 +264,7 @@ bool poll_layer(moe_layer* L) {
     e.seq = src->seq;
     e.expert = src->expert;
     e.slot = src->slot;
-    e.pad = 0;
+    e.served = src->served;
     serve_entry(L, e);
     ++L->tail;
   }
@@ -425,11 +433,13 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   }
 
   // pinned master copy in GPU layout
-  if (cudaHostAlloc((void**)&L->master, (size_t)L->blob * E, cudaHostAllocDefault) != cudaSuccess) {
+  if (cudaHostAlloc((void**)&L->master, (size_t)L->blob * E, cudaHostAllocMapped) != cudaSuccess) {
     L->master = nullptr;
     return fail(MOE_ERR_OUT_OF_MEMORY);
   }
   repack_many(d.experts, E, H, I, L->master);
+  void* master_dev = nullptr;
+  if (cudaHostGetDevicePointer(&master_dev, L->master, 0) != cudaSuccess) return fail(MOE_ERR_CUDA);
 
   if (d.n_shared) {
     std::vector<uint8_t> tmp((size_t)L->blob);
@@ -504,6 +514,8 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.topk_idx = (int32_t*)(b + o_tki);
   a.topk_w = (float*)(b + o_tkw);
   a.wait_timeout_ns = L->wait_timeout_ns;
+  a.master = (const uint8_t*)master_dev;
+  a.pull = 0;
   L->tagged_logits = (unsigned long long*)(b + o_bar);
   a.counters = (uint32_t*)(b + o_cnt);
   a.cnt_stride = Um + 2;
@@ -680,6 +692,14 @@ moe_status_t moe_get_miss_log(moe_layer_t* L, int32_t* out, int64_t max, int64_t
 moe_status_t moe_set_wait_timeout_ns(moe_layer_t* L, uint64_t ns) {
   if (!L) return MOE_ERR_INVALID_ARG;
   L->wait_timeout_ns = ns ? ns : 2000000000ull;
+  return MOE_OK;
+}
+
+moe_status_t moe_set_miss_service(moe_layer_t* L, int32_t mode) {
+  if (!L || (mode != MOE_MISS_COPY_ENGINE && mode != MOE_MISS_SM_PULL)) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(L->d.device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;  // no call in flight sees a half-set mode
+  L->args.pull = mode == MOE_MISS_SM_PULL ? 1 : 0;
   return MOE_OK;
 }
 

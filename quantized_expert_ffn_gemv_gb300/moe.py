@@ -18,7 +18,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_expert_bytes", "moe_repack_expert", "moe_unpack_expert", "moe_layer_create",
            "moe_slot_pool_configure", "moe_forward", "moe_residual_rmsnorm", "moe_get_stats", "moe_get_miss_log",
            "moe_set_wait_timeout_ns", "moe_debug_copy_faults", "moe_destroy", "moe_status_string",
-           "moe_route_noalloc"]
+           "moe_route_noalloc", "moe_set_miss_service"]
 
 
 class MoeError(RuntimeError):
@@ -64,6 +64,7 @@ def lib(build_if_missing=False):
         L.moe_get_stats.argtypes = [p, C.POINTER(Stats)]
         L.moe_get_miss_log.argtypes = [p, p, i64, C.POINTER(i64)]
         L.moe_set_wait_timeout_ns.argtypes = [p, u64]
+        L.moe_set_miss_service.argtypes = [p, i32]
         L.moe_debug_copy_faults.argtypes = [p, i64, i32]
         L.moe_destroy.argtypes = [p]
         L.moe_destroy.restype = None
@@ -190,6 +191,10 @@ class MoeLayer:
 
     def set_wait_timeout_ns(self, ns):
         check(lib().moe_set_wait_timeout_ns(self.h, ns), "moe_set_wait_timeout_ns")
+
+    def set_miss_service(self, mode):
+        """0 = copy engine behind the host doorbell (default), 1 = the kernel reads misses from host memory."""
+        check(lib().moe_set_miss_service(self.h, int(mode)), "moe_set_miss_service")
 
     def debug_copy_faults(self, fail_copy_n=0, pause=False):
         check(lib().moe_debug_copy_faults(self.h, fail_copy_n, int(pause)), "moe_debug_copy_faults")

@@ -55,6 +55,11 @@ class MoeStack:
             cur = nxt
         return bufs["x"][cur]
 
+    def set_miss_service(self, mode):
+        """Miss service of every layer's pool (see MoeLayer.set_miss_service)."""
+        for l in self.layers:
+            l.set_miss_service(mode)
+
     def stats(self):
         return [l.stats()[0] for l in self.layers]
 

@@ -17,12 +17,14 @@ def small():
     return synth.make_layer(synth.SMALL, layer=0)
 
 
+@pytest.mark.parametrize("service", [0, 1], ids=["copy_engine", "sm_pull"])
 @pytest.mark.parametrize("T,S", [(1, 16), (4, 20)])
-def test_pool_is_residency_invariant_and_matches_lru(small, T, S):
+def test_pool_is_residency_invariant_and_matches_lru(small, T, S, service):
     x, _ = resampled_tokens(small, 500, 96)
     full = make_gpu_layer(small, max_tokens=T)
     y0, i0, w0 = run(full, x, T=T)
     pool = make_gpu_layer(small, max_tokens=T, n_slots=S)
+    pool.set_miss_service(service)
     y1, i1, w1 = run(pool, x, T=T)
     assert np.array_equal(y0, y1) and np.array_equal(i0, i1) and np.array_equal(w0, w1)
     steps = [sorted(set(i1[t0:t0 + T].ravel().tolist())) for t0 in range(0, 96, T)]
