@@ -198,15 +198,22 @@ MOE_API moe_status_t moe_get_miss_log(moe_layer_t* layer, int32_t* out, int64_t 
 MOE_API moe_status_t moe_set_wait_timeout_ns(moe_layer_t* layer, uint64_t ns);
 
 /*
- * How a pooled layer serves a miss (T <= 8 calls).
- *  MOE_MISS_COPY_ENGINE (default): the kernel rings the host doorbell and
- *    waits; the copy server copies the expert from the pinned master copy
- *    into its slot (cudaMemcpyAsync) and publishes the slot's ready flag
- *    (Betelgeuse news page, section 机制, rows 调度 and 内存/盘).
+ * How a pooled layer serves a miss (T <= 8 calls).  Both ring the host
+ * doorbell and log the miss (Betelgeuse news page, section 机制, rows 调度
+ * and 内存/盘); they differ in who moves the bytes.  Results are
+ * bit-identical in both modes.
+ *  MOE_MISS_COPY_ENGINE (default): the kernel waits; the copy server copies
+ *    the expert into its slot (cudaMemcpyAsync on its own streams) and
+ *    publishes the slot's ready flag.  The copy server needs the CUDA driver
+ *    while the kernel runs: when the submitting thread sits inside the
+ *    driver with a deep queue of launches ahead of the GPU, a copy can be
+ *    held back until the kernel's bounded wait ends the call with
+ *    MOE_ERR_TIMEOUT (no hang, no dropped miss).
  *  MOE_MISS_SM_PULL: the kernel's own threads read the missed expert from
  *    the pinned master copy over the coherent host link, use it at once and
- *    write it into its slot for later calls; the doorbell entry is only
- *    logged.  Results are bit-identical to the default mode.
+ *    write it into its slot for later calls; the copy server only logs the
+ *    doorbell entry, so nothing in the call waits on the host.  Reads issued
+ *    by the SMs reach a lower host-link bandwidth than the copy engine.
  * Applies to calls launched afterwards; a CUDA graph captured earlier keeps
  * the mode it was captured with.  Synchronizes the device.
  * Errors: INVALID_ARG (null layer or unknown mode), CUDA.

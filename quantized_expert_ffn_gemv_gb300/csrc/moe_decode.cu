@@ -81,6 +81,11 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(evict_first_policy())
       : "memory");
 }
+// 16-byte copy global -> shared through L2 only (data other CTAs wrote in this call)
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -381,15 +386,16 @@ __device__ void pump(Producer& P, const Ctx& x) {
 
 // A missed expert's strip read by the threads that need it, straight from the
 // pinned host master copy (coherent over the host link), into the ring
-// stage, and written back to the expert's slot for later calls.  16 bytes
-// per thread and step; the caller then completes the stage's full phase.
+// stage: every 16-byte copy of a thread is in flight at once (one round trip
+// over the link), then the thread writes the chunks it fetched back to the
+// expert's slot for later calls.  The caller then completes the stage's full
+// phase.
 __device__ __forceinline__ void pull_strip(const uint8_t* src, uint8_t* slot_dst, unsigned char* stage, size_t bytes,
                                            int tid, int nthreads) {
-  for (size_t o = (size_t)tid * 16; o < bytes; o += (size_t)nthreads * 16) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + o));
-    *reinterpret_cast<uint4*>(stage + o) = v;
-    *reinterpret_cast<uint4*>(slot_dst + o) = v;
-  }
+  for (size_t o = (size_t)tid * 16; o < bytes; o += (size_t)nthreads * 16) cp_async16(stage + o, src + o);
+  cp_async_wait_all();
+  for (size_t o = (size_t)tid * 16; o < bytes; o += (size_t)nthreads * 16)
+    *reinterpret_cast<uint4*>(slot_dst + o) = *reinterpret_cast<const uint4*>(stage + o);
 }
 
 // Bounded wait on an mbarrier phase; the producer lane keeps pumping while it
@@ -568,7 +574,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   const Lists L = carve_lists(sm + PL.lists, T, k, PL.umax);
   __shared__ uint32_t s_seq;
   __shared__ int s_nunion, s_nmiss;
-  const uint64_t deadline = global_ns() + a.wait_timeout_ns;
   const bool is_prod = (warp == kProdWarp && lane == 0);
   const Ctx X{&a, &R, &L, c, G, NS, NSh, H, I};
   Producer P;
@@ -584,9 +589,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   const bool has_dn = c < H / 16;
   const bool pre_gu = NSh && c < NS;  // task 0 of this CTA is a shared-expert strip, loaded early
 
-  // loads whose latency overlaps the prologue: the step counter and this
-  // thread's router bias (used only once the router rows have arrived)
-  const uint32_t step0 = (tid == 0) ? (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.st->step)) : 0u;
+  // Programmatic dependent launch: the next kernel in the stream may be
+  // scheduled now.  Its CTAs take an SM only when one of ours leaves it, run
+  // their prologue (read-only weights into shared memory) and then wait for
+  // this grid to complete before touching anything it writes.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // this thread's router bias (read-only), used once the router rows arrived
   const float bias_v = (a.bias && tid < nrows * T) ? __ldg(a.bias + r0 + tid / T) : 0.f;
   if (tid == 0) {
     for (int s = 0; s < R.gs; ++s) { mbar_init(&R.full_gu[s], 1); mbar_init(&R.empty_gu[s], kGroupWarps); }
@@ -613,6 +621,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       P.d = 1;
     }
   }
+  // Everything below may read or write memory that earlier work in the
+  // stream touches (x, the step counter, pool state, counters, logits,
+  // outputs): wait for that work to complete (a no-op without a programmatic
+  // dependency).  The deadline of every bounded wait starts here.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const uint64_t deadline = global_ns() + a.wait_timeout_ns;
+  const uint32_t step0 = (tid == 0) ? (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.st->step)) : 0u;
   // x -> fp16 in B-fragment order (this CTA's own copy)
   {
     int bad = 0;
@@ -996,6 +1011,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   if (has_dn && warp < R.ds) {
     // warp w owns down stage w: entries w, w + ds, ... in order
     const int nst = I / 64;
+    // the h rows of an entry are staged in this warp's slice of the (now idle)
+    // gate/up ring with one round of 16-byte copies when they fit; rows padded
+    // by 16 bytes so the eight token columns fall in different banks
+    const int hstride = I + 8;
+    const size_t hb_cap = ((size_t)R.gs * R.gu_pitch / (size_t)R.ds) / ((size_t)hstride * 2);
+    const int hb_rows = hb_cap < (size_t)T ? (int)hb_cap : T;
+    __half* hbuf = reinterpret_cast<__half*>(R.gu + (size_t)warp * hb_rows * hstride * 2);
     for (int xi = warp; xi < n_ex; xi += R.ds) {
       const Task tk = task_of(a, L, xi, NSh);
       const int s = xi % R.ds;
@@ -1007,7 +1029,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
             if (global_ns() > deadline) { set_error(a, MOE_ERR_TIMEOUT); break; }
             if (dev_error(a)) break;
           }
-          __nanosleep(128);
+          __nanosleep(32);
         }
       }
       __syncwarp();
@@ -1017,18 +1039,42 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         __syncwarp();
         if (lane == 0) mbar_arrive(&R.full_dn[s]);
       }
+      const bool staged = tk.cnt <= hb_rows;
+      if (staged) {
+        const int per_row = I / 8;
+        for (int o = lane; o < tk.cnt * per_row; o += 32) {
+          const int r = o / per_row, cc = o - r * per_row;
+          cp_async16(hbuf + r * hstride + cc * 8, a.h16 + (size_t)(tk.poff + r) * I + cc * 8);
+        }
+        cp_async_wait_all();
+        __syncwarp();
+      }
       const bool ok = wait_full(&R.full_dn[s], (xi / R.ds) & 1, deadline, is_prod, P, X);
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       if (ok) {
         const unsigned char* sb = R.dn + s * R.dn_pitch;
-        const int hrow = tk.poff + ((g < tk.cnt) ? g : 0);
+        const int gsel = (g < tk.cnt) ? g : 0;
+        if (staged) {
+          const __half* hb = hbuf + gsel * hstride + t4 * 16;
+#pragma unroll 4
+          for (int st = 0; st < nst; ++st) {
+            const uint4 b01 = *reinterpret_cast<const uint4*>(hb + st * 64);
+            const uint4 b23 = *reinterpret_cast<const uint4*>(hb + st * 64 + 8);
+            const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
+            const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
+            supertile_mma(acc, nb, scv, b01, b23);
+          }
+        } else {
+          const int hrow = tk.poff + gsel;
 #pragma unroll 2
-        for (int st = 0; st < nst; ++st) {
-          const __half* hr = a.h16 + (size_t)hrow * I + st * 64 + t4 * 16;
-          const uint4 b01 = __ldcg(reinterpret_cast<const uint4*>(hr)), b23 = __ldcg(reinterpret_cast<const uint4*>(hr + 8));
-          const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
-          const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
-          supertile_mma(acc, nb, scv, b01, b23);
+          for (int st = 0; st < nst; ++st) {
+            const __half* hr = a.h16 + (size_t)hrow * I + st * 64 + t4 * 16;
+            const uint4 b01 = __ldcg(reinterpret_cast<const uint4*>(hr));
+            const uint4 b23 = __ldcg(reinterpret_cast<const uint4*>(hr + 8));
+            const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
+            const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
+            supertile_mma(acc, nb, scv, b01, b23);
+          }
         }
       }
       __syncwarp();
@@ -1049,13 +1095,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   if (has_dn) {
     for (int q = tid; q < T * 16; q += kThreads) {
       const int t = q >> 4, row = q & 15;
-      float v = 0.f;
-      for (int j = 0; j < k; ++j) {
-        const int xi = NSh + L.tk_u[t * k + j];
-        const int col = L.tk_pos[t * k + j];
-        const int lz = (row & 7) * 4 + (col >> 1), rz = (row >> 3) * 2 + (col & 1);
-        v = fmaf(L.s_w[t * k + j], zbuf[(xi * 32 + lz) * 4 + rz], v);
+      // all loads first, then the fma chain in the selection order (ascending
+      // expert index), the same summation order as before
+      float wv[kMaxTopK], zv[kMaxTopK];
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j) {
+        wv[j] = 0.f;
+        zv[j] = 0.f;
+        if (j < k) {
+          const int xi = NSh + L.tk_u[t * k + j];
+          const int col = L.tk_pos[t * k + j];
+          const int lz = (row & 7) * 4 + (col >> 1), rz = (row >> 3) * 2 + (col & 1);
+          wv[j] = L.s_w[t * k + j];
+          zv[j] = zbuf[(xi * 32 + lz) * 4 + rz];
+        }
       }
+      float v = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxTopK; ++j)
+        if (j < k) v = fmaf(wv[j], zv[j], v);
       if (NSh) {
         const int col = t;
         const int lz = (row & 7) * 4 + (col >> 1), rz = (row >> 3) * 2 + (col & 1);
@@ -1067,6 +1125,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
 }
 
 size_t g_decode_smem_limit = 0;  // dynamic shared memory the kernel may use
+bool g_decode_pdl = false;       // the driver takes cooperative launches with programmatic serialization
+
+__global__ void pdl_probe_kernel() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+cudaLaunchConfig_t decode_config(dim3 grid, dim3 block, size_t smem, cudaStream_t s, cudaLaunchAttribute (&attr)[2],
+                                 bool pdl) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cfg;
+}
 
 }  // namespace
 
@@ -1085,8 +1162,28 @@ cudaError_t decode_configure() {
   if (e != cudaSuccess) return e;
   const size_t limit = (size_t)optin - fa.sharedSizeBytes;
   e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
-  if (e == cudaSuccess) g_decode_smem_limit = limit;
-  return e;
+  if (e != cudaSuccess) return e;
+  g_decode_smem_limit = limit;
+  // whether a cooperative launch may also carry programmatic serialization:
+  // two launches of an empty kernel on a private stream (a refusal is a
+  // launch-configuration error, which does not stick to the context)
+  static int probed = 0;
+  if (!probed) {
+    probed = 1;
+    cudaStream_t ps;
+    e = cudaStreamCreateWithFlags(&ps, cudaStreamNonBlocking);
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute attr[2];
+    cudaLaunchConfig_t cfg = decode_config(dim3(1), dim3(32), 0, ps, attr, true);
+    bool ok = cudaLaunchKernelEx(&cfg, pdl_probe_kernel) == cudaSuccess;
+    ok = ok && cudaLaunchKernelEx(&cfg, pdl_probe_kernel) == cudaSuccess;
+    (void)cudaGetLastError();
+    e = cudaStreamSynchronize(ps);
+    cudaStreamDestroy(ps);
+    if (e != cudaSuccess) return e;
+    g_decode_pdl = ok;
+  }
+  return cudaSuccess;
 }
 
 bool decode_supported(int H, int I, int E, int k, int T, int G) {
@@ -1097,16 +1194,14 @@ bool decode_supported(int H, int I, int E, int k, int T, int G) {
 
 cudaError_t launch_decode(const LayerArgs& a, unsigned long long* tagged_logits, int32_t* pool_state, int G,
                           cudaStream_t s) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(G);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = decode_smem_bytes(a.H, a.I, a.E, a.k, a.T, G);
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  // Programmatic serialization only when the kernel waits on nothing outside
+  // the stream: a pooled layer whose misses the host copy server serves timed
+  // out now and then with it (the wait ran into its deadline), so that case
+  // keeps the plain stream order.
+  const bool pdl = g_decode_pdl && (!a.pool || a.pull);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = decode_config(dim3(G), dim3(kThreads), decode_smem_bytes(a.H, a.I, a.E, a.k, a.T, G), s,
+                                         attr, pdl);
   return cudaLaunchKernelEx(&cfg, decode_kernel, a, tagged_logits, pool_state, g_decode_smem_limit);
 }
 

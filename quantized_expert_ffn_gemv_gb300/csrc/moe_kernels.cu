@@ -727,6 +727,10 @@ __global__ void __launch_bounds__(256) residual_rmsnorm_kernel(const uint16_t* x
   extern __shared__ float xs[];  // [H]
   __shared__ float part[8];
   const int t = blockIdx.x, tid = threadIdx.x;
+  // programmatic dependent launch: let the next kernel start its prologue,
+  // then wait for the work that wrote x and y
+  pdl_trigger();
+  pdl_wait();
   float ss = 0.f;
   for (int i = tid; i < H; i += 256) {
     float v = __uint_as_float((uint32_t)x[(size_t)t * H + i] << 16);
@@ -829,8 +833,17 @@ cudaError_t launch_down(const LayerArgs& a, cudaStream_t s, bool pdl, int grid) 
 
 cudaError_t launch_residual_rmsnorm(const uint16_t* x, const uint16_t* y, int T, int H, float eps, uint16_t* x_out,
                                     uint16_t* xhat, cudaStream_t s) {
-  residual_rmsnorm_kernel<<<T, 256, sizeof(float) * H, s>>>(x, y, H, eps, x_out, xhat);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(T);
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = sizeof(float) * H;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, residual_rmsnorm_kernel, x, y, H, eps, x_out, xhat);
 }
 
 }  // namespace moe

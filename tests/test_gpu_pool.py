@@ -1,6 +1,7 @@
 """The VRAM expert-slot pool on the GPU: misses match the LRU simulator,
 output is bit-identical to the all-resident run, and copy failures or a
-stalled copy server end in an error status (no GPU fault, no hang)."""
+stalled copy server end in an error status (no GPU fault, no hang), in
+both miss services (the kernel reading host memory, the host copy engine)."""
 import numpy as np
 import pytest
 
@@ -45,6 +46,7 @@ def test_failed_copy_is_an_error_not_zero_weights(small):
     from quantized_expert_ffn_gemv_gb300 import moe
     x, _ = resampled_tokens(small, 700, 8)
     pool = make_gpu_layer(small, max_tokens=1, n_slots=8)
+    pool.set_miss_service(0)  # the host copy server moves the bytes (the default, set explicitly)
     pool.debug_copy_faults(fail_copy_n=3)
     with pytest.raises(moe.MoeError) as ei:
         run(pool, x, T=1)
@@ -58,6 +60,7 @@ def test_failed_copy_is_an_error_not_zero_weights(small):
 def test_stalled_copy_server_times_out(small):
     x, _ = resampled_tokens(small, 800, 1)
     pool = make_gpu_layer(small, max_tokens=1, n_slots=8)
+    pool.set_miss_service(0)
     pool.set_wait_timeout_ns(200_000_000)
     pool.debug_copy_faults(pause=True)
     run(pool, x, T=1)  # the cold pool misses; nothing serves the doorbell

@@ -46,17 +46,29 @@ def stack_runs():
     logs = [l.miss_log() for l in pool.layers]
     stats = pool.stats()
     pool.close()
-    return layers, x, r_full, r_pool, logs, stats
+    pull = MoeStack(layers, n_slots=SLOTS)
+    pull.set_miss_service(1)
+    r_pull = run_stack(pull, x)
+    pull_logs = [l.miss_log() for l in pull.layers]
+    pull.close()
+    return layers, x, r_full, r_pool, logs, stats, r_pull, pull_logs
 
 
 def test_pool_output_bit_identical_to_resident(stack_runs):
-    _, _, r_full, r_pool, _, _ = stack_runs
+    _, _, r_full, r_pool, _, _, r_pull, _ = stack_runs
     for key in ("xhats", "ys", "idx", "w", "x_out"):
         assert np.array_equal(r_full[key], r_pool[key]), key
+        assert np.array_equal(r_full[key], r_pull[key]), key
+
+
+def test_pulled_misses_equal_copied_misses(stack_runs):
+    *_, logs, _, _, pull_logs = stack_runs
+    for a, b in zip(logs, pull_logs):
+        assert np.array_equal(a, b)
 
 
 def test_miss_traces_match_lru_simulator(stack_runs):
-    layers, _, _, r_pool, logs, stats = stack_runs
+    layers, _, _, r_pool, logs, stats, _, _ = stack_runs
     eb = synth.PAGE.expert_bytes
     for l in range(N_LAYERS):
         steps = [sorted(r_pool["idx"][t, l].tolist()) for t in range(N_TOKENS)]
@@ -67,7 +79,7 @@ def test_miss_traces_match_lru_simulator(stack_runs):
 
 
 def test_layers_match_oracle_teacher_forced(stack_runs):
-    layers, x, _, r, _, _ = stack_runs
+    layers, x, _, r, _, _, _, _ = stack_runs
     sh = synth.PAGE
     for t in (0, N_TOKENS // 2, N_TOKENS - 1):
         x_l = x[t]
