@@ -47,8 +47,8 @@ EXPERT_BYTES = 1_769_472
 ROUTER_BYTES = E * H * 4
 STEP_BYTES_PER_TOKEN = ROUTER_BYTES + (K + 1) * EXPERT_BYTES  # 23,658,496
 WORKLOAD = ("page-scale MoE layer decode, batch 1: H 2048, 512 routed experts top-10 + 1 shared, I 512, "
-            "4-bit block-32 fp16-scale weights, Zipf(1.1) router bias; 1000 tokens per step over 8 identical "
-            "layer replicas round-robin, all experts resident")
+            "4-bit block-32 fp16-scale weights, Zipf(1.1) router bias; {tokens} tokens per step over {replicas} "
+            "identical layer replicas round-robin, all experts resident")
 
 
 def dist_env():
@@ -174,7 +174,8 @@ def run_reference(args):
             "warmup": args.warmup, "ms_per_step": 1e3 * tot / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": WORKLOAD, "sample_tokens_per_step": per_step},
+            "config": {"workload": WORKLOAD.format(tokens=args.tokens, replicas=args.replicas),
+                       "sample_tokens_per_step": per_step},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": f"{per_step} decode tokens per step, single-threaded binary64 C oracle"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -378,14 +379,14 @@ def run_prefill(args):
         "config": {"workload": "page-scale MoE layer prefill chunk: 4096 tokens, H 2048, 512 routed experts "
                                "top-10 + 1 shared, I 512, Zipf(1.1) router bias, all experts resident",
                    "l2": "inputs larger than L2 (0.91 GB of expert weights per step)"},
-        "roofline": {"bound": "tensor", "kernel": "whole moe_forward call (7 kernels)", "achieved": tflops,
+        "roofline": {"bound": "tensor", "kernel": "whole moe_forward call (9 kernels)", "achieved": tflops,
                      "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
                      "peak_kind": "measured bf16 burst (f16 runs at the bf16 rate)",
                      "flops_per_unit": PREFILL_FLOPS, "unit_of_work": "4096-token chunk", "traffic": None,
                      "hbm_frac": PREFILL_WEIGHT_BYTES / per_call / 1e9 / hbm_peak},
         "e2e": {"value": PREFILL_T * args.steps / (ms_e2e * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_pin.numel() * 2), "d2h_bytes_per_step": int(y_pin.numel() * 2)},
-        "gpu_launches": 7 * args.steps,
+        "gpu_launches": 9 * args.steps,  # prep, router, top-k, prefix, scan, pairs, 2 expert GEMMs, combine
         "clocks": clocks.summary(0),
     }
     if args.cpu_sample > 0:
@@ -519,7 +520,8 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16xf16+f32 (4-bit weights)", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "tokens_per_step": ntok, "replicas": len(layers),
+        "config": {"workload": WORKLOAD.format(tokens=ntok, replicas=len(layers)), "tokens_per_step": ntok,
+                   "replicas": len(layers),
                    "l2": f"inputs larger than L2 ({len(layers)} layer replicas, "
                          f"{len(layers) * E * EXPERT_BYTES / 2**30:.2f} GiB of expert weights, round-robin)",
                    "parallelism": f"replicas x{ws}"},
