@@ -43,6 +43,7 @@ constexpr int kMaxE = 1024;
 constexpr int kRtVec = kMaxHidden / 256;   // float4 per lane per half router row
 constexpr int kMaxGuStages = 4;
 constexpr int kMaxDnStages = 16;
+constexpr int kListStride = kMaxTopK + 1;  // (key, e) entries per warp's top-k list: odd, no bank conflicts
 
 // ------------------------------------------------------------------ PTX helpers
 
@@ -191,6 +192,10 @@ struct Plan {
 
 __host__ __device__ inline size_t al128(size_t v) { return (v + 127) & ~size_t(127); }
 
+// the routing entries (lists, then selections) fit the budget of
+// 4 * kWarps * kMaxTopK (key, e) pairs
+static_assert(kWarps * kListStride + kMaxT * kMaxTopK <= 4 * kWarps * kMaxTopK, "routing scratch");
+
 __host__ __device__ inline Plan plan_with(int H, int I, int E, int k, int T, int G, int gs, int ds) {
   Plan p;
   p.rows_max = (E + G - 1) / G;
@@ -206,8 +211,8 @@ __host__ __device__ inline Plan plan_with(int H, int I, int E, int k, int T, int
   o += al128((size_t)T * H * 2);
   // region A: router rows (prologue), routing scratch, then down results
   const size_t router = (size_t)p.rows_max * H * 4;
-  // tokmask [E], then (key, e) entries: 16 lists of kMaxTopK, merge candidates,
-  // selections; then the pool scratch (owner, stamp, key per slot, S <= E)
+  // tokmask [E], then (key, e) entries: 16 lists of kListStride, selections;
+  // then the pool scratch (owner, stamp, key per slot, S <= E)
   const size_t routing = al128((size_t)E * 8) + (size_t)4 * kWarps * kMaxTopK * 8 + (size_t)E * 16 + 16 +
                          (size_t)(p.umax + 2) * 8;
   const size_t zbuf = (size_t)(p.umax + 1) * 32 * 4 * 4;
@@ -488,22 +493,28 @@ __device__ void warp_topk(const unsigned long long* logits, int E, int k, int ba
 }
 
 // One warp per token: a k-way merge of the token's nl rank-ordered lists
-// (lane l < nl owns list l; key 0 = none).  Each round takes the best head
-// (larger key, then lower expert) and advances that list.  sel gets the
-// token's k largest logits in rank order.
-__device__ void merge_lists(const uint2* lists, int nl, int k, uint2* sel) {
+// (lane l < nl owns list l at lists[l * kListStride], key 0 = none).  Each
+// round takes the best head (larger key, then lower expert) and advances that
+// list; every lane keeps its list's next entry in a register, so an advance
+// is a register move and the load behind it has a round to land.  sel gets
+// the token's k largest logits in rank order.
+__device__ __forceinline__ void merge_lists(const uint2* lists, int nl, int k, uint2* sel) {
   const int lane = threadIdx.x & 31;
-  int ptr = 0;
-  uint2 head = (lane < nl) ? lists[lane * kMaxTopK] : make_uint2(0u, 0xFFFFFFFFu);
-  if (head.x == 0u) head.y = 0xFFFFFFFFu;
+  const uint2 none = make_uint2(0u, 0xFFFFFFFFu);
+  const uint2* my = lists + lane * kListStride;
+  auto entry = [&](int j) {
+    const uint2 v = (lane < nl && j < k) ? my[j] : none;
+    return v.x == 0u ? none : v;
+  };
+  uint2 head = entry(0), next = entry(1);
+  int ptr = 1;  // index of next
   for (int r = 0; r < k; ++r) {
     const uint32_t mx = __reduce_max_sync(0xffffffffu, head.x);
     const uint32_t emin = __reduce_min_sync(0xffffffffu, head.x == mx ? head.y : 0xFFFFFFFFu);
     if (lane == 0) sel[r] = make_uint2(mx, emin);
     if (mx != 0u && head.x == mx && head.y == emin) {
-      ++ptr;
-      head = (ptr < k) ? lists[lane * kMaxTopK + ptr] : make_uint2(0u, 0xFFFFFFFFu);
-      if (head.x == 0u) head.y = 0xFFFFFFFFu;
+      head = next;
+      next = entry(++ptr);
     }
   }
   __syncwarp();
@@ -513,7 +524,7 @@ __device__ void merge_lists(const uint2* lists, int nl, int k, uint2* sel) {
 // ascending expert order with softmax weights renormalised over the k (the
 // sum taken in ascending expert order, as on the batched path); marks the
 // token in tokmask.  sel is reused as scratch.
-__device__ void finish_topk(uint2* sel, int k, const Lists& L, unsigned long long* tokmask, int t, bool write_out,
+__device__ __forceinline__ void finish_topk(uint2* sel, int k, const Lists& L, unsigned long long* tokmask, int t, bool write_out,
                             const LayerArgs& a) {
   const int lane = threadIdx.x & 31;
   const uint2 me = (lane < k) ? sel[lane] : make_uint2(0u, 0u);
@@ -522,14 +533,22 @@ __device__ void finish_topk(uint2* sel, int k, const Lists& L, unsigned long lon
   const float m = __shfl_sync(0xffffffffu, v, 0);  // rank 0 holds the largest logit
   int pos = 0;
 #pragma unroll
-  for (int j = 0; j < kMaxTopK; ++j) pos += (j < k) && (__shfl_sync(0xffffffffu, my_e, j) < my_e);
+  for (int j = 0; j < kMaxTopK; ++j) {
+    const int ej = __shfl_sync(0xffffffffu, my_e, j);
+    pos += (int)((j < k) & (ej < my_e));
+  }
   const float ex = (lane < k) ? expf(v - m) : 0.f;
   float* ex_sorted = reinterpret_cast<float*>(sel);
   __syncwarp();
   if (lane < k) ex_sorted[pos] = ex;
   __syncwarp();
+  float exs[kMaxTopK];  // all loads first, then the sum in ascending expert order
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) exs[j] = (j < k) ? ex_sorted[j] : 0.f;
   float z = 0.f;
-  for (int j = 0; j < k; ++j) z += ex_sorted[j];
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j)
+    if (j < k) z += exs[j];
   if (lane < k) {
     const float wj = ex / z;
     L.s_idx[t * k + pos] = my_e;
@@ -538,7 +557,7 @@ __device__ void finish_topk(uint2* sel, int k, const Lists& L, unsigned long lon
       a.topk_idx[t * k + pos] = my_e;
       a.topk_w[t * k + pos] = wj;
     }
-    atomicOr(&tokmask[my_e], 1ull << t);
+    atomicOr(reinterpret_cast<unsigned int*>(&tokmask[my_e]), 1u << t);  // low word: t < 8
   }
 }
 
@@ -765,7 +784,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
 
   // ---- routing, redundantly in every CTA
   unsigned long long* tokmask = reinterpret_cast<unsigned long long*>(sm + PL.regA);
-  uint2* wlist = reinterpret_cast<uint2*>(sm + PL.regA + al128((size_t)E * 8));  // [16 warps][kMaxTopK] (key, e)
+  uint2* wlist = reinterpret_cast<uint2*>(sm + PL.regA + al128((size_t)E * 8));  // [16 warps][kListStride] (key, e)
   for (int e = tid; e < E; e += kThreads) tokmask[e] = 0ull;
   if (c == 0)  // the other parity's counters, for the next call
     for (int i = tid; i < a.cnt_stride; i += kThreads) cnt_next[i] = 0u;
@@ -779,20 +798,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     const int base = wt * range;
     if (t < T) {
       if (cpl == 1)
-        warp_topk<1>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
+        warp_topk<1>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
       else if (cpl <= 2)
-        warp_topk<2>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
+        warp_topk<2>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
       else if (cpl <= 4)
-        warp_topk<4>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
+        warp_topk<4>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
       else if (cpl <= 8)
-        warp_topk<8>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
+        warp_topk<8>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
       else
-        warp_topk<16>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kMaxTopK, a, deadline);
+        warp_topk<16>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
     }
     __syncthreads();
-    uint2* sel = wlist + kWarps * kMaxTopK;  // [T][kMaxTopK]
+    uint2* sel = wlist + kWarps * kListStride;  // [T][kMaxTopK]
     if (warp < T) {
-      merge_lists(wlist + warp * wpt * kMaxTopK, wpt, k, sel + warp * kMaxTopK);
+      merge_lists(wlist + warp * wpt * kListStride, wpt, k, sel + warp * kMaxTopK);
       finish_topk(sel + warp * kMaxTopK, k, L, tokmask, warp, c == 0, a);
     }
   }
