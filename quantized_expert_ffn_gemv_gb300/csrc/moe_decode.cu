@@ -523,9 +523,11 @@ __device__ __forceinline__ void merge_lists(const uint2* lists, int nl, int k, u
 // One warp per token: the k selected (in rank order in sel) reported in
 // ascending expert order with softmax weights renormalised over the k (the
 // sum taken in ascending expert order, as on the batched path); marks the
-// token in tokmask.  sel is reused as scratch.
+// token in tokmask.  With rank_union (one token) the union entries are in
+// rank order and the combine mapping is written here.  sel is reused as
+// scratch.
 __device__ __forceinline__ void finish_topk(uint2* sel, int k, const Lists& L, unsigned long long* tokmask, int t, bool write_out,
-                            const LayerArgs& a) {
+                                            const LayerArgs& a, bool rank_union = false) {
   const int lane = threadIdx.x & 31;
   const uint2 me = (lane < k) ? sel[lane] : make_uint2(0u, 0u);
   const int my_e = (lane < k) ? (int)me.y : INT_MAX;
@@ -553,6 +555,10 @@ __device__ __forceinline__ void finish_topk(uint2* sel, int k, const Lists& L, u
     const float wj = ex / z;
     L.s_idx[t * k + pos] = my_e;
     L.s_w[t * k + pos] = wj;
+    if (rank_union) {  // one token, union in rank order: the expert at position pos is union entry lane
+      L.tk_u[pos] = lane;
+      L.tk_pos[pos] = 0;
+    }
     if (write_out) {
       a.topk_idx[t * k + pos] = my_e;
       a.topk_w[t * k + pos] = wj;
@@ -785,6 +791,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   // ---- routing, redundantly in every CTA
   unsigned long long* tokmask = reinterpret_cast<unsigned long long*>(sm + PL.regA);
   uint2* wlist = reinterpret_cast<uint2*>(sm + PL.regA + al128((size_t)E * 8));  // [16 warps][kListStride] (key, e)
+  uint2* sel = wlist + kWarps * kListStride;                                     // [T][kMaxTopK] selections
+  // Early path (one token, every expert resident): the experts start right
+  // after the merge; a warp with no gate/up or down role finishes the
+  // softmax, the combine mapping and the statistics meanwhile.
+  const bool early = T == 1 && !a.pool;
+  const int fin_warp = R.gs < kMaxGuStages ? R.gs * kGroupWarps : 0;
   for (int e = tid; e < E; e += kThreads) tokmask[e] = 0ull;
   if (c == 0)  // the other parity's counters, for the next call
     for (int i = tid; i < a.cnt_stride; i += kThreads) cnt_next[i] = 0u;
@@ -809,17 +821,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         warp_topk<16>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
     }
     __syncthreads();
-    uint2* sel = wlist + kWarps * kListStride;  // [T][kMaxTopK]
     if (warp < T) {
       merge_lists(wlist + warp * wpt * kListStride, wpt, k, sel + warp * kMaxTopK);
-      finish_topk(sel + warp * kMaxTopK, k, L, tokmask, warp, c == 0, a);
+      if (!early) finish_topk(sel + warp * kMaxTopK, k, L, tokmask, warp, c == 0, a);
     }
   }
   __syncthreads();
   // union of the selected experts (ascending) and pair offsets, from the
   // T*k selected pairs: entry p is the first of its expert when no earlier
-  // token selected it.  One token: the union is the selection itself.
-  if (T == 1) {
+  // token selected it.  One token: the union is the selection itself (in rank
+  // order on the early path, known as soon as the merge ends).
+  if (early) {
+    if (tid < k) {
+      const int e = (int)sel[tid].y;
+      L.u_expert[tid] = e;
+      L.u_off[tid] = tid;
+      L.u_slot[tid] = e;
+      L.u_wait[tid] = 0u;
+      L.pair_token[tid] = 0;
+    }
+    if (tid == 0) {
+      L.u_off[k] = k;
+      s_nunion = k;
+      s_nmiss = 0;
+    }
+  } else if (T == 1) {
     if (tid < k) {
       const int e = L.s_idx[tid];
       L.u_expert[tid] = e;
@@ -880,7 +906,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   int32_t* nxt_owner = nxt_slot + E;
   uint32_t* nxt_stamp = reinterpret_cast<uint32_t*>(nxt_owner + S);
   if (!a.pool) {
-    if (tid == 0) s_nmiss = 0;
+    if (tid == 0 && !early) s_nmiss = 0;  // the early path set it before the barrier above
   } else {
     // pool scratch in region A after the routing lists: per slot owner, stamp
     // and candidate key; per union entry its miss number; the ranked victims
@@ -986,7 +1012,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       }
     }
   }
-  if (c == 0 && tid == 0) {
+  if (c == 0 && tid == (early ? fin_warp * 32 : 0)) {
     // stores and reductions only: nothing here waits for the (possibly cold) counters
     a.st->step = seq;
     a.st->n_union = n_union;
@@ -995,7 +1021,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     atomicAdd(&a.st->hits, (unsigned long long)(n_union - s_nmiss));
     atomicAdd(&a.st->misses, (unsigned long long)s_nmiss);
   }
-  __syncthreads();
+  if (!early) __syncthreads();  // the early path's union was published by the barrier above
+  if (early && warp == fin_warp) finish_topk(sel, k, L, tokmask, 0, c == 0, a, true);
 
   // ---- experts
   const int n_ex = NSh + n_union;
