@@ -22,7 +22,7 @@ def resampled_tokens(layer, t0, T, stream=0, gap=GAP, max_redraw=64):
         bad = []
         for t in range(T):
             srt = np.sort(l[t])[::-1]
-            if srt[sh.k - 1] - srt[sh.k] < gap:
+            if sh.k < sh.E and srt[sh.k - 1] - srt[sh.k] < gap:  # k = E: no boundary to guard
                 bad.append(t)
         if not bad:
             return x, sub
