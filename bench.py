@@ -58,6 +58,22 @@ def dist_env():
     return ws, rank, local
 
 
+def max_over_ranks(values, pg=None, device="cpu"):
+    """Elementwise max of per-rank figures (the slowest rank sets the job's
+    time); the values themselves on one rank."""
+    if pg is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank, world_size, ms):
+    """Units all ranks processed per second of the slowest rank's time."""
+    return units_per_rank * world_size / (ms * 1e-3)
+
+
 def measured_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -504,15 +520,12 @@ def main():
         s, code = l.stats()
         if code != 0:
             raise RuntimeError(f"layer error {code}")
-    if pg:
-        t = torch.tensor([ms, ms_e2e], device="cuda")
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms, ms_e2e = t.tolist()
+    ms, ms_e2e = max_over_ranks([ms, ms_e2e], pg, device="cuda")
     if rank != 0:
         pg.destroy_process_group() if pg else None
         return
     tokens = ntok * args.steps * ws
-    value = tokens / (ms * 1e-3)
+    value = whole_job_rate(ntok * args.steps, ws, ms)
     per_token_s = (ms * 1e-3) / (ntok * args.steps)
     peak, peak_kind = measured_peak()
     achieved = STEP_BYTES_PER_TOKEN / per_token_s / 1e9
@@ -529,7 +542,8 @@ def main():
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "bytes_per_unit": STEP_BYTES_PER_TOKEN, "unit_of_work": "token",
                      "traffic": recorded_traffic()},
-        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": int(x_pin.numel() * 2),
+        "e2e": {"value": whole_job_rate(ntok * args.steps, ws, ms_e2e), "unit": UNIT,
+                "h2d_bytes_per_step": int(x_pin.numel() * 2),
                 "d2h_bytes_per_step": int(y_pin.numel() * 2)},
         "gpu_launches": ntok * args.steps,  # one fused kernel per token (T = 1)
         "clocks": clocks.summary(local),

@@ -581,8 +581,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // Warps 9-16 (gather): their 256 threads copy the chunk's B rows with
 //   cp.async as far ahead as the B ring allows, each signalling b_full when
 //   its copies land.  A k-step's commit arrives on its B stage's empty barrier; the A
-//   ring (kAStages < kBStages) is reused once the MMA of k-step g - kAStages
-//   has completed, i.e. when that k-step's B stage is released.  The MMA
+//   ring (kAStages <= kBStages) is reused once the MMA of k-step g - kAStages
+//   has completed, i.e. when that k-step's B stage is released.  With more A
+//   than B stages that barrier could run two phases past the awaited one.  The MMA
 //   thread orders both halves (generic-proxy writes) before its tensor-core
 //   reads with one proxy fence after its waits.
 // Warp 17: TMEM allocation (2 x 256 columns); lane 0 issues the MMAs.
@@ -590,6 +591,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 //   half of the chunk's columns.
 constexpr int kAStages = 3;
 constexpr int kBStages = 4;
+static_assert(kAStages <= kBStages, "A stages are released through the B stages' empty barriers");
 constexpr int kRawR = 2;
 constexpr int kRawStages = 2;
 constexpr int kProd = 8;    // dequant warps
