@@ -88,7 +88,7 @@ def source_hash():
     only while the kernel it was measured on is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_expert_ffn_gemv_gb300", "csrc")
-    for f in ("moe_decode.cu", "moe_internal.h"):
+    for f in ("moe_decode.cu", "moe_internal.h", "moe_mma.cuh"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -395,14 +395,14 @@ def run_prefill(args):
         "config": {"workload": "page-scale MoE layer prefill chunk: 4096 tokens, H 2048, 512 routed experts "
                                "top-10 + 1 shared, I 512, Zipf(1.1) router bias, all experts resident",
                    "l2": "inputs larger than L2 (0.91 GB of expert weights per step)"},
-        "roofline": {"bound": "tensor", "kernel": "whole moe_forward call (9 kernels)", "achieved": tflops,
+        "roofline": {"bound": "tensor", "kernel": "whole moe_forward call (11 kernels)", "achieved": tflops,
                      "peak": tpeak, "unit": "TFLOP/s", "frac": tflops / tpeak,
                      "peak_kind": "measured bf16 burst (f16 runs at the bf16 rate)",
                      "flops_per_unit": PREFILL_FLOPS, "unit_of_work": "4096-token chunk", "traffic": None,
                      "hbm_frac": PREFILL_WEIGHT_BYTES / per_call / 1e9 / hbm_peak},
         "e2e": {"value": PREFILL_T * args.steps / (ms_e2e * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(x_pin.numel() * 2), "d2h_bytes_per_step": int(y_pin.numel() * 2)},
-        "gpu_launches": 9 * args.steps,  # prep, router, top-k, prefix, scan, pairs, 2 expert GEMMs, combine
+        "gpu_launches": 11 * args.steps,  # prep, router, top-k, prefix, scan, pairs, 2 small-chunk + 2 tensor-core GEMMs, combine
         "clocks": clocks.summary(0),
     }
     if args.cpu_sample > 0:

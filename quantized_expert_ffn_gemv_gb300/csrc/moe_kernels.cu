@@ -21,6 +21,7 @@
 
 #include "moe.h"
 #include "moe_internal.h"
+#include "moe_mma.cuh"
 
 namespace moe {
 namespace {
@@ -60,63 +61,6 @@ __device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
-}
-
-__device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-// 8 packed nibbles (GPU layout word) -> the 4 f16x2 registers of an A fragment,
-// holding q = u - 8 exactly.  A low nibble of a half becomes 1024 + u through
-// the 0x6400 exponent (minus 1032 -> q); a high nibble becomes 1024 + 16u
-// (times 1/16 minus 72 -> q).
-__device__ __forceinline__ void dequant_word(uint32_t w, uint32_t (&a)[4]) {
-  const uint32_t lo0 = (w & 0x000F000Fu) | 0x64006400u;
-  const uint32_t hi0 = (w & 0x00F000F0u) | 0x64006400u;
-  const uint32_t w8 = w >> 8;
-  const uint32_t lo1 = (w8 & 0x000F000Fu) | 0x64006400u;
-  const uint32_t hi1 = (w8 & 0x00F000F0u) | 0x64006400u;
-  const __half2 k1032 = __halves2half2(__ushort_as_half(0x6408), __ushort_as_half(0x6408));
-  const __half2 k16th = __halves2half2(__ushort_as_half(0x2C00), __ushort_as_half(0x2C00));
-  const __half2 km72 = __halves2half2(__ushort_as_half(0xD480), __ushort_as_half(0xD480));
-  __half2 r0 = __hsub2(*reinterpret_cast<const __half2*>(&lo0), k1032);
-  __half2 r1 = __hsub2(*reinterpret_cast<const __half2*>(&lo1), k1032);
-  __half2 r2 = __hfma2(*reinterpret_cast<const __half2*>(&hi0), k16th, km72);
-  __half2 r3 = __hfma2(*reinterpret_cast<const __half2*>(&hi1), k16th, km72);
-  a[0] = *reinterpret_cast<uint32_t*>(&r0);  // row g,   k 2t..2t+1
-  a[1] = *reinterpret_cast<uint32_t*>(&r1);  // row g+8, k 2t..2t+1
-  a[2] = *reinterpret_cast<uint32_t*>(&r2);  // row g,   k 2t+8..2t+9
-  a[3] = *reinterpret_cast<uint32_t*>(&r3);  // row g+8, k 2t+8..2t+9
-}
-
-__device__ __forceinline__ float half_lo(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v & 0xFFFF))); }
-__device__ __forceinline__ float half_hi(uint32_t v) { return __half2float(__ushort_as_half((uint16_t)(v >> 16))); }
-
-// One 16 x 64 super-tile against one n8 group of activations: 2 scale blocks,
-// each the exact fp32 scaling of a 32-long integer-weight dot product.
-__device__ __forceinline__ void supertile_mma(float (&acc)[4], const uint4& nib, const uint2& sc, const uint4& b01,
-                                              const uint4& b23) {
-  const uint32_t words[4] = {nib.x, nib.y, nib.z, nib.w};
-  const uint32_t bb[4][2] = {{b01.x, b01.y}, {b01.z, b01.w}, {b23.x, b23.y}, {b23.z, b23.w}};
-  const float d[4] = {half_lo(sc.x), half_hi(sc.x), half_lo(sc.y), half_hi(sc.y)};
-#pragma unroll
-  for (int blk = 0; blk < 2; ++blk) {
-    float tmp[4] = {0.f, 0.f, 0.f, 0.f};
-    uint32_t a[4];
-    dequant_word(words[2 * blk], a);
-    mma16816(tmp, a, bb[2 * blk][0], bb[2 * blk][1]);
-    dequant_word(words[2 * blk + 1], a);
-    mma16816(tmp, a, bb[2 * blk + 1][0], bb[2 * blk + 1][1]);
-    const float dg = d[2 * blk], dg8 = d[2 * blk + 1];
-    acc[0] = fmaf(dg, tmp[0], acc[0]);
-    acc[1] = fmaf(dg, tmp[1], acc[1]);
-    acc[2] = fmaf(dg8, tmp[2], acc[2]);
-    acc[3] = fmaf(dg8, tmp[3], acc[3]);
-  }
 }
 
 __device__ void set_error(const LayerArgs& a, int code) {

@@ -410,7 +410,6 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   L->d.shared = nullptr;
   L->blob = expert_bytes(d.hidden, d.inter);
   const int E = d.n_experts, H = d.hidden, I = d.inter, k = d.top_k, Tm = d.max_tokens;
-  moe_status_t st = MOE_OK;
   auto fail = [&](moe_status_t s) {
     free_layer(L);
     return s;
@@ -542,7 +541,6 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
       cs = nullptr;
       return fail(MOE_ERR_CUDA);
     }
-  (void)st;
   *out = L;
   return MOE_OK;
 }

@@ -35,6 +35,7 @@
 
 #include "moe.h"
 #include "moe_internal.h"
+#include "moe_mma.cuh"
 #include "moe_prefill.h"
 
 namespace moe {
@@ -336,66 +337,83 @@ __global__ void __launch_bounds__(256) prefill_prefix_kernel(LayerArgs a, Prefil
   if (lane == 0) p.counts[e] = run;
 }
 
-// One CTA: offsets and chunk offsets of the E routed experts and the shared
-// expert (entry E, all T tokens); layer statistics.
+// One CTA: offsets and chunk records of the E routed experts and the shared
+// expert (entry E, all T tokens): tensor-core chunks and small chunks; layer
+// statistics.
 __global__ void __launch_bounds__(1024) prefill_scan_kernel(LayerArgs a, PrefillArgs p) {
-  __shared__ int wsum[2][32];
+  __shared__ int wsum[3][32];
   __shared__ int s_used;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, NE = E + a.n_shared;
   const int per = (NE + 1023) / 1024;
   if (tid == 0) s_used = 0;
   __syncthreads();
-  int c_cnt = 0, c_chk = 0, used = 0;
+  // an entry's tokens make full kPfN chunks plus a remainder: a remainder of
+  // more than kSmallN tokens is one more tensor-core chunk, a smaller one a
+  // small chunk
+  int c_cnt = 0, c_chk = 0, c_sml = 0, used = 0;
   for (int i = 0; i < per; ++i) {
     const int e = tid * per + i;
     if (e < NE) {
       const int cnt = (e < E) ? p.counts[e] : a.T;
+      const int rem = cnt % kPfN;
       c_cnt += cnt;
-      c_chk += (cnt + kPfN - 1) / kPfN;
+      c_chk += cnt / kPfN + (rem > kSmallN);
+      c_sml += (rem > 0 && rem <= kSmallN);
       used += (e < E && cnt > 0);
     }
   }
   if (used) atomicAdd(&s_used, used);
-  int ia = c_cnt, ib = c_chk;
+  int ia = c_cnt, ib = c_chk, ic = c_sml;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const int va = __shfl_up_sync(0xffffffffu, ia, o), vb = __shfl_up_sync(0xffffffffu, ib, o);
+    const int va = __shfl_up_sync(0xffffffffu, ia, o), vb = __shfl_up_sync(0xffffffffu, ib, o),
+              vc = __shfl_up_sync(0xffffffffu, ic, o);
     if (lane >= o) {
       ia += va;
       ib += vb;
+      ic += vc;
     }
   }
   if (lane == 31) {
     wsum[0][warp] = ia;
     wsum[1][warp] = ib;
+    wsum[2][warp] = ic;
   }
   __syncthreads();
-  int ba = 0, bb = 0, ta = 0, tb = 0;
+  int ba = 0, bb = 0, bc = 0, ta = 0, tb = 0, tc = 0;
   for (int w = 0; w < 32; ++w) {
     if (w < warp) {
       ba += wsum[0][w];
       bb += wsum[1][w];
+      bc += wsum[2][w];
     }
     ta += wsum[0][w];
     tb += wsum[1][w];
+    tc += wsum[2][w];
   }
-  int oa = ba + ia - c_cnt, ob = bb + ib - c_chk;
+  int oa = ba + ia - c_cnt, ob = bb + ib - c_chk, oc = bc + ic - c_sml;
   for (int i = 0; i < per; ++i) {
     const int e = tid * per + i;
     if (e < NE) {
       const int cnt = (e < E) ? p.counts[e] : a.T;
+      const int full = cnt / kPfN, rem = cnt - full * kPfN;
       p.offsets[e] = oa;
       p.chunk_off[e] = ob;
-      for (int c = 0; c * kPfN < cnt; ++c) p.chunk_rec[ob + c] = make_int4(e, oa + c * kPfN, min(kPfN, cnt - c * kPfN), 0);
+      for (int c = 0; c < full; ++c) p.chunk_rec[ob + c] = make_int4(e, oa + c * kPfN, kPfN, 0);
+      if (rem > kSmallN)
+        p.chunk_rec[ob + full] = make_int4(e, oa + full * kPfN, rem, 0);
+      else if (rem > 0)
+        p.small_rec[oc++] = make_int4(e, oa + full * kPfN, rem, 0);
       oa += cnt;
-      ob += (cnt + kPfN - 1) / kPfN;
+      ob += full + (rem > kSmallN);
     }
   }
   if (tid == 0) {
     p.offsets[NE] = ta;
     p.chunk_off[NE] = tb;
     p.n_chunks[0] = tb;
+    p.n_chunks[1] = tc;
     a.st->forwards += 1ull;
     a.st->hits += (unsigned long long)s_used;
   }
@@ -641,6 +659,188 @@ __device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
 //   and of up, K = H.  Tile row of local gate row i: 16 (i / 8) + i % 8; the
 //   matching up row is 8 further, so an epilogue lane pairs with lane ^ 8.
 // MODE 1: down; M-block mb = output rows 128 mb .. 128 mb + 127, K = I.
+// ---- small chunks: an entry's last chunk of at most kSmallN tokens
+//
+// A tensor-core tile costs a full pass of MMA issues whatever its N, so a
+// chunk of a few tokens is cheaper on the legacy path.  A block takes a group
+// of strips of one chunk: it stages the chunk's B rows (x for gate/up, h for
+// down; at most 16) in shared memory with cp.async, then reads each strip's
+// packed weights once from global memory and applies them to the two n8 token
+// groups with mma.sync.  MODE 0: gate/up + SiLU -> h rows, four strips per
+// block, each strip's K split over eight warps (one batch of weight loads
+// each); MODE 1: down -> z rows, sixteen strips per block, a warp per strip
+// over the whole K.  Same outputs, in the same places, as the tensor-core
+// epilogues.
+__host__ __device__ constexpr int sm_warps(int mode) { return mode == 0 ? 8 : 4; }
+constexpr int kSmBatch = 4;  // super-tiles of a warp with their weight loads in flight together
+__host__ __device__ constexpr int sm_strips(int mode) { return mode == 0 ? 4 : 16; }
+// B rows staged with a 16-byte pad: the eight token columns of a fragment
+// load fall in different banks
+__host__ __device__ inline int sm_row(int K) { return K + 8; }
+__host__ __device__ inline size_t sm_smem(int mode, int K) {
+  return (size_t)kSmallN * sm_row(K) * 2 + (mode == 0 ? sizeof(float) * sm_warps(0) * 2 * 32 * 8 : 0);
+}
+
+// Weights of kSmBatch super-tiles st0, st0 + step, ... (gate and, for MODE 0, up).
+template <int MODE>
+__device__ __forceinline__ void sm_load_w(const uint8_t* strip, int K, int st0, int step, int nst, int lane, int g,
+                                          uint4 (&w0)[kSmBatch], uint2 (&s0)[kSmBatch], uint4 (&w1)[kSmBatch],
+                                          uint2 (&s1)[kSmBatch]) {
+#pragma unroll
+  for (int b = 0; b < kSmBatch; ++b) {
+    const int st = st0 + step * b;
+    if (st < nst) {
+      w0[b] = ld_cg4(strip + st * 512 + lane * 16);
+      s0[b] = __ldg(reinterpret_cast<const uint2*>(strip + 8 * K + st * 64 + g * 8));
+      if (MODE == 0) {
+        w1[b] = ld_cg4(strip + 9 * K + st * 512 + lane * 16);
+        s1[b] = __ldg(reinterpret_cast<const uint2*>(strip + 17 * K + st * 64 + g * 8));
+      }
+    }
+  }
+}
+
+// B fragments of super-tile st for n8 group q from the staged rows (natural K
+// order: k16 block j holds k 16j + 2t, +1 and 16j + 8 + 2t, +1).
+__device__ __forceinline__ void sm_load_b(const __half* bs, int K, int q, int st, int g, int t4, uint4& b01,
+                                          uint4& b23) {
+  const uint32_t* r = reinterpret_cast<const uint32_t*>(bs + (size_t)(q * 8 + g) * sm_row(K) + st * 64 + 2 * t4);
+  b01 = make_uint4(r[0], r[4], r[8], r[12]);
+  b23 = make_uint4(r[16], r[20], r[24], r[28]);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(sm_warps(MODE) * 32) prefill_small_kernel(LayerArgs a, PrefillArgs p) {
+  extern __shared__ __align__(16) unsigned char sms[];
+  constexpr int NW = sm_warps(MODE), NT = NW * 32;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, t4 = lane & 3;
+  const int H = a.H, I = a.I, E = a.E;
+  const int K = MODE == 0 ? H : I;
+  const int nst = K / 64;
+  constexpr int SG = sm_strips(MODE);
+  const int groups = (MODE == 0 ? I / 16 : H / 16) / SG;
+  __half* bs = reinterpret_cast<__half*>(sms);                                          // [16][K + 8]
+  float* red = reinterpret_cast<float*>(sms + (size_t)kSmallN * sm_row(K) * 2);  // MODE 0: [NW][2][32][8]
+  const int n_tasks = ld_cg_i32(&p.n_chunks[1]) * groups;
+  for (int task = blockIdx.x; task < n_tasks; task += gridDim.x) {
+    const int c = task / groups, sg = task - c * groups;
+    const int4 rec = ld_cg_int4(&p.small_rec[c]);
+    const int e = rec.x, poff = rec.y, nt = rec.z;
+    const int ng = (nt + 7) >> 3;
+    const uint8_t* base = (e < E) ? a.arena + (int64_t)e * a.blob : a.shared;
+    // the chunk's B rows; rows past nt are zero (row addresses looked up once)
+    __shared__ const __half* s_row[kSmallN];
+    if (tid < kSmallN)
+      s_row[tid] = tid >= nt ? nullptr
+                 : MODE == 0 ? p.x16p + (size_t)ld_cg_i32(&p.pair_token[poff + tid]) * H
+                             : p.h16p + (size_t)(poff + tid) * I;
+    __syncthreads();
+    const int per_row = K / 8;
+    for (int o = tid; o < kSmallN * per_row; o += NT) {
+      const int n = o / per_row, cc = o - n * per_row;
+      __half* dst = bs + (size_t)n * sm_row(K) + cc * 8;
+      const __half* src = s_row[n];
+      if (src)
+        cp_async16(smem_u32(dst), src + cc * 8);
+      else
+        *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    uint4 w0[kSmBatch], w1[kSmBatch];
+    uint2 s0[kSmBatch], s1[kSmBatch];
+    if (MODE == 0) {
+      for (int si = 0; si < SG; ++si) {
+        const int s = sg * SG + si;
+        const uint8_t* strip = base + (int64_t)s * gu_strip_bytes(H);
+        float ag[2][4] = {}, au[2][4] = {};
+        for (int st0 = warp; st0 < nst; st0 += NW * kSmBatch) {
+          sm_load_w<0>(strip, K, st0, NW, nst, lane, g, w0, s0, w1, s1);
+#pragma unroll
+          for (int b = 0; b < kSmBatch; ++b) {
+            const int st = st0 + NW * b;
+            if (st < nst) {
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                if (q < ng) {
+                  uint4 b01, b23;
+                  sm_load_b(bs, K, q, st, g, t4, b01, b23);
+                  supertile_mma(ag[q], w0[b], s0[b], b01, b23);
+                  supertile_mma(au[q], w1[b], s1[b], b01, b23);
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          float4* dst = reinterpret_cast<float4*>(red + ((warp * 2 + q) * 32 + lane) * 8);
+          dst[0] = make_float4(ag[q][0], ag[q][1], ag[q][2], ag[q][3]);
+          dst[1] = make_float4(au[q][0], au[q][1], au[q][2], au[q][3]);
+        }
+        __syncthreads();
+        if (warp < ng) {  // warp q sums the K slices of n8 group q, in warp order
+          const int q = warp;
+          float gv[4] = {0.f, 0.f, 0.f, 0.f}, uv[4] = {0.f, 0.f, 0.f, 0.f};
+          for (int w = 0; w < NW; ++w) {
+            const float4* src = reinterpret_cast<const float4*>(red + ((w * 2 + q) * 32 + lane) * 8);
+            const float4 x0 = src[0], x1 = src[1];
+            gv[0] += x0.x; gv[1] += x0.y; gv[2] += x0.z; gv[3] += x0.w;
+            uv[0] += x1.x; uv[1] += x1.y; uv[2] += x1.z; uv[3] += x1.w;
+          }
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int row = s * 16 + ((cc < 2) ? g : g + 8), n = q * 8 + 2 * t4 + (cc & 1);
+            if (n < nt)
+              p.h16p[(size_t)(poff + n) * I + row] =
+                  __float2half_rn(__fdividef(gv[cc], 1.0f + __expf(-gv[cc])) * uv[cc]);
+          }
+        }
+        __syncthreads();  // red is reused by the next strip
+      }
+    } else {
+      int zr[2][2];  // z rows of this lane's output columns
+#pragma unroll
+      for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int n = q * 8 + 2 * t4 + h;
+          zr[q][h] = n < nt ? ld_cg_i32(&p.pair_z[poff + n]) : 0;
+        }
+      for (int si = warp; si < SG; si += NW) {
+        const int s = sg * SG + si;
+        const uint8_t* strip = base + down_base(H, I) + (int64_t)s * down_strip_bytes(I);
+        float acc[2][4] = {};
+        for (int st0 = 0; st0 < nst; st0 += kSmBatch) {
+          sm_load_w<1>(strip, K, st0, 1, nst, lane, g, w0, s0, w1, s1);
+#pragma unroll
+          for (int b = 0; b < kSmBatch; ++b) {
+            const int st = st0 + b;
+            if (st < nst) {
+#pragma unroll
+              for (int q = 0; q < 2; ++q) {
+                if (q < ng) {
+                  uint4 b01, b23;
+                  sm_load_b(bs, K, q, st, g, t4, b01, b23);
+                  supertile_mma(acc[q], w0[b], s0[b], b01, b23);
+                }
+              }
+            }
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int cc = 0; cc < 4; ++cc) {
+            const int row = s * 16 + ((cc < 2) ? g : g + 8), n = q * 8 + 2 * t4 + (cc & 1);
+            if (n < nt) p.z16[(size_t)zr[q][cc & 1] * H + row] = __float2half_rn(acc[q][cc]);
+          }
+      }
+    }
+    __syncthreads();  // the staged rows are replaced by the next task's
+  }
+}
+
 template <int MODE>
 __global__ void __launch_bounds__(kExpThreads, 1) prefill_expert_kernel(LayerArgs a, PrefillArgs p) {
   extern __shared__ __align__(1024) unsigned char smraw[];
@@ -942,7 +1142,8 @@ size_t prefill_scratch_bytes(int H, int I, int E, int k, int Tm) {
   if (Tm <= kMaxTokens) return 0;
   const size_t P = (size_t)Tm * (k + 1), words = (size_t)(Tm + 31) / 32;
   const size_t chunks = (size_t)E + 2 + P / kPfN;
-  return pf_align(4ull * (E + 1)) + 2 * pf_align(4ull * (E + 2)) + pf_align(4) + pf_align(16 * chunks) +
+  return pf_align(4ull * (E + 1)) + 2 * pf_align(4ull * (E + 2)) + pf_align(8) + pf_align(16 * chunks) +
+         pf_align(16ull * (E + 1)) +
          2 * pf_align(4 * P) +
          2 * pf_align(4ull * E * words) + pf_align(6ull * E * H) + pf_align(2ull * Tm * H) + pf_align(2 * P * I) +
          pf_align(2 * P * H);
@@ -961,8 +1162,9 @@ PrefillArgs prefill_carve(void* block, int H, int I, int E, int k, int Tm) {
   p.counts = (int32_t*)carve(4ull * (E + 1));
   p.offsets = (int32_t*)carve(4ull * (E + 2));
   p.chunk_off = (int32_t*)carve(4ull * (E + 2));
-  p.n_chunks = (int32_t*)carve(4);
+  p.n_chunks = (int32_t*)carve(8);
   p.chunk_rec = (int4*)carve(16 * ((size_t)E + 2 + P / kPfN));
+  p.small_rec = (int4*)carve(16 * ((size_t)E + 1));
   p.pair_token = (int32_t*)carve(4 * P);
   p.pair_z = (int32_t*)carve(4 * P);
   p.bitmap = (uint32_t*)carve(4ull * E * words);
@@ -999,6 +1201,12 @@ cudaError_t prefill_configure() {
     return e;
   if ((e = cudaFuncSetAttribute(prefill_expert_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem)))
     return e;
+  if ((e = cudaFuncSetAttribute(prefill_small_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sm_smem(0, kMaxHidden))))
+    return e;
+  if ((e = cudaFuncSetAttribute(prefill_small_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)sm_smem(1, kMaxInter))))
+    return e;
   return cudaFuncSetAttribute(prefill_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
 }
 
@@ -1029,7 +1237,9 @@ cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, const Prefi
   prefill_prefix_kernel<<<(a.E + 7) / 8, 256, 0, s>>>(a, p);
   prefill_scan_kernel<<<1, 1024, 0, s>>>(a, p);
   prefill_pairs_kernel<<<(a.T * (a.k + 1) + 255) / 256, 256, 0, s>>>(a, p);
+  prefill_small_kernel<0><<<sm_count * 2, sm_warps(0) * 32, sm_smem(0, a.H), s>>>(a, p);
   prefill_expert_kernel<0><<<sm_count, kExpThreads, kGemmSmem, s>>>(a, p);
+  prefill_small_kernel<1><<<sm_count * 8, sm_warps(1) * 32, sm_smem(1, a.I), s>>>(a, p);
   prefill_expert_kernel<1><<<sm_count, kExpThreads, kGemmSmem, s>>>(a, p);
   const long long n = (long long)a.T * (a.H / 8);
   prefill_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, p);

@@ -8,6 +8,7 @@
 namespace moe {
 
 constexpr int kPfN = 256;                // tokens per GEMM chunk (the MMA's N, at most)
+constexpr int kSmallN = 16;              // an expert's last chunk of at most this many tokens takes the mma.sync path
 constexpr int kMaxPrefillTokens = 8192;  // largest T of one prefill call
 
 // Scratch of the prefill kernels.  Pairs are (token, rank) assignments; the
@@ -15,9 +16,11 @@ constexpr int kMaxPrefillTokens = 8192;  // largest T of one prefill call
 struct PrefillArgs {
   int32_t* counts;      // [E + 1] tokens per routed expert (zeroed each call)
   int32_t* offsets;     // [E + 2] first pair of each expert list entry; [NE] = total
-  int32_t* chunk_off;   // [E + 2] first kPfN-token chunk of each entry; [NE] = total
-  int32_t* n_chunks;    // [1]
-  int4* chunk_rec;      // [max chunks] per kPfN-token chunk: {expert list entry, first pair, tokens, 0}
+  int32_t* chunk_off;   // [E + 2] first tensor-core chunk of each entry; [NE] = total
+  int32_t* n_chunks;    // [2] tensor-core chunks, small chunks
+  int4* chunk_rec;      // [max chunks] per tensor-core chunk (more than kSmallN tokens, at most kPfN):
+                        //   {expert list entry, first pair, tokens, 0}
+  int4* small_rec;      // [E + 1] per small chunk (an entry's last, at most kSmallN tokens): same fields
   int32_t* pair_token;  // [T*k + T] token of each pair, grouped by expert, ascending token
   int32_t* pair_z;      // [T*k + T] z row of each pair: t*(k+1) + rank (rank k = shared)
   uint32_t* bitmap;     // [E][ceil(T/32)] bit t of row e: token t selected e (zeroed each call)
