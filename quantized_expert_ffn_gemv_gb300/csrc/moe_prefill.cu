@@ -245,8 +245,8 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(LayerArgs a, PrefillA
   float lv[kRegs];
 #pragma unroll
   for (int i = 0; i < kRegs; ++i) lv[i] = (CPL > 0 && lane + 32 * i < E) ? lt[lane + 32 * i] : -FLT_MAX;
-  int sel[kMaxTopK];
-  float selv[kMaxTopK];
+  int my_e = INT_MAX;   // lane r < k: the expert of rank r
+  float my_v = 0.f;     // and its logit
   uint32_t taken[kMaxExperts / 1024] = {};  // bit i: logit lane + 32 i already selected
   for (int r = 0; r < k; ++r) {
     float bv = -FLT_MAX;
@@ -284,31 +284,36 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(LayerArgs a, PrefillA
       if (lane == 0) set_error(a, MOE_ERR_DEVICE);
       bi = r;
     }
-    if (lane == (bi & 31)) taken[(bi >> 5) >> 5] |= 1u << ((bi >> 5) & 31);
-    sel[r] = bi;
-    selv[r] = bv;
+    if (lane == (bi & 31)) {
+      if (CPL > 0)
+        taken[0] |= 1u << ((bi >> 5) & 31);  // CPL <= 32: one word
+      else
+        taken[(bi >> 5) >> 5] |= 1u << ((bi >> 5) & 31);
+    }
+    if (lane == r) {
+      my_e = bi;
+      my_v = bv;
+    }
   }
-  if (lane == 0) {
-    const float m = selv[0];
-    for (int i = 1; i < k; ++i) {  // ascending expert index
-      const int ki = sel[i];
-      const float kv = selv[i];
-      int j = i - 1;
-      while (j >= 0 && sel[j] > ki) {
-        sel[j + 1] = sel[j];
-        selv[j + 1] = selv[j];
-        --j;
-      }
-      sel[j + 1] = ki;
-      selv[j + 1] = kv;
-    }
-    float z = 0.f;
-    for (int j = 0; j < k; ++j) z += expf(selv[j] - m);
-    for (int j = 0; j < k; ++j) {
-      a.topk_idx[t * k + j] = sel[j];
-      a.topk_w[t * k + j] = expf(selv[j] - m) / z;
-      atomicOr(&p.bitmap[(size_t)sel[j] * p.words + (t >> 5)], 1u << (t & 31));
-    }
+  // in parallel, lane r for rank r: its place in ascending expert order, the
+  // weight exp(v - max) / z with z summed in ascending expert order
+  const float m = __shfl_sync(0xffffffffu, my_v, 0);
+  int pos = 0;
+#pragma unroll
+  for (int j = 0; j < kMaxTopK; ++j) {
+    const int ej = __shfl_sync(0xffffffffu, my_e, j);
+    pos += (int)((j < k) & (ej < my_e));
+  }
+  const float ex = lane < k ? expf(my_v - m) : 0.f;
+  float z = 0.f;
+  for (int q = 0; q < k; ++q) {
+    const unsigned src = __ballot_sync(0xffffffffu, lane < k && pos == q);
+    z += __shfl_sync(0xffffffffu, ex, __ffs(src) - 1);
+  }
+  if (lane < k) {
+    a.topk_idx[t * k + pos] = my_e;
+    a.topk_w[t * k + pos] = ex / z;
+    atomicOr(&p.bitmap[(size_t)my_e * p.words + (t >> 5)], 1u << (t & 31));
   }
 }
 
