@@ -302,13 +302,16 @@ void oracle_to_bf16(int64_t n, const double* v, uint16_t* out) {
  *     ascending (least recently used first);
  *   - afterwards every selected expert's slot gets stamp n.
  * init_full != 0 starts with slot e holding expert e (needs S >= E);
- * otherwise the pool starts empty.
+ * otherwise the pool starts empty.  seed[0 .. n_seed) (a hot-expert
+ * profile, distinct experts, n_seed <= S) then start resident: seed[i] in
+ * slot i, last used before the first step (stamp 0).
  * miss_out receives (step, expert, slot) triples.  Returns the number of
  * misses, or -1 if a step selects more distinct experts than the pool can
- * hold, or -2 if miss_out is too small.
+ * hold, -2 if miss_out is too small, -3 for an invalid seed.
  */
-int64_t oracle_pool_sim(int64_t E, int64_t S, int init_full, int64_t n_steps, const int32_t* sel,
-                        int64_t maxsel, int32_t* miss_out, int64_t max_miss, int32_t* final_table) {
+int64_t oracle_pool_sim(int64_t E, int64_t S, int init_full, const int32_t* seed, int64_t n_seed, int64_t n_steps,
+                        const int32_t* sel, int64_t maxsel, int32_t* miss_out, int64_t max_miss,
+                        int32_t* final_table) {
   int32_t* table = (int32_t*)malloc((size_t)E * sizeof(int32_t));
   int32_t* owner = (int32_t*)malloc((size_t)S * sizeof(int32_t));
   int64_t* stamp = (int64_t*)calloc((size_t)S, sizeof(int64_t));
@@ -319,6 +322,15 @@ int64_t oracle_pool_sim(int64_t E, int64_t S, int init_full, int64_t n_steps, co
   for (int64_t s = 0; s < S; ++s) owner[s] = -1;
   if (init_full)
     for (int64_t e = 0; e < E && e < S; ++e) { table[e] = (int32_t)e; owner[e] = (int32_t)e; }
+  /* seeding from a hot-expert profile: seed[i] starts resident in slot i,
+     last used before the first step (stamp 0) */
+  if (n_seed > S) rc = -3;
+  for (int64_t i = 0; i < n_seed && rc == 0; ++i) {
+    const int32_t e = seed[i];
+    if (e < 0 || e >= E || table[e] >= 0 || owner[i] >= 0) { rc = -3; break; }
+    table[e] = (int32_t)i;
+    owner[i] = e;
+  }
   for (int64_t n = 0; n < n_steps && rc == 0; ++n) {
     memset(used, 0, (size_t)E);
     int64_t distinct = 0;

@@ -24,7 +24,7 @@ def lib():
         _lib.oracle_rmsnorm.argtypes = [i64, p, C.c_double, p, p]
         _lib.oracle_residual.argtypes = [i64, p, p, p]
         _lib.oracle_to_bf16.argtypes = [i64, p, p]
-        _lib.oracle_pool_sim.argtypes = [i64, i64, C.c_int, i64, p, i64, p, i64, p]
+        _lib.oracle_pool_sim.argtypes = [i64, i64, C.c_int, p, i64, i64, p, i64, p, i64, p]
         _lib.oracle_pool_sim.restype = i64
     return _lib
 
@@ -125,8 +125,11 @@ def to_bf16(v):
     return out
 
 
-def pool_sim(E, S, steps, init_full=False, max_miss=None):
-    """Replay a list of per-step expert selections; returns (misses [n,3] (step, e, slot), table [E])."""
+def pool_sim(E, S, steps, init_full=False, max_miss=None, seed=None):
+    """Replay a list of per-step expert selections; returns (misses [n,3] (step, e, slot), table [E]).
+    seed: experts resident before the first step, seed[i] in slot i, last used
+    before any step (Betelgeuse news page, section 机制, hot-expert profile
+    seeding of the slot pool)."""
     maxsel = max([len(s) for s in steps] + [1])
     sel = np.full((len(steps), maxsel), -1, np.int32)
     for n, s in enumerate(steps):
@@ -135,8 +138,9 @@ def pool_sim(E, S, steps, init_full=False, max_miss=None):
         max_miss = len(steps) * maxsel + 1
     out = np.empty((max_miss, 3), np.int32)
     table = np.empty(E, np.int32)
-    n = lib().oracle_pool_sim(E, S, int(init_full), len(steps), _ptr(sel), maxsel, _ptr(out), max_miss,
-                              _ptr(table))
+    sd = np.asarray([] if seed is None else seed, np.int32)
+    n = lib().oracle_pool_sim(E, S, int(init_full), _ptr(sd) if len(sd) else None, len(sd), len(steps), _ptr(sel),
+                              maxsel, _ptr(out), max_miss, _ptr(table))
     if n < 0:
         raise ValueError(f"pool simulation failed ({n})")
     return out[:n].copy(), table

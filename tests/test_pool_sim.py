@@ -63,3 +63,29 @@ def test_invariants_on_random_traces(seed):
         seen |= set(sel)
     assert it == len(misses)
     assert all(table[e] == resident.get(e, -1) for e in range(E))
+
+
+def test_hand_worked_seeded_trace():
+    g = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "lru_seeded_trace.json")))
+    misses, table = oracle.pool_sim(g["E"], g["S"], g["steps"], seed=g["seed"])
+    assert misses.tolist() == g["misses"]
+    assert table.tolist() == g["final_table"]
+
+
+def test_seeding_the_experts_a_step_needs_removes_its_misses():
+    rng = np.random.default_rng(3)
+    E, S = 40, 12
+    steps = [sorted(rng.choice(E, size=6, replace=False).tolist()) for _ in range(30)]
+    cold, _ = oracle.pool_sim(E, S, steps)
+    warm, _ = oracle.pool_sim(E, S, steps, seed=steps[0])
+    assert not any(m[0] == 1 for m in warm)  # the first step only hits
+    assert len(warm) <= len(cold)
+    # seeding every expert of a full-size pool is init_full with another order
+    none, _ = oracle.pool_sim(E, E, steps, seed=list(range(E))[::-1])
+    assert len(none) == 0
+
+
+def test_invalid_seeds_are_rejected():
+    for seed in ([0, 0], [7], [0, 1, 2, 3]):
+        with pytest.raises(ValueError):
+            oracle.pool_sim(6, 3, [[0]], seed=seed)
