@@ -137,6 +137,20 @@ MOE_API moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t*
 MOE_API moe_status_t moe_slot_pool_configure(moe_layer_t* layer, int32_t n_slots, void* arena_dev, size_t arena_bytes);
 
 /*
+ * Seed a configured pool from a hot-expert profile (Betelgeuse news page,
+ * section 机制: the pool starts from a profile of hot experts instead of
+ * cold).  Replaces the pool's contents: experts_host[i] (host int32,
+ * distinct, 0 <= e < E) is copied now, synchronously, into slot i, last used
+ * before the next call; slots n .. n_slots-1 are empty.  Eviction then
+ * proceeds as described above.  Synchronizes the device.
+ * Errors: INVALID_ARG (NULL layer, experts NULL with n > 0, n < 0 or
+ * n > n_slots, an expert out of range or repeated), STATE (no pool: the
+ * layer is unconfigured or every expert is resident; or the layer holds an
+ * error), CUDA.
+ */
+MOE_API moe_status_t moe_slot_pool_seed(moe_layer_t* layer, const int32_t* experts_host, int32_t n);
+
+/*
  * y = MoE(x) for T tokens, enqueued on `cuda_stream` (a cudaStream_t; NULL =
  * the legacy default stream).  Stream-ordered and asynchronous; safe to
  * capture in a CUDA graph once the pool is configured.

@@ -545,6 +545,27 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   return MOE_OK;
 }
 
+// The pool tables of both paths from a slot map (slot_of [E], owner [E], the
+// first n_slots used), every stamp 0 (used before the next step) and every
+// ready flag clear.  The device is idle.
+bool write_pool_state(moe_layer* L, const std::vector<int32_t>& slot_of, const std::vector<int32_t>& owner) {
+  const int E = L->d.n_experts, S = L->n_slots;
+  const LayerArgs& a = L->args;
+  std::vector<uint32_t> zeros(E, 0u);
+  // the fused kernel's double-buffered copy: [slot_of E][owner S][stamp S] twice
+  std::vector<int32_t> ps((size_t)2 * (E + 2 * S), 0);
+  for (int h = 0; h < 2; ++h) {
+    int32_t* base = ps.data() + (size_t)h * (E + 2 * S);
+    for (int e = 0; e < E; ++e) base[e] = slot_of[e];
+    for (int q = 0; q < S; ++q) base[E + q] = owner[q];
+  }
+  return cudaMemcpy(L->pool_state, ps.data(), ps.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(a.slot_of, slot_of.data(), 4ull * E, cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(a.owner, owner.data(), 4ull * E, cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(a.stamp, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) == cudaSuccess &&
+         cudaMemcpy(a.ready, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) == cudaSuccess;
+}
+
 moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* arena_dev, size_t arena_bytes) {
   if (!L || !arena_dev) return MOE_ERR_INVALID_ARG;
   const int E = L->d.n_experts;
@@ -568,24 +589,7 @@ moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* aren
   } else {
     for (int e = 0; e < E; ++e) slot_of[e] = -1;
   }
-  std::vector<uint32_t> zeros(E, 0u);
-  // the fused kernel's double-buffered copy: [slot_of E][owner S][stamp S] twice
-  {
-    const int S = n_slots;
-    std::vector<int32_t> ps((size_t)2 * (E + 2 * S), 0);
-    for (int h = 0; h < 2; ++h) {
-      int32_t* base = ps.data() + (size_t)h * (E + 2 * S);
-      for (int e = 0; e < E; ++e) base[e] = slot_of[e];
-      for (int q = 0; q < S; ++q) base[E + q] = owner[q];
-    }
-    if (cudaMemcpy(L->pool_state, ps.data(), ps.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess)
-      return MOE_ERR_CUDA;
-  }
-  if (cudaMemcpy(a.slot_of, slot_of.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemcpy(a.owner, owner.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemcpy(a.stamp, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemcpy(a.ready, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (!write_pool_state(L, slot_of, owner)) return MOE_ERR_CUDA;
   if (a.pool) {
     try {
       register_layer(L);
@@ -594,6 +598,28 @@ moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* aren
     }
   }
   return MOE_OK;
+}
+
+moe_status_t moe_slot_pool_seed(moe_layer_t* L, const int32_t* experts, int32_t n) {
+  if (!L || n < 0 || (n > 0 && !experts)) return MOE_ERR_INVALID_ARG;
+  if (L->n_slots == 0 || !L->args.pool) return MOE_ERR_STATE;
+  if (n > L->n_slots) return MOE_ERR_INVALID_ARG;
+  if (sticky_error(L)) return MOE_ERR_STATE;
+  const int E = L->d.n_experts;
+  std::vector<int32_t> slot_of(E, -1), owner(E, -1);
+  for (int i = 0; i < n; ++i) {
+    const int e = experts[i];
+    if (e < 0 || e >= E || slot_of[e] >= 0) return MOE_ERR_INVALID_ARG;
+    slot_of[e] = i;
+    owner[i] = e;
+  }
+  DeviceGuard guard(L->d.device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;  // no call in flight sees the change
+  for (int i = 0; i < n; ++i)
+    if (cudaMemcpy(L->arena + (int64_t)i * L->blob, L->master + (int64_t)experts[i] * L->blob, (size_t)L->blob,
+                   cudaMemcpyHostToDevice) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  return write_pool_state(L, slot_of, owner) ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status_t moe_forward(moe_layer_t* L, const void* x, int32_t T, void* y, int32_t* topk_idx, float* topk_w,

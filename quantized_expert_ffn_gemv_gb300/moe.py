@@ -18,7 +18,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_expert_bytes", "moe_repack_expert", "moe_unpack_expert", "moe_layer_create",
            "moe_slot_pool_configure", "moe_forward", "moe_residual_rmsnorm", "moe_get_stats", "moe_get_miss_log",
            "moe_set_wait_timeout_ns", "moe_debug_copy_faults", "moe_destroy", "moe_status_string",
-           "moe_route_noalloc", "moe_set_miss_service"]
+           "moe_route_noalloc", "moe_set_miss_service", "moe_slot_pool_seed"]
 
 
 class MoeError(RuntimeError):
@@ -59,6 +59,7 @@ def lib(build_if_missing=False):
             getattr(L, f).argtypes = [p, i32, i32, p]
         L.moe_layer_create.argtypes = [C.POINTER(LayerDesc), C.POINTER(p)]
         L.moe_slot_pool_configure.argtypes = [p, i32, p, C.c_size_t]
+        L.moe_slot_pool_seed.argtypes = [p, p, i32]
         L.moe_forward.argtypes = [p, p, i32, p, p, p, p]
         L.moe_residual_rmsnorm.argtypes = [p, p, i32, i32, C.c_float, p, p, p]
         L.moe_get_stats.argtypes = [p, C.POINTER(Stats)]
@@ -166,6 +167,11 @@ class MoeLayer:
         check(lib().moe_slot_pool_configure(self.h, n_slots, self.arena.data_ptr(), self.arena.numel()),
               "moe_slot_pool_configure")
         self.n_slots = n_slots
+
+    def seed(self, experts):
+        """Start the configured pool with these experts resident (expert i of the list in slot i)."""
+        e = np.ascontiguousarray(np.asarray(experts, dtype=np.int32))
+        check(lib().moe_slot_pool_seed(self.h, e.ctypes.data if len(e) else None, len(e)), "moe_slot_pool_seed")
 
     def forward(self, x, y=None, topk_idx=None, topk_w=None, stream=None):
         """x: torch bf16 [T, H] on the layer's device; returns y (bf16 [T, H])."""

@@ -15,12 +15,21 @@ from . import moe
 
 
 class MoeStack:
-    def __init__(self, layers, max_tokens=1, n_slots=None, eps=1e-6, device=0):
-        """layers: synth.Layer objects (router, bias, canonical blobs)."""
+    def __init__(self, layers, max_tokens=1, n_slots=None, eps=1e-6, device=0, seeds=None):
+        """layers: synth.Layer objects (router, bias, canonical blobs).
+        n_slots: one slot budget for every layer, or one per layer (the
+        Betelgeuse news page's 显存 row gives early layers more slots than
+        late ones); None = every expert resident.  seeds: per layer, the
+        experts a pool starts with (a hot-expert profile), or None."""
         import torch
         self.eps = eps
+        budgets = n_slots if isinstance(n_slots, (list, tuple)) else [n_slots] * len(layers)
+        if len(budgets) != len(layers):
+            raise ValueError("one slot budget per layer")
         self.layers = [moe.MoeLayer(L.shape, L.W_r, L.bias, L.experts, L.shared, max_tokens=max_tokens,
-                                    n_slots=n_slots, device=device) for L in layers]
+                                    n_slots=b, device=device) for L, b in zip(layers, budgets)]
+        if seeds is not None:
+            self.seed(seeds)
         self.H = layers[0].shape.H
         self.k = layers[0].shape.k
         self.device = torch.device("cuda", device)
@@ -54,6 +63,14 @@ class MoeStack:
             moe.residual_rmsnorm(bufs["x"][cur], y, self.eps, bufs["x"][nxt], bufs["xhat"], stream)
             cur = nxt
         return bufs["x"][cur]
+
+    def seed(self, seeds):
+        """Start every pooled layer's pool from its list of hot experts."""
+        if len(seeds) != len(self.layers):
+            raise ValueError("one seed list per layer")
+        for l, sd in zip(self.layers, seeds):
+            if sd is not None and l.n_slots < l.shape.E:
+                l.seed(list(sd)[:l.n_slots])
 
     def set_miss_service(self, mode):
         """Miss service of every layer's pool (see MoeLayer.set_miss_service)."""

@@ -68,3 +68,46 @@ def test_stalled_copy_server_times_out(small):
     assert code == 6 and stats["error"] == 6 and stats["wait_ns"] >= 150_000_000
     pool.debug_copy_faults(pause=False)
     pool.close()
+
+
+@pytest.mark.parametrize("service", [0, 1], ids=["copy_engine", "sm_pull"])
+def test_seeded_pool_matches_lru_with_the_same_seed(small, service):
+    """A pool seeded from a hot-expert profile: misses equal the simulator
+    started from the same seed, output bit-identical to all-resident."""
+    T, S = 1, 16
+    x, _ = resampled_tokens(small, 900, 48)
+    full = make_gpu_layer(small, max_tokens=T)
+    y0, i0, w0 = run(full, x, T=T)
+    # a profile: the experts the first 16 tokens select most often
+    counts = np.bincount(i0[:16].ravel(), minlength=small.shape.E)
+    seed = np.argsort(-counts, kind="stable")[:12].astype(np.int32)
+    pool = make_gpu_layer(small, max_tokens=T, n_slots=S)
+    pool.set_miss_service(service)
+    pool.seed(seed)
+    y1, i1, w1 = run(pool, x, T=T)
+    assert np.array_equal(y0, y1) and np.array_equal(i0, i1) and np.array_equal(w0, w1)
+    steps = [sorted(set(i1[t].tolist())) for t in range(48)]
+    expect, _ = oracle.pool_sim(small.shape.E, S, steps, seed=seed.tolist())
+    cold, _ = oracle.pool_sim(small.shape.E, S, steps)
+    assert np.array_equal(pool.miss_log(), expect)
+    assert len(expect) < len(cold)
+    stats, code = pool.stats()
+    assert code == 0 and stats["misses"] == len(expect)
+    pool.close()
+    full.close()
+
+
+def test_seeding_errors(small):
+    from quantized_expert_ffn_gemv_gb300 import moe
+    full = make_gpu_layer(small, max_tokens=1)
+    with pytest.raises(moe.MoeError) as ei:
+        full.seed([0, 1])
+    assert ei.value.code == 7  # every expert resident: no pool to seed
+    pool = make_gpu_layer(small, max_tokens=1, n_slots=8)
+    for bad in ([0, 0], [small.shape.E], list(range(9))):
+        with pytest.raises(moe.MoeError) as ei:
+            pool.seed(bad)
+        assert ei.value.code == 1
+    pool.seed([])  # an empty seed is the empty pool
+    full.close()
+    pool.close()

@@ -101,3 +101,29 @@ def test_layers_match_oracle_teacher_forced(stack_runs):
             assert np.abs(err).max() <= MAX_ABS
             x_l = oracle.residual(x_l, r["ys"][t, l])
         assert np.array_equal(x_l, r["x_out"][t, 0])
+
+
+def test_per_layer_budgets_and_seeds():
+    """Slot budgets that differ by layer (more early, fewer late) and pools
+    seeded from the hottest experts of a profiling run: bit-identical to the
+    all-resident stack, each layer's misses equal to its simulator."""
+    from quantized_expert_ffn_gemv_gb300.stack import MoeStack
+    layers = [synth.make_layer(synth.PAGE, layer=l) for l in range(3)]
+    x = synth.activations(synth.PAGE, 300, 0, 16)
+    full = MoeStack(layers)
+    r_full = run_stack(full, x)
+    full.close()
+    budgets = [240, 92, 60]
+    seeds = []
+    for l in range(3):
+        counts = np.bincount(r_full["idx"][:8, l].ravel(), minlength=synth.PAGE.E)
+        seeds.append(np.argsort(-counts, kind="stable")[:budgets[l]].tolist())
+    pool = MoeStack(layers, n_slots=budgets, seeds=seeds)
+    r_pool = run_stack(pool, x)
+    for key in ("xhats", "ys", "idx", "w", "x_out"):
+        assert np.array_equal(r_full[key], r_pool[key]), key
+    for l, layer in enumerate(pool.layers):
+        steps = [sorted(r_pool["idx"][t, l].tolist()) for t in range(16)]
+        expect, _ = oracle.pool_sim(synth.PAGE.E, budgets[l], steps, seed=seeds[l][:budgets[l]])
+        assert np.array_equal(layer.miss_log(), expect), l
+    pool.close()
