@@ -257,9 +257,16 @@ def run_stack(args):
         return (sum(s["misses"] for s, _ in ss), sum(s["h2d_bytes"] for s, _ in ss), [c for _, c in ss],
                 sum(s["wait_ns"] for s, _ in ss))
 
-    def run(n_slots, service=0):
+    def configure(n_slots, seeds):
+        budgets = n_slots if isinstance(n_slots, list) else [n_slots] * n_layers
+        for l, layer in enumerate(st.layers):
+            layer.configure(budgets[l])
+            if seeds is not None and budgets[l] < synth.PAGE.E:
+                layer.seed(seeds[l][:budgets[l]])
+
+    def run(n_slots, service=0, seeds=None):
+        configure(n_slots, seeds)
         for l in st.layers:
-            l.configure(n_slots)
             l.set_miss_service(service)
         outs = torch.empty((ntok, synth.PAGE.H), dtype=torch.bfloat16, device="cuda")
         with torch.cuda.stream(stream):
@@ -269,8 +276,7 @@ def run_stack(args):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             o = st.forward(xin, bufs, stream)
-        for l in st.layers:  # start every pool empty again
-            l.configure(n_slots)
+        configure(n_slots, seeds)  # start every pool as it was again
         with torch.cuda.stream(stream):
             for t in range(warm):
                 xin.copy_(x_pin[t:t + 1], non_blocking=True)
@@ -299,6 +305,29 @@ def run_stack(args):
                  "h2d_gbs": h2d_pull / (ms_pull * 1e-3) / 1e9,
                  "bit_identical_vs_resident": bool(torch.equal(out_pull.view(torch.int16),
                                                                out_res.view(torch.int16)))}
+    # per-layer budgets (early layers more, late fewer) and pools seeded from
+    # a profile: each layer's most-selected experts over the warm-up tokens of
+    # a resident profiling pass
+    tiers = [240 if 3 * l < n_layers else (92 if 3 * l < 2 * n_layers else 60) for l in range(n_layers)]
+    configure(synth.PAGE.E, None)
+    prof = st.buffers(1, record=True)
+    with torch.cuda.stream(stream):
+        counts = torch.zeros((n_layers, synth.PAGE.E), dtype=torch.int64, device="cuda")
+        for t in range(warm):
+            xin.copy_(x_pin[t:t + 1], non_blocking=True)
+            st.forward(xin, prof, stream)
+            counts.scatter_add_(1, prof["idx"].reshape(n_layers, -1).long(),
+                                torch.ones((n_layers, synth.PAGE.k), dtype=torch.int64, device="cuda"))
+    torch.cuda.synchronize()
+    seeds = [np.argsort(-c, kind="stable").astype(np.int32).tolist() for c in counts.cpu().numpy()]
+    ms_ts, out_ts, misses_ts, h2d_ts, codes_ts, _ = run(tiers, service=1, seeds=seeds)
+    tiered_line = {"tokens_per_s": meas / (ms_ts * 1e-3), "misses": misses_ts, "status": codes_ts,
+                   "slots": f"{tiers[0]}/{tiers[n_layers // 2]}/{tiers[-1]} by thirds of the stack "
+                            f"({sum(tiers)} in all, uniform {slots * n_layers})",
+                   "seed": "each layer's most-selected experts over the warm-up tokens, resident profiling pass",
+                   "service": "sm_pull",
+                   "bit_identical_vs_resident": bool(torch.equal(out_ts.view(torch.int16),
+                                                                 out_res.view(torch.int16)))}
     ms_pool, out_pool, misses, h2d_bytes, codes, wait_ns = run(slots, service=0)
     identical = bool(torch.equal(out_pool.view(torch.int16), out_res.view(torch.int16)))
     peak_small = h2d_peak_gbs(torch, synth.PAGE.expert_bytes, 256)
@@ -322,6 +351,7 @@ def run_stack(args):
                  "h2d_frac_of_expert_copy_peak": h2d_gbs / peak_small,
                  "kernel_wait_us_per_miss": wait_ns / 1e3 / max(1, misses), "status": codes},
         "pool_sm_pull": pull_line,
+        "pool_sm_pull_tiered_seeded": tiered_line,
         "resident": {"tokens_per_s": res_tps, "status": codes_res, "roofline": {
             "bound": "hbm", "achieved": step_bytes * res_tps / 1e9, "peak": hbm_peak, "unit": "GB/s",
             "frac": step_bytes * res_tps / 1e9 / hbm_peak, "peak_kind": peak_kind, "bytes_per_token": step_bytes}},
