@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 from quantized_expert_ffn_gemv_gb300 import synth
-from tests.gpu_common import check_against_oracle, make_gpu_layer, run
+from tests.gpu_common import check_against_oracle, make_gpu_layer, run, to_torch_bf16
 from tests.inputs import resampled_tokens
 
 pytestmark = pytest.mark.gpu
@@ -110,4 +110,23 @@ def test_seeding_errors(small):
         assert ei.value.code == 1
     pool.seed([])  # an empty seed is the empty pool
     full.close()
+    pool.close()
+
+
+def test_pool_serves_up_to_eight_tokens_and_refuses_more(small):
+    """A pooled layer runs the fused path (T <= 8); a larger call is
+    MOE_ERR_UNSUPPORTED before any launch, and the layer stays usable."""
+    import torch
+    from quantized_expert_ffn_gemv_gb300 import moe
+    x, _ = resampled_tokens(small, 950, 9)
+    pool = make_gpu_layer(small, max_tokens=9, n_slots=36)  # 36 >= 9 tokens x top-4
+    xd = to_torch_bf16(x)
+    yd = torch.empty_like(xd)
+    with pytest.raises(moe.MoeError) as ei:
+        pool.forward(xd, yd)
+    assert ei.value.code == 2
+    y, idx, w = run(pool, x[:8], T=8)
+    check_against_oracle(small, x[:8], y, idx, w)
+    stats, code = pool.stats()
+    assert code == 0 and stats["forwards"] == 1
     pool.close()
