@@ -132,7 +132,9 @@ MOE_API moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t*
  *    not use, least recently used first (ties to the lower slot).
  * Errors: INVALID_ARG (NULL arena, n_slots out of range), OUT_OF_MEMORY
  * when n_slots * moe_expert_bytes() > arena_bytes (the request is never
- * shrunk), CUDA.
+ * shrunk), CUDA.  After a CUDA or OUT_OF_MEMORY failure past the argument
+ * checks the layer is unconfigured (moe_forward answers STATE) until a
+ * configure succeeds.
  */
 MOE_API moe_status_t moe_slot_pool_configure(moe_layer_t* layer, int32_t n_slots, void* arena_dev, size_t arena_bytes);
 
@@ -146,7 +148,8 @@ MOE_API moe_status_t moe_slot_pool_configure(moe_layer_t* layer, int32_t n_slots
  * Errors: INVALID_ARG (NULL layer, experts NULL with n > 0, n < 0 or
  * n > n_slots, an expert out of range or repeated), STATE (no pool: the
  * layer is unconfigured or every expert is resident; or the layer holds an
- * error), CUDA.
+ * error), CUDA (the pool is then empty: it is emptied before any slot is
+ * overwritten).
  */
 MOE_API moe_status_t moe_slot_pool_seed(moe_layer_t* layer, const int32_t* experts_host, int32_t n);
 

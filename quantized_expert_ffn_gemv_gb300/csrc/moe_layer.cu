@@ -582,19 +582,28 @@ moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* aren
   a.arena = L->arena;
   a.n_slots = n_slots;
   a.pool = n_slots < E;
+  // a configure that fails part-way leaves the layer unconfigured (forward
+  // answers MOE_ERR_STATE), never half-filled slots behind a valid table
+  auto unconfigured = [&](moe_status_t code) {
+    L->n_slots = 0;
+    a.n_slots = 0;
+    a.pool = 0;
+    return code;
+  };
   std::vector<int32_t> slot_of(E), owner(E, -1);
   if (!a.pool) {
-    if (cudaMemcpy(L->arena, L->master, (size_t)L->blob * E, cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(L->arena, L->master, (size_t)L->blob * E, cudaMemcpyHostToDevice) != cudaSuccess)
+      return unconfigured(MOE_ERR_CUDA);
     for (int e = 0; e < E; ++e) slot_of[e] = owner[e] = e;
   } else {
     for (int e = 0; e < E; ++e) slot_of[e] = -1;
   }
-  if (!write_pool_state(L, slot_of, owner)) return MOE_ERR_CUDA;
+  if (!write_pool_state(L, slot_of, owner)) return unconfigured(MOE_ERR_CUDA);
   if (a.pool) {
     try {
       register_layer(L);
     } catch (...) {
-      return MOE_ERR_OUT_OF_MEMORY;
+      return unconfigured(MOE_ERR_OUT_OF_MEMORY);
     }
   }
   return MOE_OK;
@@ -615,6 +624,11 @@ moe_status_t moe_slot_pool_seed(moe_layer_t* L, const int32_t* experts, int32_t 
   }
   DeviceGuard guard(L->d.device);
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;  // no call in flight sees the change
+  // the pool is marked empty before any slot is overwritten: a copy that
+  // fails part-way leaves an empty (consistent) pool, never a table that
+  // names an expert whose bytes are no longer in its slot
+  const std::vector<int32_t> none(E, -1);
+  if (!write_pool_state(L, none, none)) return MOE_ERR_CUDA;
   for (int i = 0; i < n; ++i)
     if (cudaMemcpy(L->arena + (int64_t)i * L->blob, L->master + (int64_t)experts[i] * L->blob, (size_t)L->blob,
                    cudaMemcpyHostToDevice) != cudaSuccess)
