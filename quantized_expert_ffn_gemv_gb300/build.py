@@ -72,15 +72,20 @@ def build_cuda(force=False, verbose=False):
             sys.stderr.write(r.stderr)
         return obj
 
-    with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
-        objs = list(ex.map(compile_one, srcs))
+    objs = [os.path.join(OUT, os.path.basename(src) + f".{os.getpid()}.o") for src in srcs]
     tmp = CUDA_LIB + f".tmp{os.getpid()}"
-    r = subprocess.run([NVCC] + ARCH + ["-shared", "-o", tmp] + objs + ["-lpthread"], capture_output=True, text=True)
-    for o in objs:
-        os.remove(o)
-    if r.returncode != 0:
-        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, CUDA_LIB)
+    try:
+        with ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 1))) as ex:
+            list(ex.map(compile_one, srcs))
+        r = subprocess.run([NVCC] + ARCH + ["-shared", "-o", tmp] + objs + ["-lpthread"], capture_output=True,
+                           text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, CUDA_LIB)
+    finally:  # no objects or partial library left behind, whether the build worked or not
+        for f in objs + [tmp]:
+            if os.path.exists(f):
+                os.remove(f)
     return CUDA_LIB
 
 
