@@ -514,7 +514,7 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.topk_w = (float*)(b + o_tkw);
   a.wait_timeout_ns = L->wait_timeout_ns;
   a.master = (const uint8_t*)master_dev;
-  a.pull = 0;  // misses copied by the host copy server (moe_set_miss_service)
+  a.pull = 1;  // misses read by the kernel from the mapped master copy (moe_set_miss_service)
   L->tagged_logits = (unsigned long long*)(b + o_bar);
   a.counters = (uint32_t*)(b + o_cnt);
   a.cnt_stride = Um + 2;

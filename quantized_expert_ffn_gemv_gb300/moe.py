@@ -199,7 +199,7 @@ class MoeLayer:
         check(lib().moe_set_wait_timeout_ns(self.h, ns), "moe_set_wait_timeout_ns")
 
     def set_miss_service(self, mode):
-        """0 = host copy engine behind the doorbell (default), 1 = the kernel reads misses from host memory."""
+        """1 = the kernel reads misses from host memory (default), 0 = host copy engine behind the doorbell."""
         check(lib().moe_set_miss_service(self.h, int(mode)), "moe_set_miss_service")
 
     def debug_copy_faults(self, fail_copy_n=0, pause=False):

@@ -46,24 +46,24 @@ def stack_runs():
     logs = [l.miss_log() for l in pool.layers]
     stats = pool.stats()
     pool.close()
-    pull = MoeStack(layers, n_slots=SLOTS)
-    pull.set_miss_service(1)
-    r_pull = run_stack(pull, x)
-    pull_logs = [l.miss_log() for l in pull.layers]
-    pull.close()
-    return layers, x, r_full, r_pool, logs, stats, r_pull, pull_logs
+    copy = MoeStack(layers, n_slots=SLOTS)
+    copy.set_miss_service(0)
+    r_copy = run_stack(copy, x)
+    copy_logs = [l.miss_log() for l in copy.layers]
+    copy.close()
+    return layers, x, r_full, r_pool, logs, stats, r_copy, copy_logs
 
 
 def test_pool_output_bit_identical_to_resident(stack_runs):
-    _, _, r_full, r_pool, _, _, r_pull, _ = stack_runs
+    _, _, r_full, r_pool, _, _, r_copy, _ = stack_runs
     for key in ("xhats", "ys", "idx", "w", "x_out"):
         assert np.array_equal(r_full[key], r_pool[key]), key
-        assert np.array_equal(r_full[key], r_pull[key]), key
+        assert np.array_equal(r_full[key], r_copy[key]), key
 
 
-def test_pulled_misses_equal_copied_misses(stack_runs):
-    *_, logs, _, _, pull_logs = stack_runs
-    for a, b in zip(logs, pull_logs):
+def test_copied_misses_equal_pulled_misses(stack_runs):
+    *_, logs, _, _, copy_logs = stack_runs
+    for a, b in zip(logs, copy_logs):
         assert np.array_equal(a, b)
 
 
