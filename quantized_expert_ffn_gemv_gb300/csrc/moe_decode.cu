@@ -1,5 +1,7 @@
 // Fused decode kernel (T <= 8 tokens per call): the whole MoE layer in one
-// cooperative launch of one CTA per SM, 16 warps.
+// cooperative launch of one CTA per SM, 16 warps.  Consecutive launches are
+// chained by programmatic dependent launch: the prologue below runs before
+// the wait for the previous grid, everything else after it.
 //
 // Weights stream through shared-memory rings filled with 1-D TMA bulk copies
 // (cp.async.bulk + mbarrier); lane 0 of warp 15 is the producer and keeps
@@ -17,12 +19,19 @@
 //              victims (double-buffered pool state; CTA 0 writes the next
 //              state and rings the host doorbell).  Betelgeuse news page,
 //              section 机制, 调度 row: the hit check runs in-stream on the GPU.
+//              One resident token takes an early path: the experts start as
+//              soon as the merge ends and an idle warp finishes the softmax.
+//   misses     by default the consuming warps read a missed expert's strips
+//              from the mapped pinned master copy themselves (and write them
+//              back to its slot); otherwise they wait for the slot's ready
+//              flag, set by the host copy server after its copy.
 //   gate/up    four warps per 16-row strip (K split four ways), one strip per
 //              ring stage at once; h = silu(g) * u goes to global as fp16 and the
 //              expert's completion counter (double-buffered by step parity)
 //              is bumped with a release reduction.
 //   down       warp w handles selected experts w, w + ds, ...: waits for the
-//              expert's counter, z = W_d h for this CTA's 16 output rows;
+//              expert's counter, stages its h rows in shared memory with one
+//              round of cp.async, z = W_d h for this CTA's 16 output rows;
 //              then y = sum_j w_j z_j (ascending expert) + z_shared in fp32,
 //              rounded once to bf16.
 #include <cfloat>

@@ -13,18 +13,23 @@
 //              index), ascending expert order, softmax over the selection;
 //              bit t of the expert's token bitmap
 //   prefix     warp per expert: set bits before each bitmap word
-//   scan       per-expert counts -> pair offsets and 128-token chunks
+//   scan       per-expert counts -> pair offsets, chunk records of up to 256
+//              tokens for the tensor cores, and an expert's last chunk of at
+//              most 16 tokens for the mma.sync path
 //   pairs      thread per (token, rank): its place in the expert's token
 //              list (ascending token: a stable counting sort)
+//   small      the chunks of at most 16 tokens: the chunk's x (or h) rows
+//              staged in shared memory, each 16-row strip's packed weights
+//              read once and applied with mma.sync (gate/up + SiLU, or down)
 //   gate/up    grouped GEMM, M = 128 (64 gate rows and the 64 matching up
-//              rows), N = the chunk's tokens (<= 128, rounded up to 16),
+//              rows), N = the chunk's tokens (<= 256, rounded up to 16),
 //              K = H in steps of 64.  One warp streams the packed 4-bit
-//              tiles into shared memory (bulk copies, four k-steps each);
-//              eight warps dequantize them to fp16 d*q, written with stmatrix
-//              in the 128-byte-swizzled K-major layout, and gather the
-//              chunk's activation rows with cp.async two k-steps ahead; one
-//              thread issues the MMAs into a double-buffered TMEM
-//              accumulator; four epilogue warps compute h = silu(g) * u.
+//              tiles into shared memory (batched bulk copies); eight warps
+//              dequantize them to fp16 d*q, written with stmatrix in the
+//              128-byte-swizzled K-major layout; eight warps gather the
+//              chunk's activation rows with cp.async; one thread issues the
+//              MMAs into a double-buffered TMEM accumulator; eight epilogue
+//              warps compute h = silu(g) * u.
 //   down       the same engine, M = 128 output rows, K = I, B = the pairs'
 //              h rows; the epilogue writes each pair's expert output z as
 //              fp16.
