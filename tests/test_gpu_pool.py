@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 from quantized_expert_ffn_gemv_gb300 import synth
-from tests.gpu_common import check_against_oracle, make_gpu_layer, run, to_torch_bf16
+from tests.gpu_common import check_against_oracle, from_torch_bf16, make_gpu_layer, run, to_torch_bf16
 from tests.inputs import resampled_tokens
 
 pytestmark = pytest.mark.gpu
@@ -129,4 +129,42 @@ def test_pool_serves_up_to_eight_tokens_and_refuses_more(small):
     check_against_oracle(small, x[:8], y, idx, w)
     stats, code = pool.stats()
     assert code == 0 and stats["forwards"] == 1
+    pool.close()
+
+
+@pytest.mark.parametrize("service", [0, 1], ids=["copy_engine", "sm_pull"])
+def test_pool_with_calls_of_mixed_sizes(small, service):
+    """One pooled layer called with 1, 3, 8, 2, 5, ... tokens per call: each
+    call is one step of the LRU simulator (its union of selected experts),
+    outputs bit-identical to the all-resident layer called the same way."""
+    import torch
+    sizes = [1, 3, 8, 2, 5, 1, 7, 4, 8, 6, 1, 2]
+    n = sum(sizes)
+    x, _ = resampled_tokens(small, 1200, n)
+    full = make_gpu_layer(small, max_tokens=8)
+    pool = make_gpu_layer(small, max_tokens=8, n_slots=40)
+    pool.set_miss_service(service)
+    outs = {}
+    for name, layer in (("full", full), ("pool", pool)):
+        xd = to_torch_bf16(x)
+        yd = torch.empty_like(xd)
+        idd = torch.empty((n, small.shape.k), dtype=torch.int32, device="cuda")
+        wd = torch.empty((n, small.shape.k), dtype=torch.float32, device="cuda")
+        t0 = 0
+        for T in sizes:
+            layer.forward(xd[t0:t0 + T], yd[t0:t0 + T], idd[t0:t0 + T], wd[t0:t0 + T])
+            t0 += T
+        torch.cuda.synchronize()
+        outs[name] = (from_torch_bf16(yd), idd.cpu().numpy(), wd.cpu().numpy())
+    for a, b in zip(outs["full"], outs["pool"]):
+        assert np.array_equal(a, b)
+    idx = outs["pool"][1]
+    steps, t0 = [], 0
+    for T in sizes:
+        steps.append(sorted(set(idx[t0:t0 + T].ravel().tolist())))
+        t0 += T
+    expect, _ = oracle.pool_sim(small.shape.E, 40, steps)
+    assert np.array_equal(pool.miss_log(), expect)
+    check_against_oracle(small, x, *outs["pool"], rows=np.arange(0, n, 5))
+    full.close()
     pool.close()
