@@ -97,15 +97,11 @@ struct LayerArgs {
   int64_t blob;
   DevState* st;
   HostMapped* hm;  // device address of the mapped host block
-  int32_t* slot_of;
-  int32_t* owner;
-  uint32_t* stamp;
-  uint32_t* ready;
+  uint32_t* ready;       // [E] per slot: step whose copy has landed (host copy server)
   float* logits;        // [T][E]
   __half* x16;          // [T][H] B-fragment order
   int32_t* u_expert;    // [Umax]
   int32_t* u_slot;      // [Umax]
-  uint32_t* u_wait;     // [Umax] sequence number to wait for (0: resident)
   int32_t* u_off;       // [Umax + 1] pair offsets
   int32_t* pair_token;  // [T*k] pairs sorted by (expert, token)
   float* pair_w;        // [T*k]

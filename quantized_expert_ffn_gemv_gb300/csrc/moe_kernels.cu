@@ -4,9 +4,8 @@
 // dependent launch (griddepcontrol), so each grid is already resident when
 // its predecessor finishes:
 //   route_kernel   router GEMV (fp32, warp pair per expert row), then in the
-//                  last-arriving CTA: top-k per token, softmax weights,
-//                  grouping of (token, expert) pairs by expert, the slot hit
-//                  check with LRU victim choice, and the host doorbell.
+//                  last-arriving CTA: top-k per token, softmax weights and
+//                  grouping of (token, expert) pairs by expert.
 //   gateup_kernel  per (expert, 16-row strip): 4-bit gate and up rows
 //                  dequantized in registers into mma.m16n8k16 fragments,
 //                  fp32 accumulation with exact per-block scaling, then
@@ -14,8 +13,9 @@
 //   down_kernel    per 16-row output strip: every selected expert's down rows,
 //                  then the routing-weighted combine in ascending expert
 //                  order (shared expert last) and one bf16 rounding.
-// Betelgeuse news page, section 机制: 调度 row (the hit check runs in-stream
-// on the GPU; the host is only involved on a miss) and 显存 row (VRAM slots).
+// These kernels serve layers whose experts are all resident (slot = expert);
+// a layer with a slot pool runs the fused decode kernel, which holds the
+// hit check (Betelgeuse news page, section 机制: 调度 and 显存 rows).
 #include <cfloat>
 #include <climits>
 
@@ -30,12 +30,6 @@ namespace {
 
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 __device__ __forceinline__ uint4 ld_cg4(const void* p) {
   uint4 r;
@@ -57,11 +51,6 @@ __device__ __forceinline__ float ld_cg_f32(const float* p) {
   asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(r) : "l"(p));
   return r;
 }
-__device__ __forceinline__ uint32_t ld_acquire_sys(const uint32_t* p) {
-  uint32_t v;
-  asm volatile("ld.acquire.sys.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
 __device__ void set_error(const LayerArgs& a, int code) {
   atomicCAS(&a.st->error, 0, code);
@@ -82,12 +71,12 @@ constexpr int kRouteChunk = 8;       // tokens staged in shared memory at a time
 constexpr int kRouteVec = kMaxHidden / 256;  // float4 per lane per half row
 
 struct FinishSmem {
-  size_t lrow, tokmask, uidx, poff, sidx, sw, taken, misc, total;
+  size_t lrow, tokmask, uidx, poff, sidx, sw, misc, total;
 };
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
-__host__ __device__ inline FinishSmem finish_layout(int E, int S) {
+__host__ __device__ inline FinishSmem finish_layout(int E) {
   FinishSmem f;
   f.lrow = 0;
   f.tokmask = f.lrow + align16(sizeof(float) * 8 * (size_t)E);
@@ -95,8 +84,7 @@ __host__ __device__ inline FinishSmem finish_layout(int E, int S) {
   f.poff = f.uidx + align16(sizeof(int) * (size_t)E);
   f.sidx = f.poff + align16(sizeof(int) * (size_t)E);
   f.sw = f.sidx + align16(sizeof(int) * kMaxTokens * kMaxTopK);
-  f.taken = f.sw + align16(sizeof(float) * kMaxTokens * kMaxTopK);
-  f.misc = f.taken + align16((size_t)S);
+  f.misc = f.sw + align16(sizeof(float) * kMaxTokens * kMaxTopK);
   f.total = f.misc + sizeof(unsigned long long) * 64;
   return f;
 }
@@ -129,17 +117,16 @@ __device__ void block_scan2(int& a, int& b, int& tot_a, int& tot_b, int* scratch
 __device__ void route_finish(const LayerArgs& a, unsigned char* smem) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = a.E, k = a.k, T = a.T;
-  const FinishSmem f = finish_layout(E, a.n_slots);
+  const FinishSmem f = finish_layout(E);
   float* lrow = reinterpret_cast<float*>(smem + f.lrow);
   unsigned long long* tokmask = reinterpret_cast<unsigned long long*>(smem + f.tokmask);
   int* uidx = reinterpret_cast<int*>(smem + f.uidx);
   int* poff = reinterpret_cast<int*>(smem + f.poff);
   int* sidx = reinterpret_cast<int*>(smem + f.sidx);
   float* sw = reinterpret_cast<float*>(smem + f.sw);
-  uint8_t* taken = smem + f.taken;
   unsigned long long* misc = reinterpret_cast<unsigned long long*>(smem + f.misc);
   __shared__ uint32_t s_seq;
-  __shared__ int s_nunion, s_nmiss;
+  __shared__ int s_nunion;
 
   if (tid == 0) {
     a.st->ticket = 0;
@@ -245,87 +232,13 @@ __device__ void route_finish(const LayerArgs& a, unsigned char* smem) {
     a.tk_pos[p] = pos;
   }
 
-  // ---- slot hit check
-  int n_miss = 0;
-  if (!a.pool) {
-    for (int u = tid; u < n_union; u += kRouteThreads) {
-      a.u_slot[u] = a.u_expert[u];
-      a.u_wait[u] = 0u;
-    }
-  } else {
-    for (int s = tid; s < a.n_slots; s += kRouteThreads) taken[s] = 0;
-    for (int u = tid; u < n_union; u += kRouteThreads) {
-      const int e = a.u_expert[u];
-      const int s = a.slot_of[e];
-      a.u_slot[u] = s;
-      a.u_wait[u] = 0u;
-    }
-    __syncthreads();
-    // misses in ascending expert order; the i-th takes the i-th best victim
-    if (tid == 0) s_nmiss = 0;
-    __syncthreads();
-    for (int u0 = 0; u0 < n_union; ++u0) {
-      const int e = a.u_expert[u0];
-      if (a.slot_of[e] >= 0) continue;  // uniform across the block
-      unsigned long long best = ~0ull;
-      for (int s = tid; s < a.n_slots; s += kRouteThreads) {
-        if (taken[s]) continue;
-        const int ow = a.owner[s];
-        if (ow >= 0 && tokmask[ow] != 0ull) continue;  // used by this step
-        unsigned long long key = ((unsigned long long)(ow >= 0) << 44) |
-                                 ((unsigned long long)a.stamp[s] << 12) | (unsigned long long)s;
-        best = key < best ? key : best;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        unsigned long long ob = __shfl_xor_sync(0xffffffffu, best, o);
-        best = ob < best ? ob : best;
-      }
-      if (lane == 0) misc[16 + warp] = best;
-      __syncthreads();
-      if (tid == 0) {
-        unsigned long long b = misc[16];
-        for (int w = 1; w < 8; ++w) b = misc[16 + w] < b ? misc[16 + w] : b;
-        const int s = (int)(b & 0xFFFull);
-        if (b == ~0ull) {
-          // pool smaller than the step's distinct experts (configure forbids
-          // this); keep every address in bounds and fail the step
-          a.u_slot[u0] = 0;
-          set_error(a, MOE_ERR_STATE);
-        } else {
-          const int old = a.owner[s];
-          if (old >= 0) a.slot_of[old] = -1;
-          a.owner[s] = e;
-          a.slot_of[e] = s;
-          taken[s] = 1;
-          a.u_slot[u0] = s;
-          a.u_wait[u0] = seq;
-          const uint32_t slot_i = a.st->ring_head + (uint32_t)s_nmiss;
-          volatile RingEntry* re = &a.hm->ring[slot_i % kRingSize];
-          re->seq = seq;
-          re->expert = e;
-          re->slot = s;
-          s_nmiss = s_nmiss + 1;
-        }
-      }
-      __syncthreads();
-    }
-    n_miss = s_nmiss;
-    for (int u = tid; u < n_union; u += kRouteThreads) a.stamp[a.u_slot[u]] = seq;
-    if (tid == 0 && n_miss > 0) {
-      __threadfence_system();
-      const uint32_t head = a.st->ring_head + (uint32_t)n_miss;
-      a.st->ring_head = head;
-      *reinterpret_cast<volatile uint32_t*>(&a.hm->head) = head;
-      __threadfence_system();
-    }
-  }
+  // ---- every expert resident: slot = expert (pooled layers run the fused path)
+  for (int u = tid; u < n_union; u += kRouteThreads) a.u_slot[u] = a.u_expert[u];
   if (tid == 0) {
     a.st->n_union = n_union;
-    a.st->n_miss = n_miss;
+    a.st->n_miss = 0;
     a.st->forwards += 1ull;
-    a.st->hits += (unsigned long long)(n_union - n_miss);
-    a.st->misses += (unsigned long long)n_miss;
+    a.st->hits += (unsigned long long)n_union;
   }
   __threadfence();
 }
@@ -425,28 +338,6 @@ constexpr int kGuThreads = 128;  // 4 warps split the K = H reduction of a strip
 constexpr int kGuWarpsPerTask = kGuThreads / 32;
 constexpr int kGuBatch = 4;      // super-tiles per warp with loads in flight together
 
-// Waits (one thread, bounded by the layer's timeout) until the slot holds the
-// step's copy.  Returns false when the copy failed, timed out or the layer
-// already carries an error.
-// Called by one thread: waits (bounded by the layer's timeout) until the slot
-// holds this step's copy.  Returns false when the copy failed, timed out or
-// the layer already carries an error.
-__device__ bool wait_slot(const LayerArgs& a, int slot, uint32_t seq, bool count_time) {
-  const uint64_t t0 = global_ns();
-  const uint64_t deadline = t0 + a.wait_timeout_ns;
-  bool ok = true;
-  for (;;) {
-    const uint32_t v = ld_acquire_sys(&a.ready[slot]);
-    if (v == seq) break;
-    if (v == (seq | kReadyError)) { set_error(a, MOE_ERR_COPY); ok = false; break; }
-    if (dev_error(a)) { ok = false; break; }
-    if (global_ns() > deadline) { set_error(a, MOE_ERR_TIMEOUT); ok = false; break; }
-    __nanosleep(200);
-  }
-  if (count_time) atomicAdd(&a.st->wait_ns, (unsigned long long)(global_ns() - t0));
-  return ok;
-}
-
 template <int NG>
 __global__ void __launch_bounds__(kGuThreads) gateup_kernel(LayerArgs a) {
   extern __shared__ __align__(16) float red[];  // [4 warps][NG][32 lanes][8]
@@ -464,23 +355,18 @@ __global__ void __launch_bounds__(kGuThreads) gateup_kernel(LayerArgs a) {
     const bool sh = gu < a.n_shared;
     const uint8_t* base;
     int cnt, poff;
-    uint32_t wseq = 0u;
-    int slot = 0;
     if (sh) {
       base = a.shared;
       cnt = a.T;
       poff = a.T * a.k;
     } else {
       const int u = gu - a.n_shared;
-      slot = ld_cg_i32(&a.u_slot[u]);
-      base = a.arena + (int64_t)slot * a.blob;
+      base = a.arena + (int64_t)ld_cg_i32(&a.u_slot[u]) * a.blob;
       poff = ld_cg_i32(&a.u_off[u]);
       cnt = ld_cg_i32(&a.u_off[u + 1]) - poff;
-      wseq = (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.u_wait[u]));
     }
-    // one thread decides for the block: no error so far, and the slot's
-    // copy (if this step missed the expert) has landed
-    if (tid == 0) s_go = (dev_error(a) == 0) && (wseq == 0u || wait_slot(a, slot, wseq, s == 0));
+    // one thread decides for the block whether the layer still runs
+    if (tid == 0) s_go = dev_error(a) == 0;
     __syncthreads();
     if (!s_go) return;
     const uint8_t* strip = base + (int64_t)s * gu_strip_bytes(H);
@@ -719,7 +605,7 @@ size_t down_smem(int NG, int T) { return sizeof(float) * (kDnWarps * NG * 32 * 4
 
 size_t route_smem_bytes(int H, int E) {
   size_t a = sizeof(float) * (kRouteChunk * (size_t)H + 8 * kRouteChunk);
-  size_t b = finish_layout(E, kMaxExperts).total;
+  size_t b = finish_layout(E).total;
   return a > b ? a : b;
 }
 
@@ -759,10 +645,7 @@ int down_max_blocks_per_sm(int T) {
 
 cudaError_t launch_route(const LayerArgs& a, cudaStream_t s, bool pdl) {
   const int grid = (a.E + kRouteRows - 1) / kRouteRows;
-  size_t smem = route_smem_bytes(a.H, a.E);
-  const size_t fin = finish_layout(a.E, a.n_slots).total;
-  if (fin > smem) smem = fin;
-  return launch(route_kernel, grid, kRouteThreads, smem, s, pdl, a);
+  return launch(route_kernel, grid, kRouteThreads, route_smem_bytes(a.H, a.E), s, pdl, a);
 }
 
 cudaError_t launch_gateup(const LayerArgs& a, cudaStream_t s, bool pdl, int grid) {

@@ -470,10 +470,9 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
     off += align256(bytes);
     return o;
   };
-  const size_t o_st = carve(sizeof(DevState)), o_slot_of = carve(4ull * E), o_owner = carve(4ull * E),
-               o_stamp = carve(4ull * E), o_ready = carve(4ull * E), o_logits = carve(4ull * Tm * E),
+  const size_t o_st = carve(sizeof(DevState)), o_ready = carve(4ull * E), o_logits = carve(4ull * Tm * E),
                o_x16 = carve(2ull * Tb * H), o_uexp = carve(4ull * Um), o_uslot = carve(4ull * Um),
-               o_uwait = carve(4ull * Um), o_uoff = carve(4ull * (Um + 1)), o_ptok = carve(4 * P),
+               o_uoff = carve(4ull * (Um + 1)), o_ptok = carve(4 * P),
                o_pw = carve(4 * P), o_tku = carve(4 * P), o_tkpos = carve(4 * P),
                o_h16 = carve(2ull * (P + Tb) * I), o_tki = carve(4ull * Tm * k), o_tkw = carve(4ull * Tm * k),
                o_bar = carve(8ull * Tb * E), o_cnt = carve(8ull * (Um + 2)), o_pool = carve(4ull * 2 * 3 * E);
@@ -495,15 +494,11 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.blob = L->blob;
   a.st = (DevState*)(b + o_st);
   a.hm = L->hm_dev;
-  a.slot_of = (int32_t*)(b + o_slot_of);
-  a.owner = (int32_t*)(b + o_owner);
-  a.stamp = (uint32_t*)(b + o_stamp);
   a.ready = (uint32_t*)(b + o_ready);
   a.logits = (float*)(b + o_logits);
   a.x16 = (__half*)(b + o_x16);
   a.u_expert = (int32_t*)(b + o_uexp);
   a.u_slot = (int32_t*)(b + o_uslot);
-  a.u_wait = (uint32_t*)(b + o_uwait);
   a.u_off = (int32_t*)(b + o_uoff);
   a.pair_token = (int32_t*)(b + o_ptok);
   a.pair_w = (float*)(b + o_pw);
@@ -545,14 +540,13 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   return MOE_OK;
 }
 
-// The pool tables of both paths from a slot map (slot_of [E], owner [E], the
+// The fused kernel's pool table from a slot map (slot_of [E], owner [E], the
 // first n_slots used), every stamp 0 (used before the next step) and every
 // ready flag clear.  The device is idle.
 bool write_pool_state(moe_layer* L, const std::vector<int32_t>& slot_of, const std::vector<int32_t>& owner) {
   const int E = L->d.n_experts, S = L->n_slots;
-  const LayerArgs& a = L->args;
   std::vector<uint32_t> zeros(E, 0u);
-  // the fused kernel's double-buffered copy: [slot_of E][owner S][stamp S] twice
+  // double-buffered: [slot_of E][owner S][stamp S] twice
   std::vector<int32_t> ps((size_t)2 * (E + 2 * S), 0);
   for (int h = 0; h < 2; ++h) {
     int32_t* base = ps.data() + (size_t)h * (E + 2 * S);
@@ -560,10 +554,7 @@ bool write_pool_state(moe_layer* L, const std::vector<int32_t>& slot_of, const s
     for (int q = 0; q < S; ++q) base[E + q] = owner[q];
   }
   return cudaMemcpy(L->pool_state, ps.data(), ps.size() * 4, cudaMemcpyHostToDevice) == cudaSuccess &&
-         cudaMemcpy(a.slot_of, slot_of.data(), 4ull * E, cudaMemcpyHostToDevice) == cudaSuccess &&
-         cudaMemcpy(a.owner, owner.data(), 4ull * E, cudaMemcpyHostToDevice) == cudaSuccess &&
-         cudaMemcpy(a.stamp, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) == cudaSuccess &&
-         cudaMemcpy(a.ready, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) == cudaSuccess;
+         cudaMemcpy(L->args.ready, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) == cudaSuccess;
 }
 
 moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* arena_dev, size_t arena_bytes) {
