@@ -275,10 +275,11 @@ def run_stack(args):
             if seeds is not None and budgets[l] < synth.PAGE.E:
                 layer.seed(seeds[l][:budgets[l]])
 
-    def run(n_slots, service=1, seeds=None):
+    def run(n_slots, service=1, seeds=None, fused=True):
         configure(n_slots, seeds)
         for l in st.layers:
             l.set_miss_service(service)
+        st.fused = fused
         outs = torch.empty((ntok, synth.PAGE.H), dtype=torch.bfloat16, device="cuda")
         with torch.cuda.stream(stream):
             xin.copy_(x_pin[0:1], non_blocking=True)
@@ -312,6 +313,9 @@ def run_stack(args):
     # host copy engine behind the doorbell (a bounded-wait error there leaves
     # the layers' sticky error set)
     ms_res, out_res, _, _, codes_res, _ = run(synth.PAGE.E)
+    # the same, with the residual + RMSNorm as a kernel of its own between layers
+    ms_split, out_split, _, _, _, _ = run(synth.PAGE.E, fused=False)
+    st.fused = True
     ms_pool, out_pool, misses, h2d_bytes, codes, _ = run(slots, service=1)
     identical = bool(torch.equal(out_pool.view(torch.int16), out_res.view(torch.int16)))
     # per-layer budgets (early layers more, late fewer) and pools seeded from
@@ -366,6 +370,9 @@ def run_stack(args):
                  "h2d_frac_of_expert_copy_peak": h2d_gbs / peak_small, "status": codes},
         "pool_tiered_seeded": tiered_line,
         "pool_copy_engine": copy_line,
+        "resident_norm_kernel_between_layers": {
+            "tokens_per_s": meas / (ms_split * 1e-3),
+            "bit_identical_vs_fused": bool(torch.equal(out_split.view(torch.int16), out_res.view(torch.int16)))},
         "resident": {"tokens_per_s": res_tps, "status": codes_res, "roofline": {
             "bound": "hbm", "achieved": step_bytes * res_tps / 1e9, "peak": hbm_peak, "unit": "GB/s",
             "frac": step_bytes * res_tps / 1e9 / hbm_peak, "peak_kind": peak_kind, "bytes_per_token": step_bytes}},

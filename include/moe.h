@@ -182,6 +182,27 @@ MOE_API moe_status_t moe_forward(moe_layer_t* layer, const void* x_bf16_dev, int
                                  int32_t* topk_idx_dev, float* topk_w_dev, void* cuda_stream);
 
 /*
+ * One layer of a pre-norm stack in one call: residual add and RMSNorm
+ * (as moe_residual_rmsnorm below), then y = MoE(xhat) (as moe_forward):
+ *   x_out = bf16(x + y_prev)                      (y_prev may be NULL: x_out = x)
+ *   xhat  = bf16(x_out / sqrt(mean(x_out^2) + eps))   (no learned weight)
+ *   y     = MoE(xhat)
+ * x, y_prev, x_out, xhat: device bf16 [T][H], 16-byte aligned; x_out may be
+ * NULL (not written); xhat is always written.  y, topk_idx_dev, topk_w_dev as
+ * in moe_forward.  No output may overlap an input or another output.
+ * With T <= 8 the residual and the norm run in the fused kernel's prologue
+ * (every CTA normalises the T rows itself: no launch between layers), with
+ * the same summation order as moe_residual_rmsnorm, so x_out, xhat and y are
+ * bit-identical to moe_residual_rmsnorm followed by moe_forward.  Larger T
+ * launch exactly that pair.
+ * Errors: as moe_forward; INVALID_ARG also for NULL x/xhat, eps < 0 or NaN,
+ * misalignment or overlap.
+ */
+MOE_API moe_status_t moe_forward_norm(moe_layer_t* layer, const void* x_bf16_dev, const void* y_prev_bf16_dev,
+                                      int32_t T, float eps, void* x_out_bf16_dev, void* xhat_bf16_dev,
+                                      void* y_bf16_dev, int32_t* topk_idx_dev, float* topk_w_dev, void* cuda_stream);
+
+/*
  * Residual + RMSNorm between the layers of a stack, enqueued on the stream:
  *   x_out   = bf16(x + y)                 (y may be NULL: x_out = x)
  *   xhat    = bf16(x_out / sqrt(mean(x_out^2) + eps))   (no learned weight)

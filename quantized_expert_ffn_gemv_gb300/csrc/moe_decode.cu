@@ -611,12 +611,64 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint64_t deadline = global_ns() + a.wait_timeout_ns;
   const uint32_t step0 = (tid == 0) ? (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.st->step)) : 0u;
+  __shared__ float s_inv[kMaxT];
+  if (a.resid) {
+    // Fused pre-norm: xs = bf16(resid + y_prev) into xraw, and each token's
+    // sum of squares in residual_rmsnorm_kernel's order (256 threads per
+    // token, thread i over elements i, i + 256, ...; xor-shuffle warp sums;
+    // the 8 warp sums in order), so the result is bit-identical to that
+    // kernel's.
+    float* part = red;  // [kMaxT][8]
+    for (int t0 = 0; t0 < T; t0 += kThreads / 256) {
+      const int t = t0 + tid / 256, vt = tid % 256;
+      float ss = 0.f;
+      if (t < T)
+        for (int i = vt; i < H; i += 256) {
+          float v = __uint_as_float((uint32_t)a.resid[(size_t)t * H + i] << 16);
+          if (a.y_prev) v += __uint_as_float((uint32_t)a.y_prev[(size_t)t * H + i] << 16);
+          const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+          xraw[t * H + i] = b;
+          const float vr = __uint_as_float((uint32_t)b << 16);
+          ss = fmaf(vr, vr, ss);
+        }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0 && t < T) part[t * 8 + vt / 32] = ss;
+    }
+    __syncthreads();
+    if (tid < T) {
+      float tot = 0.f;
+      for (int w = 0; w < 8; ++w) tot += part[tid * 8 + w];
+      s_inv[tid] = 1.0f / sqrtf(tot / (float)H + a.eps);
+    }
+    __syncthreads();
+  }
   // x -> fp16 in B-fragment order (this CTA's own copy)
   {
     int bad = 0;
     for (int o = tid; o < T * H / 8; o += kThreads) {
       const int t = o / (H / 8), k8 = (o % (H / 8)) * 8;
-      const uint4 v = *reinterpret_cast<const uint4*>(a.x + (size_t)t * H + k8);
+      uint4 v;
+      if (a.resid) {
+        // xhat = bf16(xs * inv); this CTA writes its share of xs and xhat out
+        const uint4 xs = *reinterpret_cast<const uint4*>(xraw + t * H + k8);
+        const float inv = s_inv[t];
+        const uint32_t xw[4] = {xs.x, xs.y, xs.z, xs.w};
+        uint32_t hw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(xw[i] << 16) * inv));
+          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(xw[i] & 0xFFFF0000u) * inv));
+          hw[i] = lo | (hi << 16);
+        }
+        v = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        if (o % G == c) {
+          if (a.x_out) *reinterpret_cast<uint4*>(a.x_out + (size_t)t * H + k8) = xs;
+          *reinterpret_cast<uint4*>(a.xhat_out + (size_t)t * H + k8) = v;
+        }
+      } else {
+        v = *reinterpret_cast<const uint4*>(a.x + (size_t)t * H + k8);
+      }
       *reinterpret_cast<uint4*>(xraw + t * H + k8) = v;
       const uint32_t vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll

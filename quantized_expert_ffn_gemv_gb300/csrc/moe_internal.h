@@ -112,6 +112,14 @@ struct LayerArgs {
   float* topk_w;        // [T][k]
   const uint16_t* x;    // bf16 [T][H]
   uint16_t* y;          // bf16 [T][H]
+  // Fused pre-norm (moe_forward_norm, fused decode kernel only): when resid is
+  // set the layer input is xhat = bf16(rmsnorm(bf16(resid + y_prev))), formed
+  // in the kernel's prologue; x is then unused.
+  const uint16_t* resid;   // bf16 [T][H] or null
+  const uint16_t* y_prev;  // bf16 [T][H] or null (no residual branch)
+  uint16_t* x_out;         // bf16 [T][H] or null: bf16(resid + y_prev)
+  uint16_t* xhat_out;      // bf16 [T][H]: the normalised layer input
+  float eps;
   unsigned long long wait_timeout_ns;
   uint32_t* counters;   // [2][cnt_stride] gate/up completion counts, by step parity
   int cnt_stride;       // max distinct experts per call + 2

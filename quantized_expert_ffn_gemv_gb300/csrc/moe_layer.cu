@@ -627,11 +627,29 @@ moe_status_t moe_slot_pool_seed(moe_layer_t* L, const int32_t* experts, int32_t 
   return write_pool_state(L, slot_of, owner) ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status_t moe_forward(moe_layer_t* L, const void* x, int32_t T, void* y, int32_t* topk_idx, float* topk_w,
-                         void* stream) {
-  if (!L || !x || !y) return MOE_ERR_INVALID_ARG;
-  if (T < 1 || T > L->d.max_tokens) return MOE_ERR_INVALID_ARG;
-  if (((uintptr_t)x & 15) || ((uintptr_t)y & 3)) return MOE_ERR_INVALID_ARG;
+namespace {
+
+// The residual + RMSNorm that moe_forward_norm puts in front of the layer.
+struct PreNorm {
+  const void* x;
+  const void* y_prev;
+  float eps;
+  void* x_out;
+  void* xhat;
+};
+
+// [p, p + n) and [q, q + n) share a byte (a null pointer shares none).
+bool overlap(const void* p, const void* q, size_t n) {
+  if (!p || !q) return false;
+  const uintptr_t a = (uintptr_t)p, b = (uintptr_t)q;
+  return a < b + n && b < a + n;
+}
+
+// x is the layer input; with a pre-norm it is the xhat buffer, which the
+// fused kernel writes itself and the other paths get from
+// residual_rmsnorm_kernel first.
+moe_status_t forward_impl(moe_layer_t* L, const void* x, int32_t T, void* y, int32_t* topk_idx, float* topk_w,
+                          void* stream, const PreNorm* pn) {
   if (L->n_slots == 0) return MOE_ERR_STATE;
   if (sticky_error(L)) return MOE_ERR_STATE;
   DeviceGuard guard(L->d.device);
@@ -644,10 +662,20 @@ moe_status_t moe_forward(moe_layer_t* L, const void* x, int32_t T, void* y, int3
   a.wait_timeout_ns = L->wait_timeout_ns;
   cudaStream_t s = (cudaStream_t)stream;
   if (decode_supported(L->d.hidden, L->d.inter, L->d.n_experts, L->d.top_k, T, L->sm_count)) {
+    if (pn) {
+      a.resid = (const uint16_t*)pn->x;
+      a.y_prev = (const uint16_t*)pn->y_prev;
+      a.x_out = (uint16_t*)pn->x_out;
+      a.xhat_out = (uint16_t*)pn->xhat;
+      a.eps = pn->eps;
+    }
     if (launch_decode(a, L->tagged_logits, L->pool_state, L->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
   if (a.pool) return MOE_ERR_UNSUPPORTED;  // the slot pool runs on the fused path only
+  if (pn && launch_residual_rmsnorm((const uint16_t*)pn->x, (const uint16_t*)pn->y_prev, T, L->d.hidden, pn->eps,
+                                    (uint16_t*)pn->x_out, (uint16_t*)pn->xhat, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (T > kMaxTokens) {
     if (!prefill_encode_x(L->encode_map, x, L->d.hidden, T, &L->pf_maps)) return MOE_ERR_CUDA;
     if (launch_prefill(a, L->pf, L->pf_maps, L->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -663,6 +691,31 @@ moe_status_t moe_forward(moe_layer_t* L, const void* x, int32_t T, void* y, int3
   if (launch_gateup(a, s, true, gu_grid) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_down(a, s, true, dn_grid) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+}  // namespace
+
+moe_status_t moe_forward(moe_layer_t* L, const void* x, int32_t T, void* y, int32_t* topk_idx, float* topk_w,
+                         void* stream) {
+  if (!L || !x || !y) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > L->d.max_tokens) return MOE_ERR_INVALID_ARG;
+  if (((uintptr_t)x & 15) || ((uintptr_t)y & 3)) return MOE_ERR_INVALID_ARG;
+  return forward_impl(L, x, T, y, topk_idx, topk_w, stream, nullptr);
+}
+
+moe_status_t moe_forward_norm(moe_layer_t* L, const void* x, const void* y_prev, int32_t T, float eps, void* x_out,
+                              void* xhat, void* y, int32_t* topk_idx, float* topk_w, void* stream) {
+  if (!L || !x || !xhat || !y) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || T > L->d.max_tokens || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
+  if ((((uintptr_t)x | (uintptr_t)y_prev | (uintptr_t)x_out | (uintptr_t)xhat) & 15) || ((uintptr_t)y & 3))
+    return MOE_ERR_INVALID_ARG;
+  const size_t n = (size_t)T * (size_t)L->d.hidden * 2;
+  if (overlap(xhat, x, n) || overlap(xhat, y_prev, n) || overlap(xhat, x_out, n) || overlap(xhat, y, n) ||
+      overlap(x_out, x, n) || overlap(x_out, y_prev, n) || overlap(x_out, y, n) || overlap(y, x, n) ||
+      overlap(y, y_prev, n))
+    return MOE_ERR_INVALID_ARG;
+  const PreNorm pn{x, y_prev, eps, x_out, xhat};
+  return forward_impl(L, xhat, T, y, topk_idx, topk_w, stream, &pn);
 }
 
 moe_status_t moe_residual_rmsnorm(const void* x, const void* y, int32_t T, int32_t hidden, float eps, void* x_out,

@@ -18,7 +18,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_expert_bytes", "moe_repack_expert", "moe_unpack_expert", "moe_layer_create",
            "moe_slot_pool_configure", "moe_forward", "moe_residual_rmsnorm", "moe_get_stats", "moe_get_miss_log",
            "moe_set_wait_timeout_ns", "moe_debug_copy_faults", "moe_destroy", "moe_status_string",
-           "moe_route_noalloc", "moe_set_miss_service", "moe_slot_pool_seed"]
+           "moe_route_noalloc", "moe_set_miss_service", "moe_slot_pool_seed", "moe_forward_norm"]
 
 
 class MoeError(RuntimeError):
@@ -61,6 +61,7 @@ def lib(build_if_missing=False):
         L.moe_slot_pool_configure.argtypes = [p, i32, p, C.c_size_t]
         L.moe_slot_pool_seed.argtypes = [p, p, i32]
         L.moe_forward.argtypes = [p, p, i32, p, p, p, p]
+        L.moe_forward_norm.argtypes = [p, p, p, i32, C.c_float, p, p, p, p, p, p]
         L.moe_residual_rmsnorm.argtypes = [p, p, i32, i32, C.c_float, p, p, p]
         L.moe_get_stats.argtypes = [p, C.POINTER(Stats)]
         L.moe_get_miss_log.argtypes = [p, p, i64, C.POINTER(i64)]
@@ -182,6 +183,16 @@ class MoeLayer:
         check(lib().moe_forward(self.h, x.data_ptr(), T, y.data_ptr(),
                                 None if topk_idx is None else topk_idx.data_ptr(),
                                 None if topk_w is None else topk_w.data_ptr(), _stream_ptr(stream)), "moe_forward")
+        return y
+
+    def forward_norm(self, x, y_prev, eps, x_out, xhat, y, topk_idx=None, topk_w=None, stream=None):
+        """One pre-norm stack layer: x_out = bf16(x + y_prev), xhat = bf16(rmsnorm(x_out)),
+        y = MoE(xhat).  torch bf16 [T, H] tensors on the layer's device; y_prev and
+        x_out may be None."""
+        opt = lambda t: None if t is None else t.data_ptr()
+        check(lib().moe_forward_norm(self.h, x.data_ptr(), opt(y_prev), x.shape[0], eps, opt(x_out),
+                                     xhat.data_ptr(), y.data_ptr(), opt(topk_idx), opt(topk_w),
+                                     _stream_ptr(stream)), "moe_forward_norm")
         return y
 
     def stats(self):

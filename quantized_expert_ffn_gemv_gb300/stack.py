@@ -34,11 +34,13 @@ class MoeStack:
         self.k = layers[0].shape.k
         self.device = torch.device("cuda", device)
 
+    fused = True  # residual + RMSNorm inside each layer's call (moe_forward_norm)
+
     def buffers(self, T, record=False):
         import torch
         n = len(self.layers)
         z = lambda *s, dt=torch.bfloat16: torch.empty(*s, dtype=dt, device=self.device)
-        b = {"x": z(2, T, self.H), "xhat": z(T, self.H), "y": z(T, self.H)}
+        b = {"x": z(2, T, self.H), "xhat": z(T, self.H), "y": z(2, T, self.H)}
         if record:
             b["xhats"] = z(n, T, self.H)
             b["ys"] = z(n, T, self.H)
@@ -47,22 +49,44 @@ class MoeStack:
         return b
 
     def forward(self, x, bufs, stream=None):
-        """x: torch bf16 [T, H] (device).  Returns the output x_L (a view into bufs)."""
+        """x: torch bf16 [T, H] (device).  Returns the output x_L (a view into bufs).
+
+        fused: each layer's call adds the residual and normalises its own input
+        (one kernel per layer for T <= 8); otherwise a residual + RMSNorm
+        kernel runs between the layers.  Both give bit-identical results."""
+        rec = "xhats" in bufs
+        T = x.shape[0]
         cur = 0
-        bufs["x"][0].copy_(x)
-        moe.residual_rmsnorm(bufs["x"][0], None, self.eps, None, bufs["xhat"], stream)
+        bufs["x"][0][:T].copy_(x)
+        if not self.fused:
+            moe.residual_rmsnorm(bufs["x"][0][:T], None, self.eps, None, bufs["xhat"][:T], stream)
+        y_prev = None
         for l, layer in enumerate(self.layers):
-            rec = "xhats" in bufs
-            if rec:
-                bufs["xhats"][l].copy_(bufs["xhat"])
-            y = bufs["ys"][l] if rec else bufs["y"]
-            layer.forward(bufs["xhat"], y, bufs["idx"][l] if rec else None, bufs["w"][l] if rec else None,
-                          stream=stream)
+            y = bufs["ys"][l][:T] if rec else bufs["y"][l % 2][:T]
+            idx = bufs["idx"][l][:T] if rec else None
+            w = bufs["w"][l][:T] if rec else None
             nxt = 1 - cur
-            # x_{l+1} = bf16(x_l + y_l); its RMSNorm feeds the next layer
-            moe.residual_rmsnorm(bufs["x"][cur], y, self.eps, bufs["x"][nxt], bufs["xhat"], stream)
-            cur = nxt
-        return bufs["x"][cur]
+            if self.fused:
+                # x_l = bf16(x_{l-1} + y_{l-1}) (x_0 = x), its RMSNorm, the layer
+                xhat = bufs["xhats"][l][:T] if rec else bufs["xhat"][:T]
+                x_out = None if y_prev is None else bufs["x"][nxt][:T]
+                layer.forward_norm(bufs["x"][cur][:T], y_prev, self.eps, x_out, xhat, y, idx, w, stream=stream)
+                if y_prev is not None:
+                    cur = nxt
+            else:
+                if rec:
+                    bufs["xhats"][l][:T].copy_(bufs["xhat"][:T])
+                layer.forward(bufs["xhat"][:T], y, idx, w, stream=stream)
+                # x_{l+1} = bf16(x_l + y_l); its RMSNorm feeds the next layer
+                moe.residual_rmsnorm(bufs["x"][cur][:T], y, self.eps, bufs["x"][nxt][:T], bufs["xhat"][:T], stream)
+                cur = nxt
+            y_prev = y
+        if self.fused:
+            # x_L = bf16(x_{L-1} + y_{L-1})
+            moe.residual_rmsnorm(bufs["x"][cur][:T], y_prev, self.eps, bufs["x"][1 - cur][:T], bufs["xhat"][:T],
+                                 stream)
+            cur = 1 - cur
+        return bufs["x"][cur][:T]
 
     def seed(self, seeds):
         """Start every pooled layer's pool from its list of hot experts."""

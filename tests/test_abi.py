@@ -61,6 +61,7 @@ def test_create_rejects_bad_descriptions_before_touching_the_gpu(moe):
     d.hidden = 1024
     assert h.value is None
     assert moe.lib().moe_forward(None, None, 1, None, None, None, None) == 1
+    assert moe.lib().moe_forward_norm(None, None, None, 1, 1e-6, None, None, None, None, None, None) == 1
     assert moe.lib().moe_set_miss_service(None, 1) == 1
     assert moe.lib().moe_slot_pool_seed(None, None, 0) == 1
     assert moe.expert_bytes(2048, 512) == 1_769_472

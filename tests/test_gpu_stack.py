@@ -51,24 +51,71 @@ def stack_runs():
     r_copy = run_stack(copy, x)
     copy_logs = [l.miss_log() for l in copy.layers]
     copy.close()
-    return layers, x, r_full, r_pool, logs, stats, r_copy, copy_logs
+    split = MoeStack(layers)
+    split.fused = False
+    r_split = run_stack(split, x)
+    split.close()
+    return layers, x, r_full, r_pool, logs, stats, r_copy, copy_logs, r_split
 
 
 def test_pool_output_bit_identical_to_resident(stack_runs):
-    _, _, r_full, r_pool, _, _, r_copy, _ = stack_runs
+    _, _, r_full, r_pool, _, _, r_copy, _, _ = stack_runs
     for key in ("xhats", "ys", "idx", "w", "x_out"):
         assert np.array_equal(r_full[key], r_pool[key]), key
         assert np.array_equal(r_full[key], r_copy[key]), key
 
 
+def test_fused_prenorm_bit_identical_to_separate_kernel(stack_runs):
+    """Residual + RMSNorm in each layer's kernel gives the same bits as the
+    residual + RMSNorm kernel between the layers."""
+    _, _, r_full, *_, r_split = stack_runs
+    for key in ("xhats", "ys", "idx", "w", "x_out"):
+        assert np.array_equal(r_full[key], r_split[key]), key
+
+
+@pytest.mark.parametrize("T", [1, 3, 8, 16])
+def test_forward_norm_equals_norm_then_forward(T):
+    """moe_forward_norm against moe_residual_rmsnorm + moe_forward on the same
+    inputs, bit for bit: T <= 8 fuses the norm into the decode kernel, T = 16
+    runs the norm kernel and the batched kernels."""
+    import torch
+    from quantized_expert_ffn_gemv_gb300 import moe
+    L = synth.make_layer(synth.PAGE, layer=2)
+    layer = moe.MoeLayer(L.shape, L.W_r, L.bias, L.experts, L.shared, max_tokens=16)
+    sh = synth.PAGE
+    x = to_torch_bf16(synth.activations(sh, 7, 0, T))
+    y_prev = to_torch_bf16(synth.activations(sh, 8, 0, T))
+    z = lambda *s, dt=torch.bfloat16: torch.zeros(*s, dtype=dt, device="cuda")
+    for yp in (None, y_prev):
+        x_out, xhat, y = z(T, sh.H), z(T, sh.H), z(T, sh.H)
+        idx, w = z(T, sh.k, dt=torch.int32), z(T, sh.k, dt=torch.float32)
+        layer.forward_norm(x, yp, 1e-6, x_out, xhat, y, idx, w)
+        x_out2, xhat2, y2 = z(T, sh.H), z(T, sh.H), z(T, sh.H)
+        idx2, w2 = z(T, sh.k, dt=torch.int32), z(T, sh.k, dt=torch.float32)
+        moe.residual_rmsnorm(x, yp, 1e-6, x_out2, xhat2)
+        layer.forward(xhat2, y2, idx2, w2)
+        torch.cuda.synchronize()
+        for a, b in ((x_out, x_out2), (xhat, xhat2), (y, y2)):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert torch.equal(idx, idx2) and torch.equal(w.view(torch.int32), w2.view(torch.int32))
+    # outputs may not overlap inputs or each other
+    with pytest.raises(moe.MoeError) as e:
+        layer.forward_norm(x, y_prev, 1e-6, x_out, x, y)
+    assert e.value.code == 1
+    with pytest.raises(moe.MoeError) as e:
+        layer.forward_norm(x, y_prev, 1e-6, x_out, xhat, y_prev)
+    assert e.value.code == 1
+    layer.close()
+
+
 def test_copied_misses_equal_pulled_misses(stack_runs):
-    *_, logs, _, _, copy_logs = stack_runs
+    *_, logs, _, _, copy_logs, _ = stack_runs
     for a, b in zip(logs, copy_logs):
         assert np.array_equal(a, b)
 
 
 def test_miss_traces_match_lru_simulator(stack_runs):
-    layers, _, _, r_pool, logs, stats, _, _ = stack_runs
+    layers, _, _, r_pool, logs, stats, _, _, _ = stack_runs
     eb = synth.PAGE.expert_bytes
     for l in range(N_LAYERS):
         steps = [sorted(r_pool["idx"][t, l].tolist()) for t in range(N_TOKENS)]
@@ -79,7 +126,7 @@ def test_miss_traces_match_lru_simulator(stack_runs):
 
 
 def test_layers_match_oracle_teacher_forced(stack_runs):
-    layers, x, _, r, _, _, _, _ = stack_runs
+    layers, x, _, r, _, _, _, _, _ = stack_runs
     sh = synth.PAGE
     for t in (0, N_TOKENS // 2, N_TOKENS - 1):
         x_l = x[t]
