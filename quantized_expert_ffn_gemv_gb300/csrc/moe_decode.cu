@@ -789,7 +789,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
           a.h16[(size_t)(tk.poff + col) * I + frag_pos(strip * 16 + rowin)] =
               __float2half_rn(silu(gsum[cc]) * usum[cc]);
       }
-      __threadfence();
+      // the warp's h stores happen before lane 0's release through the warp
+      // barrier (no per-thread fence: the release covers them)
       __syncwarp();
       if (lane == 0) red_release_add(&cnt_cur[xi], 1u);
     }
@@ -1245,6 +1246,7 @@ cudaError_t decode_configure() {
 bool decode_supported(int H, int I, int E, int k, int T, int G) {
   if (T > kMaxT || E > kMaxE || k > kMaxTopK) return false;
   if ((E + G - 1) / G > 8) return false;  // router: two warps per row, 16 warps
+  if (H / 16 > G) return false;            // down: one 16-row output strip per CTA
   return g_decode_smem_limit > 0 && decode_smem_bytes(H, I, E, k, T, G) <= g_decode_smem_limit;
 }
 

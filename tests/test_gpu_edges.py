@@ -102,3 +102,24 @@ def test_degenerate_selections(k, T):
     else:
         assert np.array_equal(w, np.ones((T, 1), np.float32))
     g.close()
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_hidden_wider_than_one_down_strip_per_sm(T):
+    """H = 4,096 has 256 down strips of 16 rows, more than the GPU has SMs:
+    the fused kernel (one strip per CTA) declines and the batched kernels run,
+    every output row against the oracle; a slot pool, which only the fused
+    kernel serves, is refused."""
+    from quantized_expert_ffn_gemv_gb300 import moe
+    sh = synth.LayerShape(H=4096, E=32, k=2, I=128)
+    L = synth.make_layer(sh, layer=60)
+    x, _ = resampled_tokens(L, 900, T)
+    g = make_gpu_layer(L, max_tokens=T)
+    y, idx, w = run(g, x, T=T)
+    check_against_oracle(L, x, y, idx, w)
+    g.close()
+    p = make_gpu_layer(L, max_tokens=T, n_slots=2 * T)
+    with pytest.raises(moe.MoeError) as e:
+        run(p, x, T=T)
+    assert e.value.code == 2
+    p.close()
