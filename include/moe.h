@@ -125,16 +125,20 @@ MOE_API moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t*
  * next configure call, 256-byte aligned).
  *  - n_slots == E: every expert resident.  All blobs are copied into the
  *    arena now (synchronously); no host traffic during moe_forward.
- *  - min(E, max_tokens*k) <= n_slots < E: the pool starts empty; a host
- *    copy-server thread serves misses.  Eviction is LRU over forward calls:
- *    the misses of a call are filled in ascending expert index, taking
- *    empty slots first (ascending), then slots whose expert the call does
- *    not use, least recently used first (ties to the lower slot).
+ *  - min(E, max_tokens*k) <= n_slots < E: the pool starts empty (or as
+ *    moe_slot_pool_seed sets it); misses are served from the pinned host
+ *    master copy (moe_set_miss_service).  Eviction is LRU over forward
+ *    calls: the misses of a call are filled in ascending expert index,
+ *    taking empty slots first (ascending), then slots whose expert the call
+ *    does not use, least recently used first (ties to the lower slot).
  * Errors: INVALID_ARG (NULL arena, n_slots out of range), OUT_OF_MEMORY
  * when n_slots * moe_expert_bytes() > arena_bytes (the request is never
- * shrunk), CUDA.  After a CUDA or OUT_OF_MEMORY failure past the argument
- * checks the layer is unconfigured (moe_forward answers STATE) until a
- * configure succeeds.
+ * shrunk), UNSUPPORTED (n_slots < E on a layer the fused decode kernel does
+ * not take: more than 16 x SMs hidden rows, more than min(1024, 8 x SMs)
+ * experts, or a shared-memory plan that does not fit; the layer keeps its
+ * previous configuration), CUDA.  After a CUDA or OUT_OF_MEMORY failure
+ * past the argument checks the layer is unconfigured (moe_forward answers
+ * STATE) until a configure succeeds.
  */
 MOE_API moe_status_t moe_slot_pool_configure(moe_layer_t* layer, int32_t n_slots, void* arena_dev, size_t arena_bytes);
 
@@ -167,8 +171,9 @@ MOE_API moe_status_t moe_slot_pool_seed(moe_layer_t* layer, const int32_t* exper
  * lower index.  Output: y = sum over the selected experts, in ascending
  * index, of w_j * FFN_j(x), plus FFN_shared(x), accumulated in fp32 and
  * rounded once to bf16 (round to nearest even).
- * Execution by T: T <= 8 one fused kernel (slot pool or all resident);
- * 9..64 three kernels (all resident); 65..max_tokens the prefill path
+ * Execution by T: T <= 8 one fused kernel (slot pool or all resident) when
+ * the layer fits it (see moe_slot_pool_configure), else the three kernels
+ * below; 9..64 three kernels (all resident); 65..max_tokens the prefill path
  * (all resident): grouped GEMMs on the tensor cores with fp16 operands
  * (dequantized weights d*q and activations) and fp32 accumulation
  * (halogen-flash-server README, section "Measured": prefill is compute-bound).

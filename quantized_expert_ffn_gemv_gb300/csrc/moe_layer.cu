@@ -564,6 +564,9 @@ moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* aren
   if (n_slots < need || n_slots > E) return MOE_ERR_INVALID_ARG;
   if (((uintptr_t)arena_dev & 255) != 0) return MOE_ERR_INVALID_ARG;
   if ((size_t)n_slots * (size_t)L->blob > arena_bytes) return MOE_ERR_OUT_OF_MEMORY;
+  // only the fused decode kernel serves a pool
+  if (n_slots < E && !decode_supported(L->d.hidden, L->d.inter, E, L->d.top_k, 1, L->sm_count))
+    return MOE_ERR_UNSUPPORTED;
   DeviceGuard guard(L->d.device);
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
   stop_server(L);

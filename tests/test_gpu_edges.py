@@ -109,7 +109,7 @@ def test_hidden_wider_than_one_down_strip_per_sm(T):
     """H = 4,096 has 256 down strips of 16 rows, more than the GPU has SMs:
     the fused kernel (one strip per CTA) declines and the batched kernels run,
     every output row against the oracle; a slot pool, which only the fused
-    kernel serves, is refused."""
+    kernel serves, is refused when it is configured."""
     from quantized_expert_ffn_gemv_gb300 import moe
     sh = synth.LayerShape(H=4096, E=32, k=2, I=128)
     L = synth.make_layer(sh, layer=60)
@@ -118,8 +118,6 @@ def test_hidden_wider_than_one_down_strip_per_sm(T):
     y, idx, w = run(g, x, T=T)
     check_against_oracle(L, x, y, idx, w)
     g.close()
-    p = make_gpu_layer(L, max_tokens=T, n_slots=2 * T)
     with pytest.raises(moe.MoeError) as e:
-        run(p, x, T=T)
+        make_gpu_layer(L, max_tokens=T, n_slots=2 * T)
     assert e.value.code == 2
-    p.close()
