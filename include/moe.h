@@ -4,9 +4,10 @@
  * One call of moe_forward runs the MoE FFN layer of Qwen3.8-Flash-Next-style
  * decode on one GPU: router GEMV, softmax and top-k selection, an in-stream
  * check of whether each selected expert is resident in a VRAM expert-slot
- * pool (misses copied from pinned host RAM behind a host doorbell, never
- * dropped), 4-bit block-quantized gate/up/down expert GEMVs with SiLU gating,
- * and the routing-weighted combine.
+ * pool (misses served from pinned host RAM after a host doorbell: read by
+ * the kernel itself or copied by a host thread, never dropped), 4-bit
+ * block-quantized gate/up/down expert GEMVs with SiLU gating, and the
+ * routing-weighted combine.
  *
  * Sources for what the layer is and how residency works:
  *  - Betelgeuse news page ("Betelgeuse: RTX 3060 12GB + 16GB 内存跑 Qwen 3.8
@@ -188,7 +189,10 @@ MOE_API moe_status_t moe_forward(moe_layer_t* layer, const void* x_bf16_dev, int
 
 /*
  * One layer of a pre-norm stack in one call: residual add and RMSNorm
- * (as moe_residual_rmsnorm below), then y = MoE(xhat) (as moe_forward):
+ * (as moe_residual_rmsnorm below), then y = MoE(xhat) (as moe_forward).
+ * The source pages stack 48 such layers but do not spell out the norm; this
+ * is the plainest pre-norm: no learned weight, eps from the caller (the
+ * stacked workload uses 1e-6).
  *   x_out = bf16(x + y_prev)                      (y_prev may be NULL: x_out = x)
  *   xhat  = bf16(x_out / sqrt(mean(x_out^2) + eps))   (no learned weight)
  *   y     = MoE(xhat)
@@ -208,7 +212,8 @@ MOE_API moe_status_t moe_forward_norm(moe_layer_t* layer, const void* x_bf16_dev
                                       void* y_bf16_dev, int32_t* topk_idx_dev, float* topk_w_dev, void* cuda_stream);
 
 /*
- * Residual + RMSNorm between the layers of a stack, enqueued on the stream:
+ * Residual + RMSNorm between the layers of a stack (the pre-norm described
+ * at moe_forward_norm), enqueued on the stream:
  *   x_out   = bf16(x + y)                 (y may be NULL: x_out = x)
  *   xhat    = bf16(x_out / sqrt(mean(x_out^2) + eps))   (no learned weight)
  * All device bf16 [T][H]; x_out may alias x; xhat must not alias the others.
