@@ -133,3 +133,13 @@ def test_fragment_dequantization_reproduces_the_matrices(moe):
         R, K = (sh.I, sh.H) if m < 2 else (sh.H, sh.I)
         ref = oracle.dequant_matrix(blob[m * mb:(m + 1) * mb], R, K)
         assert np.array_equal(emulate_a_fragments(gpu, sh.H, sh.I, which), ref), which
+
+
+def test_binding_fails_loudly_without_the_library(moe, monkeypatch, tmp_path):
+    """No CPU fallback: with the CUDA library missing every call raises."""
+    monkeypatch.setattr(moe, "_lib", None)
+    monkeypatch.setattr(build, "CUDA_LIB", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        moe.lib()
+    with pytest.raises(RuntimeError, match="not built"):
+        moe.expert_bytes(2048, 512)
