@@ -242,6 +242,7 @@ void serve_entry(moe_layer* L, const RingEntry& e) {
 // (decode rings one every few tens of microseconds) and sleeps in 50 us steps
 // after 20 ms without one.
 struct CopyServer {
+  std::mutex life_mu;  // serializes starting and stopping the thread (taken before mu)
   std::mutex mu;
   std::vector<moe_layer*> layers;
   std::thread th;
@@ -302,6 +303,7 @@ void server_main() {
 // exit handler was registered earlier, so it runs later).
 void shutdown_server() {
   CopyServer& S = copy_server();
+  std::lock_guard<std::mutex> life(S.life_mu);
   S.stop = true;
   if (S.th.joinable()) S.th.join();
 }
@@ -310,6 +312,7 @@ void register_layer(moe_layer* L) {
   static const bool exit_hook = (std::atexit(shutdown_server), true);
   (void)exit_hook;
   CopyServer& S = copy_server();
+  std::lock_guard<std::mutex> life(S.life_mu);
   std::lock_guard<std::mutex> g(S.mu);
   L->tail = __atomic_load_n(&L->hm_host->head, __ATOMIC_ACQUIRE);
   S.layers.push_back(L);
@@ -320,10 +323,14 @@ void register_layer(moe_layer* L) {
   }
 }
 
-// After this returns the server no longer touches L.
+// After this returns the server no longer touches L.  Layers created and
+// destroyed from several host threads: life_mu keeps a registration from
+// slipping in between the decision to stop the thread and the join (which
+// would leave a layer with no server) and keeps two joins apart.
 void stop_server(moe_layer* L) {
   if (!L->registered) return;
   CopyServer& S = copy_server();
+  std::lock_guard<std::mutex> life(S.life_mu);
   bool join = false;
   {
     std::lock_guard<std::mutex> g(S.mu);
