@@ -310,3 +310,59 @@ def test_residual_exact_sum_rounded_once():
     out = oracle.residual(a, b)
     # 1 + 2^-8 ties to 1.0; 257 is halfway between 256 and 258 -> 256; -3+3 = 0
     assert out.tolist() == [0x3F80, 0x4380, 0x0000]
+
+
+# ---------------------------------------------------------------- forced selection and the gap
+
+
+def numpy_layer(L, sh, x_u16, sel):
+    """Independent float64 layer for a given selection: softmax of the
+    selected logits (numpy router), dense expert maths from the numpy decoder."""
+    xs = synth.bf16_to_f32(x_u16).astype(np.float64)
+    l = L.W_r.astype(np.float64) @ xs + (0.0 if L.bias is None else L.bias.astype(np.float64))
+    ls = l[sel]
+    w = np.exp(ls - ls.max())
+    w /= w.sum()
+    eb = sh.expert_bytes
+    y = np.zeros(sh.H)
+    for wj, e in zip(w, sel):
+        g, u, d = expert_mats(L.experts[e * eb:(e + 1) * eb], sh.H, sh.I)
+        y += wj * (d @ (silu(g @ xs) * (u @ xs)))
+    g, u, d = expert_mats(L.shared, sh.H, sh.I)
+    return y + d @ (silu(g @ xs) * (u @ xs)), w, l
+
+
+def test_forced_selection_and_gap():
+    """force= replaces the selection (weights: softmax over the forced set);
+    forcing the oracle's own choice changes nothing; gap is the distance
+    between the k-th and (k+1)-th largest logits."""
+    sh = synth.LayerShape(H=128, E=8, k=3, I=64, zipf_s=1.1)
+    L = synth.make_layer(sh, layer=905)
+    x = synth.activations(sh, 905, 0, 3)
+    r = oracle.moe_forward(sh.H, sh.I, sh.E, sh.k, L.W_r, L.bias, L.experts, L.shared, x)
+    same = oracle.moe_forward(sh.H, sh.I, sh.E, sh.k, L.W_r, L.bias, L.experts, L.shared, x, force=r["idx"])
+    for key in ("y", "idx", "w"):
+        assert np.array_equal(r[key], same[key]), key
+    forced = np.tile(np.array([1, 4, 7], np.int32), (3, 1))
+    f = oracle.moe_forward(sh.H, sh.I, sh.E, sh.k, L.W_r, L.bias, L.experts, L.shared, x, force=forced)
+    for t in range(3):
+        y, w, l = numpy_layer(L, sh, x[t], forced[t])
+        assert np.array_equal(f["idx"][t], forced[t])
+        assert np.allclose(f["w"][t], w, rtol=1e-12, atol=0)
+        assert np.allclose(f["y"][t], y, rtol=1e-11, atol=1e-14)
+        srt = np.sort(l)[::-1]
+        assert r["gap"][t] == pytest.approx(srt[sh.k - 1] - srt[sh.k], abs=1e-12)
+        assert r["gap"][t] >= 0.0
+
+
+def test_all_logits_tied_picks_the_lowest_indices_with_zero_gap():
+    """Every router row the same and no bias: all logits tie, the selection
+    is experts 0..k-1, the weights are 1/k and the gap is exactly 0."""
+    sh = synth.LayerShape(H=128, E=8, k=3, I=64)
+    L = synth.make_layer(sh, layer=906)
+    W = np.tile(L.W_r[:1], (sh.E, 1))
+    x = synth.activations(sh, 906, 0, 2)
+    r = oracle.moe_forward(sh.H, sh.I, sh.E, sh.k, W, None, L.experts, L.shared, x)
+    assert np.array_equal(r["idx"], np.tile(np.arange(sh.k, dtype=np.int32), (2, 1)))
+    assert np.all(r["w"] == 1.0 / 3.0) or np.allclose(r["w"], 1.0 / 3.0, rtol=1e-15, atol=0)
+    assert np.all(r["gap"] == 0.0)
