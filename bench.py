@@ -398,6 +398,101 @@ def run_stack(args):
     print(json.dumps(line), flush=True)
     st.close()
 
+def run_batched(args):
+    """Batched decode: calls of T independent tokens (T = 8: the fused
+    kernel; 9..64: route + gate/up + down kernels) through the page-scale
+    layer, all experts resident, about 1,000 tokens per step over 8 layer
+    replicas round-robin.  Algorithmic bytes of a call: W_r plus the
+    distinct experts its T tokens select (counted from the call's routing
+    output) plus the shared expert."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from quantized_expert_ffn_gemv_gb300 import moe, synth
+    T = args.batch
+    if not 2 <= T <= 64:
+        raise SystemExit("--batch must be 2..64")
+    torch.cuda.set_device(0)
+    L = synth.make_layer(synth.PAGE, layer=0)
+    layers = [moe.MoeLayer(L.shape, L.W_r, L.bias, L.experts, L.shared, max_tokens=T) for _ in range(args.replicas)]
+    calls = (args.tokens + T - 1) // T
+    ntok = calls * T
+    x_host = L_tokens(L, 0, ntok)
+    x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
+    y_pin = torch.empty_like(x_pin).pin_memory()
+    xd = x_pin.to("cuda")
+    yd = torch.empty_like(xd)
+    idx = torch.empty((ntok, K), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def step():
+        for c in range(calls):
+            sl = slice(c * T, (c + 1) * T)
+            layers[c % len(layers)].forward(xd[sl], yd[sl], idx[sl])
+
+    with torch.cuda.stream(stream):
+        step()
+    torch.cuda.synchronize()
+    routed = idx.cpu().numpy().reshape(calls, T * K)
+    distinct = [len(np.unique(r)) for r in routed]
+    step_bytes = sum(ROUTER_BYTES + (d + 1) * EXPERT_BYTES for d in distinct)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(os.path.join(tempfile.gettempdir(), "bench_batched_clocks.csv"))
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    with clocks:
+        with torch.cuda.stream(stream):
+            ev[0].record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            ev[1].record(stream)
+        torch.cuda.synchronize()
+    ms = ev[0].elapsed_time(ev[1])
+    with torch.cuda.stream(stream):
+        ev[2].record(stream)
+        for _ in range(args.steps):
+            xd.copy_(x_pin, non_blocking=True)
+            graph.replay()
+            y_pin.copy_(yd, non_blocking=True)
+        ev[3].record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = ev[2].elapsed_time(ev[3])
+    for l in layers:
+        _, code = l.stats()
+        if code != 0:
+            raise RuntimeError(f"layer error {code}")
+    peak, peak_kind = measured_peak()
+    step_s = ms * 1e-3 / args.steps
+    achieved = step_bytes / step_s / 1e9
+    fused = T <= 8
+    line = {
+        "metric": METRIC, "value": ntok / step_s, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16xf16+f32 (4-bit weights)", "data": "synthetic",
+        "config": {"workload": f"page-scale MoE layer, batched decode: {calls} calls of {T} independent tokens per "
+                               f"step over {len(layers)} layer replicas round-robin, all experts resident",
+                   "batch": T, "calls_per_step": calls, "replicas": len(layers),
+                   "l2": "inputs larger than L2 (layer replicas round-robin)", "parallelism": "replicas x1"},
+        "roofline": {"bound": "hbm", "kernel": "moe_decode_kernel" if fused else "route_kernel + gateup_kernel + "
+                     "down_kernel", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind, "bytes_per_unit": step_bytes / calls, "unit_of_work": "call",
+                     "distinct_experts_per_call": sum(distinct) / calls, "traffic": None},
+        "e2e": {"value": ntok / (ms_e2e * 1e-3 / args.steps), "unit": UNIT,
+                "h2d_bytes_per_step": int(x_pin.numel() * 2), "d2h_bytes_per_step": int(y_pin.numel() * 2)},
+        "gpu_launches": calls * (1 if fused else 3) * args.steps,
+        "clocks": clocks.summary(0),
+    }
+    print(json.dumps(line), flush=True)
+    for l in layers:
+        l.close()
+
+
 PREFILL_T = 4096
 PREFILL_PAIRS = PREFILL_T * (K + 1)                   # routed pairs + shared-expert rows
 PREFILL_FLOPS = 2 * PREFILL_PAIRS * 3 * H * I         # gate, up, down: 283.5 GFLOP on the tensor cores
@@ -492,9 +587,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-sample", type=int, default=32, help="oracle tokens timed for cpu_baseline")
     ap.add_argument("--tokens", type=int, default=TOKENS_PER_STEP)
-    ap.add_argument("--workload", default="decode", choices=["decode", "stack", "prefill"],
+    ap.add_argument("--workload", default="decode", choices=["decode", "stack", "prefill", "batched"],
                     help="decode: one page-scale layer, batch 1 (default); stack: 48-layer stack with a 25%% "
-                         "pool; prefill: one 4096-token chunk")
+                         "pool; prefill: one 4096-token chunk; batched: calls of --batch tokens")
+    ap.add_argument("--batch", type=int, default=8, help="tokens per call for --workload batched (2..64)")
     ap.add_argument("--layers", type=int, default=48, help="stack depth for --workload stack")
     ap.add_argument("--replicas", type=int, default=REPLICAS,
                     help="decode: identical layer copies cycled round-robin (8 keeps every reuse out of L2)")
@@ -509,6 +605,8 @@ def main():
         return run_stack(args)
     if args.workload == "prefill":
         return run_prefill(args)
+    if args.workload == "batched":
+        return run_batched(args)
 
     import torch
     import __graft_entry__
