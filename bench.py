@@ -399,7 +399,7 @@ def run_stack(args):
     st.close()
 
 def run_batched(args):
-    """Batched decode: calls of T independent tokens (T = 8: the fused
+    """Batched decode: calls of T independent tokens (T <= 8: the fused
     kernel; 9..64: route + gate/up + down kernels) through the page-scale
     layer, all experts resident, about 1,000 tokens per step over 8 layer
     replicas round-robin.  Algorithmic bytes of a call: W_r plus the
