@@ -169,7 +169,10 @@ MOE_API moe_status_t moe_slot_pool_seed(moe_layer_t* layer, const int32_t* exper
  *   topk_w_dev:  device fp32 [T][k] or NULL: their routing weights (softmax
  *                over all E renormalised over the selected k)
  * Selection: the k largest logits (router_w x + router_bias), ties to the
- * lower index.  Output: y = sum over the selected experts, in ascending
+ * lower index.  Logits are compensated (double-float) fp32 dot products,
+ * within about 1e-13 of the exact value (bound 5e-10 at H = 2048), so the
+ * selection equals a binary64 evaluation's unless two logits lie closer
+ * than that; NaN logits rank below every number.  Output: y = sum over the selected experts, in ascending
  * index, of w_j * FFN_j(x), plus FFN_shared(x), accumulated in fp32 and
  * rounded once to bf16 (round to nearest even).
  * Execution by T: T <= 8 one fused kernel (slot pool or all resident) when
@@ -229,6 +232,9 @@ typedef struct {
   uint64_t wait_ns;      /* device time spent waiting for slot copies */
   int32_t n_slots;       /* configured pool size (0 = none) */
   int32_t error;         /* sticky error code (moe_status_t), MOE_OK if none */
+  uint64_t rechecks;     /* prefill path: experts whose logit was recomputed exactly because
+                            the tensor-core logits put them within the GEMM's error bound of
+                            a token's k-th/(k+1)-th boundary, summed over calls */
 } moe_stats_t;
 
 /* Synchronize the layer's device and copy stream, then report counters.
@@ -291,12 +297,15 @@ MOE_API void moe_destroy(moe_layer_t* layer);
  * current device and the given stream.
  *   router_w: device fp32 [E][H], 16-byte aligned; router_bias: device fp32
  *   [E] or NULL; x_bf16: device bf16 [T][H].
- * Scratch: a fixed 256 KiB device array inside the library (T * E <= 65536
- * logits), shared by every call on a device and kept by it until the
- * process exits.  Nothing is allocated, ever.  The first call on a device
- * sets the array up (resolves its device address, clears its ticket):
- * make that first call before any stream capture.  Calls that overlap on
- * the GPU race on the array: serialize them.
+ * The logits are the compensated ones of moe_forward, computed in the same
+ * order, so the selection and weights are bit-identical to its routing.
+ * Scratch: a fixed 512 KiB device array inside the library (T * E <= 65536
+ * 64-bit router keys plus an arrival ticket), shared by every call on a
+ * device and kept by it until the process exits.  Nothing is allocated,
+ * ever.  The first call on a device sets the array up (resolves its device
+ * address and the kernel's shared-memory limit): make that first call
+ * before any stream capture.  Calls that overlap on the GPU race on the
+ * array: serialize them.
  * Errors: INVALID_ARG (NULL or misaligned pointers, bad shapes),
  * UNSUPPORTED (T > 64, k > 16, H > 4096, E > 4096 or T * E > 65536),
  * CUDA (set-up or launch failure).

@@ -9,12 +9,15 @@
 //
 //   prologue   this CTA's router rows, its shared-expert gate/up strip and
 //              down strip start loading; x -> fp16 in B-fragment order.
-//   router     fp32 dot products -> logits, each stored with the step number
+//   router     compensated (double-float) dot products, four warps per row;
+//              each logit's 52-bit order key is stored with a 12-bit call tag
 //              in one 64-bit word; readers poll for the tag (no grid barrier).
-//   routing    every CTA redundantly: top-k per token as a warp tournament
-//              (redux max over order-preserving keys) over each warp's range,
-//              a k-way merge of the warps' lists, ascending expert order, softmax
-//              weights renormalised over the k, the union of selected experts
+//   routing    every CTA redundantly: each warp ranks its range of experts
+//              (one 64-bit compare orders by logit, then index) and keeps its
+//              k best; entries below the best warp's k-th cannot be selected;
+//              the survivors are ranked against each other, giving the k in
+//              rank order; then ascending expert order, softmax weights
+//              renormalised over the k, the union of selected experts
 //              and the (expert, token) pair lists, the slot hit check and LRU
 //              victims (double-buffered pool state; CTA 0 writes the next
 //              state and rings the host doorbell).  Betelgeuse news page,
@@ -40,6 +43,7 @@
 #include "moe.h"
 #include "moe_internal.h"
 #include "moe_mma.cuh"
+#include "moe_route.cuh"
 
 namespace moe {
 namespace {
@@ -50,7 +54,6 @@ constexpr int kGroupWarps = 4;             // warps per gate/up strip
 constexpr int kProdWarp = 15;
 constexpr int kMaxT = 8;
 constexpr int kMaxE = 1024;
-constexpr int kRtVec = kMaxHidden / 256;   // float4 per lane per half router row
 constexpr int kMaxGuStages = 4;
 constexpr int kMaxDnStages = 16;
 constexpr int kListStride = kMaxTopK + 1;  // (key, e) entries per warp's top-k list: odd, no bank conflicts
@@ -150,10 +153,6 @@ struct Plan {
 
 __host__ __device__ inline size_t al128(size_t v) { return (v + 127) & ~size_t(127); }
 
-// the routing entries (lists, then selections) fit the budget of
-// 4 * kWarps * kMaxTopK (key, e) pairs
-static_assert(kWarps * kListStride + kMaxT * kMaxTopK <= 4 * kWarps * kMaxTopK, "routing scratch");
-
 __host__ __device__ inline Plan plan_with(int H, int I, int E, int k, int T, int G, int gs, int ds) {
   Plan p;
   p.rows_max = (E + G - 1) / G;
@@ -169,8 +168,8 @@ __host__ __device__ inline Plan plan_with(int H, int I, int E, int k, int T, int
   o += al128((size_t)T * H * 2);
   // region A: router rows (prologue), routing scratch, then down results
   const size_t router = (size_t)p.rows_max * H * 4;
-  // tokmask [E], then (key, e) entries: 16 lists of kListStride, selections;
-  // then the pool scratch (owner, stamp, key per slot, S <= E)
+  // tokmask [E], then the top-k scratch (TopkScratch, at most
+  // 4 * kWarps * kMaxTopK words); then the pool scratch (owner, stamp, key per slot, S <= E)
   const size_t routing = al128((size_t)E * 8) + (size_t)4 * kWarps * kMaxTopK * 8 + (size_t)E * 16 + 16 +
                          (size_t)(p.umax + 2) * 8;
   const size_t zbuf = (size_t)(p.umax + 1) * 32 * 4 * 4;
@@ -379,103 +378,130 @@ __device__ bool wait_full(uint64_t* bar, uint32_t parity, uint64_t deadline, boo
 
 // ------------------------------------------------------------------ top-k
 
-// Order-preserving key of a finite float (never 0), and its inverse.
-__device__ __forceinline__ uint32_t fkey(float v) {
-  const uint32_t u = __float_as_uint(v);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float fkey_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-// (key, e) ranks before (key2, e2): larger logit, or equal logit and lower index
-__device__ __forceinline__ bool before(uint32_t key, int e, uint32_t key2, int e2) {
-  return key > key2 || (key == key2 && e < e2);
-}
+constexpr uint32_t kTagMask = 0xFFFu;  // call tag in the low 12 bits of a published logit word
 
-// Poll one tagged logit until it carries this step's tag.
-__device__ __forceinline__ float wait_logit(const unsigned long long* p, uint32_t seq, const LayerArgs& a,
-                                            uint64_t deadline) {
+// Poll one published logit until it carries this call's tag; returns its key.
+__device__ __forceinline__ uint64_t wait_key(const unsigned long long* p, uint32_t tag, const LayerArgs& a,
+                                             uint64_t deadline) {
   unsigned long long v = ld_relaxed_u64(p);
   int spins = 0;
-  while ((uint32_t)(v >> 32) != seq) {
+  while (((uint32_t)v & kTagMask) != tag) {
     if (((++spins) & 63) == 0 && global_ns() > deadline) {
       set_error(a, MOE_ERR_TIMEOUT);
       break;
     }
     v = ld_relaxed_u64(p);
   }
-  return __uint_as_float((uint32_t)v);
+  return (uint64_t)v >> 12;
 }
 
-// The top k of this warp's range [base, base + range) in rank order, written
-// to out[0..k) as (key, expert); key 0 marks "none".  CPL keys per lane.
+// Routing scratch of one CTA (region A after the token masks).
+struct TopkScratch {
+  unsigned long long* list;  // [kWarps][kListStride] each warp's best, in rank order
+  unsigned long long* sel;   // [kMaxT][kMaxTopK] each token's k best, in rank order
+  unsigned long long* surv;  // survivors: token t's at t * wpt * kMaxTopK (wpt warps per token, wpt * T <= kWarps)
+  unsigned long long* kth;   // [kWarps] each warp's k-th best (0: fewer than k)
+  int* len;                  // [kWarps] entries in each warp's list
+  int* nsurv;                // [kMaxT] survivors per token
+};
+constexpr int kSurvTotal = kWarps * kMaxTopK;  // every list entry of every warp
+
+__device__ inline TopkScratch carve_topk(unsigned char* base) {
+  TopkScratch s;
+  s.list = reinterpret_cast<unsigned long long*>(base);
+  s.sel = s.list + kWarps * kListStride;
+  s.kth = s.sel + kMaxT * kMaxTopK;
+  s.surv = s.kth + kWarps;
+  s.len = reinterpret_cast<int*>(s.surv + kSurvTotal);
+  s.nsurv = s.len + kWarps;
+  return s;
+}
+constexpr size_t kTopkScratchBytes =
+    8 * (kWarps * kListStride + kMaxT * kMaxTopK + kWarps + kSurvTotal) + 4 * (kWarps + kMaxT);
+// the shared-memory plan reserves 4 * kWarps * kMaxTopK words for it
+static_assert(kTopkScratchBytes <= (size_t)4 * kWarps * kMaxTopK * 8, "routing scratch");
+
+// Level 1: the k best of this warp's range [base, base + range) of one
+// token's experts, in rank order, into list[0..len); kth = the k-th best or
+// 0.  One key per lane: each lane's rank from 32 compares.  Several keys per
+// lane: k rounds of a warp maximum.
 template <int CPL>
-__device__ void warp_topk(const unsigned long long* logits, int E, int k, int base, int range, uint32_t seq,
-                          uint2* out, const LayerArgs& a, uint64_t deadline) {
+__device__ void warp_best(const unsigned long long* words, int E, int k, int base, int range, uint32_t tag,
+                          unsigned long long* list, unsigned long long* kth, int* len, const LayerArgs& a,
+                          uint64_t deadline) {
   const int lane = threadIdx.x & 31;
-  uint32_t key[CPL];
+  uint64_t w[CPL];
 #pragma unroll
   for (int j = 0; j < CPL; ++j) {
     const int e = base + lane + 32 * j;
-    key[j] = (lane + 32 * j < range && e < E) ? fkey(wait_logit(logits + e, seq, a, deadline)) : 0u;
+    w[j] = (lane + 32 * j < range && e < E) ? rank_word(wait_key(words + e, tag, a, deadline), e) : 0ull;
   }
   if (CPL == 1) {
-    // exact rank inside the warp from 32 independent shuffles
-    const int e = base + lane;
     int r = 0;
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      const uint32_t ki = __shfl_sync(0xffffffffu, key[0], i);
-      r += (ki != 0u) && before(ki, base + i, key[0], e);
+      const uint64_t wi = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(w[0] >> 32), i) << 32) |
+                          __shfl_sync(0xffffffffu, (uint32_t)w[0], i);
+      r += wi > w[0];
     }
-    if (key[0] != 0u && r < k) out[r] = make_uint2(key[0], (uint32_t)e);
-    const int n = __popc(__ballot_sync(0xffffffffu, key[0] != 0u));
-    if (lane >= n && lane < k) out[lane] = make_uint2(0u, 0u);
+    const int n = __popc(__ballot_sync(0xffffffffu, w[0] != 0ull));
+    const int nl = n < k ? n : k;
+    if (w[0] != 0ull && r < k) list[r] = w[0];
+    if (lane == 0) {
+      len[0] = nl;
+      if (n < k) kth[0] = 0ull;
+    }
+    if (n >= k && r == k - 1) kth[0] = w[0];
     return;
   }
-  // k rounds of a warp max; equal keys -> lowest j, then lowest lane
   uint32_t taken = 0u;
+  int nl = 0;
+  uint64_t m = 0ull;
   for (int r = 0; r < k; ++r) {
-    uint32_t my = 0u;
-    int myj = CPL;
+    uint64_t my = 0ull;
+    int myj = -1;
 #pragma unroll
     for (int j = 0; j < CPL; ++j)
-      if (key[j] != 0u && !((taken >> j) & 1u) && (key[j] > my || myj == CPL)) { my = key[j]; myj = j; }
-    const uint32_t mx = __reduce_max_sync(0xffffffffu, my);
-    const uint32_t jmin = __reduce_min_sync(0xffffffffu, (mx != 0u && my == mx) ? (uint32_t)myj : 0xFFFFu);
-    const uint32_t ball = __ballot_sync(0xffffffffu, mx != 0u && my == mx && (uint32_t)myj == jmin);
-    const int wl = ball ? __ffs(ball) - 1 : 0;
-    if (lane == wl && ball) taken |= 1u << myj;
-    if (lane == 0) out[r] = make_uint2(ball ? mx : 0u, (uint32_t)(base + wl + 32 * (int)(jmin & 0xFF)));
+      if (!((taken >> j) & 1u) && w[j] > my) { my = w[j]; myj = j; }
+    m = warp_max_u64(my);
+    if (m == 0ull) break;
+    if (my == m) taken |= 1u << myj;  // words are distinct: one lane wins
+    if (lane == 0) list[r] = m;
+    ++nl;
+  }
+  if (lane == 0) {
+    len[0] = nl;
+    kth[0] = nl == k ? m : 0ull;
   }
 }
 
-// One warp per token: a k-way merge of the token's nl rank-ordered lists
-// (lane l < nl owns list l at lists[l * kListStride], key 0 = none).  Each
-// round takes the best head (larger key, then lower expert) and advances that
-// list; every lane keeps its list's next entry in a register, so an advance
-// is a register move and the load behind it has a round to land.  sel gets
-// the token's k largest logits in rank order.
-__device__ __forceinline__ void merge_lists(const uint2* lists, int nl, int k, uint2* sel) {
+// Level 2, step 1 (warp w of token t's wpt warps): the entries of list w
+// that are not below the best k-th of the token's warps (any selected
+// expert is among them) are appended to the token's survivors.
+__device__ __forceinline__ void keep_survivors(const TopkScratch& S, int t, int w, int wpt) {
   const int lane = threadIdx.x & 31;
-  const uint2 none = make_uint2(0u, 0xFFFFFFFFu);
-  const uint2* my = lists + lane * kListStride;
-  auto entry = [&](int j) {
-    const uint2 v = (lane < nl && j < k) ? my[j] : none;
-    return v.x == 0u ? none : v;
-  };
-  uint2 head = entry(0), next = entry(1);
-  int ptr = 1;  // index of next
-  for (int r = 0; r < k; ++r) {
-    const uint32_t mx = __reduce_max_sync(0xffffffffu, head.x);
-    const uint32_t emin = __reduce_min_sync(0xffffffffu, head.x == mx ? head.y : 0xFFFFFFFFu);
-    if (lane == 0) sel[r] = make_uint2(mx, emin);
-    if (mx != 0u && head.x == mx && head.y == emin) {
-      head = next;
-      next = entry(++ptr);
-    }
-  }
-  __syncwarp();
+  const uint64_t kv = lane < wpt ? S.kth[t * wpt + lane] : 0ull;
+  const uint64_t beta = warp_max_u64(kv);
+  const int n = S.len[w];
+  const uint64_t e = lane < n ? S.list[w * kListStride + lane] : 0ull;
+  const bool keep = e != 0ull && e >= beta;
+  const unsigned b = __ballot_sync(0xffffffffu, keep);
+  int base = 0;
+  if (lane == 0 && b) base = atomicAdd(&S.nsurv[t], __popc(b));
+  base = __shfl_sync(0xffffffffu, base, 0);
+  if (keep) S.surv[t * wpt * kMaxTopK + base + __popc(b & ((1u << lane) - 1u))] = e;
+}
+
+// Level 2, step 2 (thread i of token t's wpt * 32 threads): survivor i's
+// rank among the token's survivors; the k best land in sel in rank order.
+__device__ __forceinline__ void rank_survivors(const TopkScratch& S, int t, int wpt, int i, int k) {
+  const int n = S.nsurv[t];
+  if (i >= n) return;
+  const unsigned long long* sv = S.surv + t * wpt * kMaxTopK;
+  const uint64_t me = sv[i];
+  int r = 0;
+  for (int j = 0; j < n; ++j) r += sv[j] > me;
+  if (r < k) S.sel[t * kMaxTopK + r] = me;
 }
 
 // One warp per token: the k selected (in rank order in sel) reported in
@@ -484,12 +510,12 @@ __device__ __forceinline__ void merge_lists(const uint2* lists, int nl, int k, u
 // token in tokmask.  With rank_union (one token) the union entries are in
 // rank order and the combine mapping is written here.  sel is reused as
 // scratch.
-__device__ __forceinline__ void finish_topk(uint2* sel, int k, const Lists& L, unsigned long long* tokmask, int t, bool write_out,
-                                            const LayerArgs& a, bool rank_union = false) {
+__device__ __forceinline__ void finish_topk(unsigned long long* sel, int k, const Lists& L, unsigned long long* tokmask,
+                                            int t, bool write_out, const LayerArgs& a, bool rank_union = false) {
   const int lane = threadIdx.x & 31;
-  const uint2 me = (lane < k) ? sel[lane] : make_uint2(0u, 0u);
-  const int my_e = (lane < k) ? (int)me.y : INT_MAX;
-  const float v = (lane < k) ? fkey_value(me.x) : 0.f;
+  const uint64_t me = (lane < k) ? sel[lane] : 0ull;
+  const int my_e = (lane < k) ? word_expert(me) : INT_MAX;
+  const float v = (lane < k) ? key_value(word_key(me)) : 0.f;
   const float m = __shfl_sync(0xffffffffu, v, 0);  // rank 0 holds the largest logit
   int pos = 0;
 #pragma unroll
@@ -577,8 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   // their prologue (read-only weights into shared memory) and then wait for
   // this grid to complete before touching anything it writes.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // this thread's router bias (read-only), used once the router rows arrived
-  const float bias_v = (a.bias && tid < nrows * T) ? __ldg(a.bias + r0 + tid / T) : 0.f;
+  // this thread's router bias (read-only; thread i publishes row i / kMaxT)
+  const float bias_v = (a.bias && tid < nrows * kMaxT) ? __ldg(a.bias + r0 + tid / kMaxT) : 0.f;
   if (tid == 0) {
     for (int s = 0; s < R.gs; ++s) { mbar_init(&R.full_gu[s], 1); mbar_init(&R.empty_gu[s], kGroupWarps); }
     for (int s = 0; s < R.ds; ++s) { mbar_init(&R.full_dn[s], 1); mbar_init(&R.empty_dn[s], 1); }
@@ -611,6 +637,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const uint64_t deadline = global_ns() + a.wait_timeout_ns;
   const uint32_t step0 = (tid == 0) ? (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.st->step)) : 0u;
+  const uint32_t dstep0 = (tid == 0) ? (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.st->dstep)) : 0u;
+  __shared__ uint32_t s_dseq;
   __shared__ float s_inv[kMaxT];
   if (a.resid) {
     // Fused pre-norm: xs = bf16(resid + y_prev) into xraw, and each token's
@@ -680,58 +708,48 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     }
     if (bad) set_error(a, MOE_ERR_DEVICE);
   }
-  if (tid == 0) s_seq = step0 + 1u;
+  if (tid == 0) {
+    s_seq = step0 + 1u;
+    s_dseq = dstep0 + 1u;
+  }
   __syncthreads();
   const uint32_t seq = s_seq;
+  const uint32_t tag = s_dseq & kTagMask;  // this call's tag on the published logits
   uint32_t* cnt_cur = a.counters + (size_t)(seq & 1u) * a.cnt_stride;
   uint32_t* cnt_next = a.counters + (size_t)((seq + 1u) & 1u) * a.cnt_stride;
 
-  // ---- router: two warps per row (one per half), the same summation order
-  // as the batched path's router; bf16 x read exactly (shared-memory copy)
+  // ---- router: four warps per row (one per quarter of H) in the canonical
+  // compensated order; bf16 x read exactly (shared-memory copy)
   {
-    float* part = red;  // [16 warps][kMaxT]
-    const int row = warp >> 1, half = warp & 1;
+    DF* part = reinterpret_cast<DF*>(red);  // [rows_max <= 8][4 quarters][kMaxT]
     if (nrows > 0) {
       int spins = 0;
       while (!mbar_try_wait(full_rt, 0)) {
         if (((++spins) & 31) == 0 && global_ns() > deadline) { set_error(a, MOE_ERR_TIMEOUT); break; }
       }
     }
-    if (row < nrows) {
-      const float* wr = wrows + (size_t)row * H + half * (H / 2);
+    const int q = warp & 3, n4 = H / 16;
+    for (int row = warp >> 2; row < nrows; row += kWarps / 4) {
+      const float* wq = wrows + (size_t)row * H + q * (H / 4);
       for (int t = 0; t < T; ++t) {
-        const uint16_t* xr = xraw + t * H + half * (H / 2);
-        uint2 xv[kRtVec];
-#pragma unroll
-        for (int i = 0; i < kRtVec; ++i) {
-          const int q = lane + 32 * i;
-          xv[i] = (q < H / 8) ? *reinterpret_cast<const uint2*>(xr + 4 * q) : make_uint2(0u, 0u);
-        }
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < kRtVec; ++i) {
-          const int q = lane + 32 * i;
-          if (q < H / 8) {
-            const float4 wv = *reinterpret_cast<const float4*>(wr + 4 * q);
-            s = fmaf(wv.x, __uint_as_float(xv[i].x << 16), s);
-            s = fmaf(wv.y, __uint_as_float(xv[i].x & 0xFFFF0000u), s);
-            s = fmaf(wv.z, __uint_as_float(xv[i].y << 16), s);
-            s = fmaf(wv.w, __uint_as_float(xv[i].y & 0xFFFF0000u), s);
-          }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) part[warp * kMaxT + t] = s;
+        const DF d = warp_sum_df(quarter_partial_bf16(wq, xraw + t * H + q * (H / 4), n4, lane));
+        if (lane == 0) part[(row * 4 + q) * kMaxT + t] = d;
       }
     }
     __syncthreads();
-    if (tid < nrows * T) {
-      const int rr = tid / T, t = tid % T, e = r0 + rr;
-      const float l = part[(2 * rr) * kMaxT + t] + part[(2 * rr + 1) * kMaxT + t];
-      const float v = l + bias_v;
-      // value and step number in one 64-bit word: a reader that sees this
-      // step's tag sees this step's value (no fence, no grid barrier)
-      st_relaxed_u64(&tagged_logits[(size_t)t * E + e], ((unsigned long long)seq << 32) | __float_as_uint(v));
+    if (tid < nrows * kMaxT) {
+      // every row of the kMaxT-token table is published each call (rows past
+      // T with no key), so an unread row never keeps a tag older than the
+      // previous call's
+      const int rr = tid / kMaxT, t = tid % kMaxT, e = r0 + rr;
+      uint64_t key = 0ull;
+      if (t < T) {
+        const DF* pr = part + rr * 4 * kMaxT + t;
+        key = logit_key(pr[0], pr[kMaxT], pr[2 * kMaxT], pr[3 * kMaxT], bias_v);
+      }
+      // key and call tag in one 64-bit word: a reader that sees this call's
+      // tag sees this call's key (no fence, no grid barrier)
+      st_relaxed_u64(&tagged_logits[(size_t)t * E + e], (unsigned long long)((key << 12) | tag));
     }
   }
 
@@ -801,14 +819,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
 
   // ---- routing, redundantly in every CTA
   unsigned long long* tokmask = reinterpret_cast<unsigned long long*>(sm + PL.regA);
-  uint2* wlist = reinterpret_cast<uint2*>(sm + PL.regA + al128((size_t)E * 8));  // [16 warps][kListStride] (key, e)
-  uint2* sel = wlist + kWarps * kListStride;                                     // [T][kMaxTopK] selections
+  const TopkScratch TS = carve_topk(sm + PL.regA + al128((size_t)E * 8));
+  unsigned long long* sel = TS.sel;  // [T][kMaxTopK] selections in rank order
   // Early path (one token, every expert resident): the experts start right
-  // after the merge; a warp with no gate/up or down role finishes the
+  // after the selection; a warp with no gate/up or down role finishes the
   // softmax, the combine mapping and the statistics meanwhile.
   const bool early = T == 1 && !a.pool;
   const int fin_warp = R.gs < kMaxGuStages ? R.gs * kGroupWarps : 0;
   for (int e = tid; e < E; e += kThreads) tokmask[e] = 0ull;
+  if (tid < kMaxT) TS.nsurv[tid] = 0;
   if (c == 0)  // the other parity's counters, for the next call
     for (int i = tid; i < a.cnt_stride; i += kThreads) cnt_next[i] = 0u;
   {
@@ -820,22 +839,25 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     const int cpl = (range + 31) / 32;
     const int base = wt * range;
     if (t < T) {
+      const unsigned long long* words = tagged_logits + (size_t)t * E;
+      unsigned long long* lw = TS.list + warp * kListStride;
       if (cpl == 1)
-        warp_topk<1>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
+        warp_best<1>(words, E, k, base, range, tag, lw, TS.kth + warp, TS.len + warp, a, deadline);
       else if (cpl <= 2)
-        warp_topk<2>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
+        warp_best<2>(words, E, k, base, range, tag, lw, TS.kth + warp, TS.len + warp, a, deadline);
       else if (cpl <= 4)
-        warp_topk<4>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
+        warp_best<4>(words, E, k, base, range, tag, lw, TS.kth + warp, TS.len + warp, a, deadline);
       else if (cpl <= 8)
-        warp_topk<8>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
+        warp_best<8>(words, E, k, base, range, tag, lw, TS.kth + warp, TS.len + warp, a, deadline);
       else
-        warp_topk<16>(tagged_logits + (size_t)t * E, E, k, base, range, seq, wlist + warp * kListStride, a, deadline);
+        warp_best<16>(words, E, k, base, range, tag, lw, TS.kth + warp, TS.len + warp, a, deadline);
     }
     __syncthreads();
-    if (warp < T) {
-      merge_lists(wlist + warp * wpt * kListStride, wpt, k, sel + warp * kMaxTopK);
-      if (!early) finish_topk(sel + warp * kMaxTopK, k, L, tokmask, warp, c == 0, a);
-    }
+    if (t < T) keep_survivors(TS, t, warp, wpt);
+    __syncthreads();
+    if (t < T) rank_survivors(TS, t, wpt, wt * 32 + lane, k);
+    __syncthreads();
+    if (warp < T && !early) finish_topk(sel + warp * kMaxTopK, k, L, tokmask, warp, c == 0, a);
   }
   __syncthreads();
   // union of the selected experts (ascending) and pair offsets, from the
@@ -844,7 +866,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   // order on the early path, known as soon as the merge ends).
   if (early) {
     if (tid < k) {
-      const int e = (int)sel[tid].y;
+      const int e = word_expert(sel[tid]);
       L.u_expert[tid] = e;
       L.u_off[tid] = tid;
       L.u_slot[tid] = e;
@@ -1026,6 +1048,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   if (c == 0 && tid == (early ? fin_warp * 32 : 0)) {
     // stores and reductions only: nothing here waits for the (possibly cold) counters
     a.st->step = seq;
+    a.st->dstep = s_dseq;
     a.st->n_union = n_union;
     a.st->n_miss = s_nmiss;
     atomicAdd(&a.st->forwards, 1ull);

@@ -64,8 +64,10 @@ struct DevState {
   int32_t n_union;    // distinct routed experts of the current step
   int32_t n_miss;     // misses of the current step
   uint32_t ring_head; // doorbell entries written so far
-  int32_t pad[2];
+  uint32_t dstep;     // fused decode calls so far (tags the logits they publish)
+  int32_t pad;
   unsigned long long forwards, hits, misses, wait_ns;
+  unsigned long long rechecks;  // prefill: experts whose logit was recomputed exactly near the top-k boundary
 };
 
 struct RingEntry {
@@ -98,7 +100,8 @@ struct LayerArgs {
   DevState* st;
   HostMapped* hm;  // device address of the mapped host block
   uint32_t* ready;       // [E] per slot: step whose copy has landed (host copy server)
-  float* logits;        // [T][E]
+  float* logits;        // [T][E] tensor-core router output (prefill path)
+  unsigned long long* keys;  // [T <= 64][E] router keys of the batched path (moe_route.cuh)
   __half* x16;          // [T][H] B-fragment order
   int32_t* u_expert;    // [Umax]
   int32_t* u_slot;      // [Umax]

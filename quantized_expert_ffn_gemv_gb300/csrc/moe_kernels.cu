@@ -3,7 +3,8 @@
 // One moe_forward = three stream-ordered kernels chained with programmatic
 // dependent launch (griddepcontrol), so each grid is already resident when
 // its predecessor finishes:
-//   route_kernel   router GEMV (fp32, warp pair per expert row), then in the
+//   route_kernel   router GEMV (compensated fp32, four warps per expert row,
+//                  the canonical order of moe_route.cuh), then in the
 //                  last-arriving CTA: top-k per token, softmax weights and
 //                  grouping of (token, expert) pairs by expert.
 //   gateup_kernel  per (expert, 16-row strip): 4-bit gate and up rows
@@ -22,6 +23,7 @@
 #include "moe.h"
 #include "moe_internal.h"
 #include "moe_mma.cuh"
+#include "moe_route.cuh"
 
 namespace moe {
 namespace {
@@ -65,10 +67,10 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 // ------------------------------------------------------------------ route
 
-constexpr int kRouteRows = 4;        // expert rows per CTA (two warps per row)
+constexpr int kRouteRows = 2;        // expert rows per CTA (four warps per row, one per quarter of H)
 constexpr int kRouteThreads = 256;
 constexpr int kRouteChunk = 8;       // tokens staged in shared memory at a time
-constexpr int kRouteVec = kMaxHidden / 256;  // float4 per lane per half row
+constexpr int kRouteVec = kMaxHidden / 512;  // float4 per lane per quarter row
 
 struct FinishSmem {
   size_t lrow, tokmask, uidx, poff, sidx, sw, misc, total;
@@ -76,10 +78,14 @@ struct FinishSmem {
 
 __host__ __device__ inline size_t align16(size_t v) { return (v + 15) & ~size_t(15); }
 
+// Warps of the last CTA that select top-k (each stages one token's E rank
+// words in shared memory).
+__host__ __device__ inline int topk_warps(int E) { return E <= 2048 ? 8 : 4; }
+
 __host__ __device__ inline FinishSmem finish_layout(int E) {
   FinishSmem f;
   f.lrow = 0;
-  f.tokmask = f.lrow + align16(sizeof(float) * 8 * (size_t)E);
+  f.tokmask = f.lrow + align16(sizeof(unsigned long long) * topk_warps(E) * (size_t)E);
   f.uidx = f.tokmask + align16(sizeof(unsigned long long) * (size_t)E);
   f.poff = f.uidx + align16(sizeof(int) * (size_t)E);
   f.sidx = f.poff + align16(sizeof(int) * (size_t)E);
@@ -140,55 +146,26 @@ __device__ void route_finish(const LayerArgs& a, unsigned char* smem) {
   for (int i = tid; i < a.cnt_stride; i += kRouteThreads) a.counters[(size_t)((seq + 1u) & 1u) * a.cnt_stride + i] = 0u;
 
   // ---- top-k per token (warp per token), ties to the lower index
-  for (int t = warp; t < T; t += 8) {
-    float* lr = lrow + warp * E;
-    for (int e = lane; e < E; e += 32) lr[e] = ld_cg_f32(&a.logits[(size_t)t * E + e]);
-    __syncwarp();
-    int sel[kMaxTopK];
-    float selv[kMaxTopK];
-    for (int r = 0; r < k; ++r) {
-      float bv = -FLT_MAX;
-      int bi = INT_MAX;
-      for (int e = lane; e < E; e += 32) {
-        float v = lr[e];  // NaN marks an expert already taken
-        if (v > bv || (v == bv && e < bi)) { bv = v; bi = e; }
+  const int nw = topk_warps(E);
+  if (warp < nw)
+    for (int t = warp; t < T; t += nw) {
+      unsigned long long* lr = reinterpret_cast<unsigned long long*>(lrow) + (size_t)warp * E;
+      for (int e = lane; e < E; e += 32) lr[e] = rank_word(__ldcg(&a.keys[(size_t)t * E + e]), e);
+      __syncwarp();
+      int sel[kMaxTopK];
+      float selv[kMaxTopK];
+      warp_select_k(lr, E, k, sel, selv);
+      if (lane == 0) {
+        // ascending expert index, weights renormalised over the selection
+        softmax_ascending(sel, selv, k, a.topk_idx + t * k, a.topk_w + t * k);
+        for (int j = 0; j < k; ++j) {
+          sidx[t * k + j] = sel[j];
+          sw[t * k + j] = a.topk_w[t * k + j];
+          atomicOr(&tokmask[sel[j]], 1ull << t);
+        }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-      }
-      if (bi == INT_MAX) bi = 0;  // only reachable with non-finite logits
-      if (lane == (bi & 31)) lr[bi] = __int_as_float(0x7fc00000);
-      sel[r] = bi;
-      selv[r] = bv;
       __syncwarp();
     }
-    if (lane == 0) {
-      // ascending expert index, weights renormalised over the selection
-      const float m = selv[0];
-      for (int i = 1; i < k; ++i) {
-        int ki = sel[i];
-        float kv = selv[i];
-        int j = i - 1;
-        while (j >= 0 && sel[j] > ki) { sel[j + 1] = sel[j]; selv[j + 1] = selv[j]; --j; }
-        sel[j + 1] = ki;
-        selv[j + 1] = kv;
-      }
-      float z = 0.f;
-      for (int j = 0; j < k; ++j) z += expf(selv[j] - m);
-      for (int j = 0; j < k; ++j) {
-        float wj = expf(selv[j] - m) / z;
-        sidx[t * k + j] = sel[j];
-        sw[t * k + j] = wj;
-        a.topk_idx[t * k + j] = sel[j];
-        a.topk_w[t * k + j] = wj;
-        atomicOr(&tokmask[sel[j]], 1ull << t);
-      }
-    }
-    __syncwarp();
-  }
   __syncthreads();
 
   // ---- union of selected experts (ascending) and pair offsets
@@ -247,18 +224,18 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(LayerArgs a) {
   extern __shared__ __align__(16) unsigned char smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int H = a.H, E = a.E, T = a.T;
-  const int row = blockIdx.x * kRouteRows + (warp >> 1);
-  const int half = warp & 1;
-  const int q4 = H / 8;  // float4 per half row
+  const int row = blockIdx.x * kRouteRows + (warp >> 2);
+  const int q = warp & 3;
+  const int n4 = H / 16;  // float4 groups per quarter row
   const bool row_ok = row < E;
 
   // Router rows do not depend on the previous kernel: load them first.
   float4 w[kRouteVec];
-  const float4* wrow = reinterpret_cast<const float4*>(a.W_r + (size_t)(row_ok ? row : 0) * H) + half * q4;
+  const float4* wq = reinterpret_cast<const float4*>(a.W_r + (size_t)(row_ok ? row : 0) * H + q * (H / 4));
 #pragma unroll
   for (int i = 0; i < kRouteVec; ++i) {
-    const int q = lane + 32 * i;
-    w[i] = (row_ok && q < q4) ? __ldg(wrow + q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int j = lane + 32 * i;
+    w[i] = (row_ok && j < n4) ? __ldg(wq + j) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
   pdl_wait();
 
@@ -281,8 +258,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(LayerArgs a) {
     if (bad) set_error(a, MOE_ERR_DEVICE);
   }
 
-  float* xs = reinterpret_cast<float*>(smem);            // [chunk][H]
-  float* red = xs + kRouteChunk * H;                      // [8 warps][chunk]
+  float* xs = reinterpret_cast<float*>(smem);                  // [chunk][H]
+  DF* red = reinterpret_cast<DF*>(xs + kRouteChunk * H);        // [8 warps][chunk]
   for (int t0 = 0; t0 < T; t0 += kRouteChunk) {
     const int nt = min(kRouteChunk, T - t0);
     __syncthreads();
@@ -294,30 +271,26 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(LayerArgs a) {
     }
     __syncthreads();
     for (int tt = 0; tt < nt; ++tt) {
-      const float4* xr = reinterpret_cast<const float4*>(xs + tt * H) + half * q4;
-      float s = 0.f;
+      // the canonical compensated order (moe_route.cuh): lane-strided float4
+      // groups of this quarter, then the xor butterfly
+      const float4* xr = reinterpret_cast<const float4*>(xs + tt * H + q * (H / 4));
+      DF d{0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < kRouteVec; ++i) {
-        const int q = lane + 32 * i;
-        if (q < q4) {
-          const float4 xv = xr[q];
-          s = fmaf(w[i].x, xv.x, s);
-          s = fmaf(w[i].y, xv.y, s);
-          s = fmaf(w[i].z, xv.z, s);
-          s = fmaf(w[i].w, xv.w, s);
-        }
+        const int j = lane + 32 * i;
+        if (j < n4) dot2_acc4(d, w[i], xr[j]);
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-      if (lane == 0) red[warp * kRouteChunk + tt] = s;
+      d = warp_sum_df(d);
+      if (lane == 0) red[warp * kRouteChunk + tt] = d;
     }
     __syncthreads();
     if (tid < kRouteRows * nt) {
       const int r = tid / nt, tt = tid % nt;
       const int e = blockIdx.x * kRouteRows + r;
       if (e < E) {
-        const float l = red[(2 * r) * kRouteChunk + tt] + red[(2 * r + 1) * kRouteChunk + tt];
-        a.logits[(size_t)(t0 + tt) * E + e] = l + ((a.bias) ? __ldg(a.bias + e) : 0.f);
+        const DF* pr = red + (4 * r) * kRouteChunk + tt;
+        a.keys[(size_t)(t0 + tt) * E + e] = logit_key(pr[0], pr[kRouteChunk], pr[2 * kRouteChunk],
+                                                      pr[3 * kRouteChunk], a.bias ? __ldg(a.bias + e) : 0.f);
       }
     }
   }
@@ -604,7 +577,7 @@ size_t down_smem(int NG, int T) { return sizeof(float) * (kDnWarps * NG * 32 * 4
 }  // namespace
 
 size_t route_smem_bytes(int H, int E) {
-  size_t a = sizeof(float) * (kRouteChunk * (size_t)H + 8 * kRouteChunk);
+  size_t a = sizeof(float) * kRouteChunk * (size_t)H + sizeof(DF) * 8 * kRouteChunk;
   size_t b = finish_layout(E).total;
   return a > b ? a : b;
 }

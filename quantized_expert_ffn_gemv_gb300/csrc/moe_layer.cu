@@ -477,12 +477,15 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
     off += align256(bytes);
     return o;
   };
-  const size_t o_st = carve(sizeof(DevState)), o_ready = carve(4ull * E), o_logits = carve(4ull * Tm * E),
+  const int Tl = Tm > kMaxTokens ? Tm : 1;   // fp32 logits: the prefill path only
+  const int Tk = Tb > 8 ? Tb : 8;            // the fused kernel publishes 8 token rows every call
+  const size_t o_st = carve(sizeof(DevState)), o_ready = carve(4ull * E), o_logits = carve(4ull * Tl * E),
+               o_keys = carve(8ull * Tb * E),
                o_x16 = carve(2ull * Tb * H), o_uexp = carve(4ull * Um), o_uslot = carve(4ull * Um),
                o_uoff = carve(4ull * (Um + 1)), o_ptok = carve(4 * P),
                o_pw = carve(4 * P), o_tku = carve(4 * P), o_tkpos = carve(4 * P),
                o_h16 = carve(2ull * (P + Tb) * I), o_tki = carve(4ull * Tm * k), o_tkw = carve(4ull * Tm * k),
-               o_bar = carve(8ull * Tb * E), o_cnt = carve(8ull * (Um + 2)), o_pool = carve(4ull * 2 * 3 * E);
+               o_bar = carve(8ull * Tk * E), o_cnt = carve(8ull * (Um + 2)), o_pool = carve(4ull * 2 * 3 * E);
   if (cudaMalloc(&L->dev_block, off) != cudaSuccess) {
     L->dev_block = nullptr;
     return fail(MOE_ERR_OUT_OF_MEMORY);
@@ -503,6 +506,7 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.hm = L->hm_dev;
   a.ready = (uint32_t*)(b + o_ready);
   a.logits = (float*)(b + o_logits);
+  a.keys = (unsigned long long*)(b + o_keys);
   a.x16 = (__half*)(b + o_x16);
   a.u_expert = (int32_t*)(b + o_uexp);
   a.u_slot = (int32_t*)(b + o_uslot);
@@ -538,8 +542,15 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
     L->encode_map = (TensorMapEncodeFn)fn;
     if (!prefill_encode_maps(L->encode_map, L->pf, H, I, E, k, Tm, &L->pf_maps)) return fail(MOE_ERR_CUDA);
   }
+  // The copy streams take the device's highest priority.  Streams of
+  // different priorities never share a hardware work queue, so a slot copy
+  // is never queued behind compute work that waits for the decode kernel
+  // (which itself waits for the copy): compute streams are created at the
+  // default, lowest, priority.
+  int prio_least = 0, prio_greatest = 0;
+  if (cudaDeviceGetStreamPriorityRange(&prio_least, &prio_greatest) != cudaSuccess) return fail(MOE_ERR_CUDA);
   for (auto& cs : L->copy_stream)
-    if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) {
+    if (cudaStreamCreateWithPriority(&cs, cudaStreamNonBlocking, prio_greatest) != cudaSuccess) {
       cs = nullptr;
       return fail(MOE_ERR_CUDA);
     }
@@ -754,6 +765,7 @@ moe_status_t moe_get_stats(moe_layer_t* L, moe_stats_t* out) {
   int e = L->host_error.load();
   if (!e) e = ds.error;
   out->error = e;
+  out->rechecks = ds.rechecks;
   return (moe_status_t)e;
 }
 

@@ -10,8 +10,11 @@
 //              x -> fp16 rows for the expert GEMMs
 //   router     tcgen05 GEMM: logits [T][E] = sum of the three pieces' products
 //   top-k      warp per token: the k largest logits (ties to the lower
-//              index), ascending expert order, softmax over the selection;
-//              bit t of the expert's token bitmap
+//              index), made exact by recomputing, with the compensated
+//              router, the experts whose tensor-core logits lie within the
+//              GEMM's error bound of the k-th/(k+1)-th boundary; ascending
+//              expert order, softmax over the selection; bit t of the
+//              expert's token bitmap
 //   prefix     warp per expert: set bits before each bitmap word
 //   scan       per-expert counts -> pair offsets, chunk records of up to 256
 //              tokens for the tensor cores, and an expert's last chunk of at
@@ -42,6 +45,7 @@
 #include "moe_internal.h"
 #include "moe_mma.cuh"
 #include "moe_prefill.h"
+#include "moe_route.cuh"
 
 namespace moe {
 namespace {
@@ -219,6 +223,20 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(LayerArgs a, PrefillA
     p.w_split[nw + i] = __bfloat16_as_ushort(w1);
     p.w_split[2 * nw + i] = __bfloat16_as_ushort(w2);
   }
+  // router row norms, for the recheck bound of the top-k kernel (fp32 sum of
+  // squares rounded up by 0.1 %, far more than its own rounding error)
+  {
+    const int lane = threadIdx.x & 31;
+    const int gw = (int)((blockIdx.x * 256 + threadIdx.x) >> 5), nwarps = (int)(gridDim.x * 8);
+    for (int e = gw; e < a.E; e += nwarps) {
+      const float* wr = a.W_r + (size_t)e * a.H;
+      float ss = 0.f;
+      for (int h = lane; h < a.H; h += 32) ss = fmaf(wr[h], wr[h], ss);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) p.wnorm[e] = sqrtf(ss) * 1.001f;
+    }
+  }
   int bad = 0;
   for (size_t i = ((size_t)blockIdx.x * 256 + threadIdx.x) * 8; i < nx; i += stride * 8) {
     const uint4 v = *reinterpret_cast<const uint4*>(a.x + i);
@@ -235,25 +253,60 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(LayerArgs a, PrefillA
   if (bad) set_error(a, MOE_ERR_DEVICE);
 }
 
-// Warp per token: k rounds of a warp argmax (value desc, index asc) over the
-// token's logits, held in registers (CPL per lane; CPL = 0: read from
-// memory each round, for very large E).  Sets bit t of each selected
-// expert's bitmap row; the per-expert counts come from the bitmap.
+// Bound on |tensor-core logit - exact logit| per unit of |W_r[e]| |x_t|:
+// the router GEMM adds 3 * H / 16 MMA steps of exact bf16 x bf16 products
+// into an fp32 accumulator (at most 2^-23 relative per step even without
+// round-to-nearest: 4.6e-5 at H = 2048), and the three bf16 pieces miss W_r
+// by at most 2^-27 relative; 1.25e-4 leaves a factor 2.5 over their sum.
+constexpr float kTcBound = 1.25e-4f;
+
+__device__ __forceinline__ uint64_t shfl_u64(uint64_t v, int src) {
+  const uint32_t lo = __shfl_sync(0xffffffffu, (uint32_t)v, src);
+  const uint32_t hi = __shfl_sync(0xffffffffu, (uint32_t)(v >> 32), src);
+  return ((uint64_t)hi << 32) | lo;
+}
+__device__ __forceinline__ uint64_t shfl_up_u64(uint64_t v, int d) {
+  const uint32_t lo = __shfl_up_sync(0xffffffffu, (uint32_t)v, d);
+  const uint32_t hi = __shfl_up_sync(0xffffffffu, (uint32_t)(v >> 32), d);
+  return ((uint64_t)hi << 32) | lo;
+}
+
+// Warp per token: k + 1 rounds of a warp argmax (value desc, index asc) over
+// the token's tensor-core logits, held in registers (CPL per lane; CPL = 0:
+// read from memory each round, for very large E).  The selection is exact:
+// when the k-th and (k+1)-th tensor-core logits are closer than twice the
+// error bound delta_t (kTcBound * max_e |W_r[e]| * |x_t|), every expert
+// whose logit lies within 2 delta_t of that boundary is recomputed with the
+// compensated router in the library's canonical order (moe_route.cuh), and
+// the places the experts above the band do not fill go to the best of those
+// by exact key.  Sets bit t of each selected expert's bitmap row; the
+// per-expert counts come from the bitmap.
 template <int CPL>
 __global__ void __launch_bounds__(256) prefill_topk_kernel(LayerArgs a, PrefillArgs p) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int E = a.E, k = a.k;
+  const int E = a.E, k = a.k, H = a.H;
+  __shared__ unsigned int s_wmax;  // max row norm (positive floats order as their bits)
+  if (threadIdx.x == 0) s_wmax = 0u;
+  __syncthreads();
+  {
+    unsigned int m = 0u;
+    for (int e = threadIdx.x; e < E; e += 256) m = max(m, __float_as_uint(p.wnorm[e]));
+    atomicMax(&s_wmax, m);
+  }
+  __syncthreads();
   if (t >= a.T) return;
   const float* lt = a.logits + (size_t)t * E;
   constexpr int kRegs = CPL > 0 ? CPL : 1;
   float lv[kRegs];
 #pragma unroll
   for (int i = 0; i < kRegs; ++i) lv[i] = (CPL > 0 && lane + 32 * i < E) ? lt[lane + 32 * i] : -FLT_MAX;
-  int my_e = INT_MAX;   // lane r < k: the expert of rank r
+  int my_e = INT_MAX;   // lane r <= k: the expert of rank r
   float my_v = 0.f;     // and its logit
   uint32_t taken[kMaxExperts / 1024] = {};  // bit i: logit lane + 32 i already selected
-  for (int r = 0; r < k; ++r) {
+  const int rounds = k < E ? k + 1 : k;
+  bool boundary = k < E;  // a (k+1)-th comparable logit exists
+  for (int r = 0; r < rounds; ++r) {
     float bv = -FLT_MAX;
     int bi = INT_MAX;
     if (CPL > 0) {
@@ -285,9 +338,13 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(LayerArgs a, PrefillA
         bi = oi;
       }
     }
-    if (bi == INT_MAX) {  // fewer than k comparable logits (NaN): flagged; keep the indices distinct
-      if (lane == 0) set_error(a, MOE_ERR_DEVICE);
-      bi = r;
+    if (bi == INT_MAX) {
+      if (r == k) {  // only k comparable logits: no boundary to check
+        boundary = false;
+        break;
+      }
+      if (lane == 0) set_error(a, MOE_ERR_DEVICE);  // fewer than k comparable logits (NaN): flagged
+      bi = r;                                       // keep the indices distinct
     }
     if (lane == (bi & 31)) {
       if (CPL > 0)
@@ -300,8 +357,75 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(LayerArgs a, PrefillA
       my_v = bv;
     }
   }
+  if (boundary) {
+    const float lk = __shfl_sync(0xffffffffu, my_v, k - 1), lk1 = __shfl_sync(0xffffffffu, my_v, k);
+    const uint32_t* xw = reinterpret_cast<const uint32_t*>(a.x + (size_t)t * H);
+    float xs = 0.f;
+    for (int i = lane; i < H / 2; i += 32) {
+      const uint32_t v = xw[i];
+      xs = fmaf(bf_lo(v), bf_lo(v), xs);
+      xs = fmaf(bf_hi(v), bf_hi(v), xs);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, o);
+    const float delta = kTcBound * __uint_as_float(s_wmax) * (sqrtf(xs) * 1.001f) + 1e-6f * (fabsf(lk) + 1.f);
+    if (lk - lk1 <= 2.f * delta) {
+      // above hi: surely selected; below lo: surely not; in between: exact
+      const float hi = lk + 2.f * delta, lo = lk1 - 2.f * delta;
+      const int n_in = __popc(__ballot_sync(0xffffffffu, lane < k && my_v > hi));
+      const int pick = k - n_in;
+      uint64_t best = 0ull;  // lanes 0 .. pick-1: the best exact words so far, in rank order
+      int nchk = 0;
+      auto consider = [&](int e) {
+        DF q4[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          q4[q] = warp_sum_df(quarter_partial_bf16(a.W_r + (size_t)e * H + q * (H / 4),
+                                                   a.x + (size_t)t * H + q * (H / 4), H / 16, lane));
+        const uint64_t w = rank_word(logit_key(q4[0], q4[1], q4[2], q4[3], a.bias ? a.bias[e] : 0.f), e);
+        const unsigned below = __ballot_sync(0xffffffffu, lane < pick && best < w);
+        if (below) {
+          const int pos = __ffs(below) - 1;
+          const uint64_t up = shfl_up_u64(best, 1);
+          if (lane > pos && lane < pick) best = up;
+          if (lane == pos) best = w;
+        }
+        ++nchk;
+      };
+      if (CPL > 0) {
+#pragma unroll
+        for (int i = 0; i < kRegs; ++i) {
+          const int e = lane + 32 * i;
+          unsigned b = __ballot_sync(0xffffffffu, e < E && lv[i] >= lo && lv[i] <= hi);
+          while (b) {
+            const int src = __ffs(b) - 1;
+            b &= b - 1;
+            consider(src + 32 * i);
+          }
+        }
+      } else {
+        for (int i = 0; i < (E + 31) / 32; ++i) {
+          const int e = lane + 32 * i;
+          const float v = e < E ? lt[e] : -FLT_MAX;
+          unsigned b = __ballot_sync(0xffffffffu, e < E && v >= lo && v <= hi);
+          while (b) {
+            const int src = __ffs(b) - 1;
+            b &= b - 1;
+            consider(src + 32 * i);
+          }
+        }
+      }
+      const uint64_t got = shfl_u64(best, lane >= n_in ? lane - n_in : 0);
+      if (lane >= n_in && lane < k) {
+        my_e = word_expert(got);
+        my_v = key_value(word_key(got));
+      }
+      if (lane == 0) atomicAdd(&a.st->rechecks, (unsigned long long)nchk);
+    }
+  }
   // in parallel, lane r for rank r: its place in ascending expert order, the
-  // weight exp(v - max) / z with z summed in ascending expert order
+  // weight exp(v - m) / z with z summed in ascending expert order (m = lane
+  // 0's logit, the largest up to the recheck band)
   const float m = __shfl_sync(0xffffffffu, my_v, 0);
   int pos = 0;
 #pragma unroll
@@ -1155,7 +1279,8 @@ size_t prefill_scratch_bytes(int H, int I, int E, int k, int Tm) {
   return pf_align(4ull * (E + 1)) + 2 * pf_align(4ull * (E + 2)) + pf_align(8) + pf_align(16 * chunks) +
          pf_align(16ull * (E + 1)) +
          2 * pf_align(4 * P) +
-         2 * pf_align(4ull * E * words) + pf_align(6ull * E * H) + pf_align(2ull * Tm * H) + pf_align(2 * P * I) +
+         2 * pf_align(4ull * E * words) + pf_align(6ull * E * H) + pf_align(4ull * E) + pf_align(2ull * Tm * H) +
+         pf_align(2 * P * I) +
          pf_align(2 * P * H);
 }
 
@@ -1180,6 +1305,7 @@ PrefillArgs prefill_carve(void* block, int H, int I, int E, int k, int Tm) {
   p.bitmap = (uint32_t*)carve(4ull * E * words);
   p.prefix = (int32_t*)carve(4ull * E * words);
   p.w_split = (uint16_t*)carve(6ull * E * H);
+  p.wnorm = (float*)carve(4ull * E);
   p.x16p = (__half*)carve(2ull * Tm * H);
   p.h16p = (__half*)carve(2 * P * I);
   p.z16 = (__half*)carve(2 * P * H);

@@ -36,7 +36,7 @@ class LayerDesc(C.Structure):
 
 class Stats(C.Structure):
     _fields_ = [("forwards", C.c_uint64), ("hits", C.c_uint64), ("misses", C.c_uint64), ("h2d_bytes", C.c_uint64),
-                ("wait_ns", C.c_uint64), ("n_slots", C.c_int32), ("error", C.c_int32)]
+                ("wait_ns", C.c_uint64), ("n_slots", C.c_int32), ("error", C.c_int32), ("rechecks", C.c_uint64)]
 
 
 _lib = None
@@ -126,8 +126,28 @@ def residual_rmsnorm(x, y, eps, x_out, xhat, stream=None):
 
 
 def route_noalloc(W_r, bias, x, k, topk_idx, topk_w, stream=None):
-    """Router + top-k without any device allocation (torch CUDA tensors)."""
+    """Router + top-k without any device allocation (torch CUDA tensors).
+
+    W_r float32 [E, H], bias float32 [E] or None, x bf16 [T, H]; writes
+    topk_idx int32 [T, k] and topk_w float32 [T, k].  Shapes, dtypes,
+    contiguity and device are checked here, so a mismatched tensor is an
+    error and never an out-of-bounds device access."""
+    import torch
+    if x.dim() != 2 or W_r.dim() != 2:
+        raise ValueError("x must be [T, H] and W_r [E, H]")
     T, H = x.shape
+    E = W_r.shape[0]
+    tensors = {"W_r": (W_r, torch.float32, (E, H)), "x": (x, torch.bfloat16, (T, H)),
+               "topk_idx": (topk_idx, torch.int32, (T, k)), "topk_w": (topk_w, torch.float32, (T, k))}
+    if bias is not None:
+        tensors["bias"] = (bias, torch.float32, (E,))
+    for name, (t, dt, shape) in tensors.items():
+        if t.dtype != dt or tuple(t.shape) != shape:
+            raise ValueError(f"{name}: expected {dt} {shape}, got {t.dtype} {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device != x.device or t.device.type != "cuda":
+            raise ValueError(f"{name} must be a CUDA tensor on {x.device}")
     check(lib().moe_route_noalloc(W_r.data_ptr(), None if bias is None else bias.data_ptr(), x.data_ptr(), T, H,
                                   W_r.shape[0], k, topk_idx.data_ptr(), topk_w.data_ptr(), _stream_ptr(stream)),
           "moe_route_noalloc")

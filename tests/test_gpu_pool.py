@@ -46,7 +46,7 @@ def test_failed_copy_is_an_error_not_zero_weights(small):
     from quantized_expert_ffn_gemv_gb300 import moe
     x, _ = resampled_tokens(small, 700, 8)
     pool = make_gpu_layer(small, max_tokens=1, n_slots=8)
-    pool.set_miss_service(0)  # the host copy server moves the bytes (the default, set explicitly)
+    pool.set_miss_service(0)  # the host copy server moves the bytes (not the default: set explicitly)
     pool.debug_copy_faults(fail_copy_n=3)
     with pytest.raises(moe.MoeError) as ei:
         run(pool, x, T=1)
@@ -168,3 +168,52 @@ def test_pool_with_calls_of_mixed_sizes(small, service):
     check_against_oracle(small, x, *outs["pool"], rows=np.arange(0, n, 5))
     full.close()
     pool.close()
+
+
+def test_copy_engine_service_never_times_out_under_stream_syncs():
+    """The host copy server behind the doorbell, 10 runs of 200 tokens
+    through 8 page-scale pooled layers (64 slots each), eager calls with a
+    stream synchronize every 2 tokens: every run ends without a timeout and
+    bit-identical to the all-resident layers.  The decode kernel waits for
+    the copies, so a copy held behind the caller's queued work would end a
+    call with MOE_ERR_TIMEOUT (bounded here at 0.5 s)."""
+    import torch
+    from quantized_expert_ffn_gemv_gb300 import moe
+    n_layers, n_tok, slots = 8, 200, 64
+    layers = []
+    for l in range(n_layers):
+        L = synth.make_layer(synth.PAGE, layer=l)
+        layers.append(moe.MoeLayer(L.shape, L.W_r, L.bias, L.experts, L.shared, max_tokens=1))
+        del L
+    x = synth.activations(synth.PAGE, 5000, 0, n_tok)
+    xd = to_torch_bf16(x)
+    stream = torch.cuda.Stream()
+
+    def once():
+        ys = torch.empty((n_layers, n_tok, synth.PAGE.H), dtype=torch.bfloat16, device="cuda")
+        with torch.cuda.stream(stream):
+            for t in range(n_tok):
+                for l, layer in enumerate(layers):
+                    layer.forward(xd[t:t + 1], ys[l, t:t + 1], stream=stream)
+                if t % 2 == 1:
+                    stream.synchronize()
+        torch.cuda.synchronize()
+        return ys
+
+    ref = once()
+    for layer in layers:
+        layer.configure(slots)
+        layer.set_miss_service(0)
+        layer.set_wait_timeout_ns(500_000_000)
+    codes = []
+    for run_no in range(10):
+        for layer in layers:
+            layer.configure(slots)
+        ys = once()
+        st = [layer.stats() for layer in layers]
+        codes.append([c for _, c in st])
+        assert all(c == 0 for c in codes[-1]), (run_no, codes[-1])
+        assert torch.equal(ys.view(torch.int16), ref.view(torch.int16)), run_no
+        assert sum(s["misses"] for s, _ in st) > 0
+    for layer in layers:
+        layer.close()
