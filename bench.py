@@ -297,10 +297,27 @@ class StackBench:
                 s.device = torch.device("cuda", torch.cuda.current_device())
 
         self.st = _Stack(layers)
+        self.st.link()  # each layer warms L2 with the next layer's router rows and shared expert
         self.stream = torch.cuda.Stream()
         self.xin = torch.empty((1, H), dtype=torch.bfloat16, device="cuda")
         self.bufs = self.st.buffers(1)
         self.graph = None
+
+    def hot_lists(self, x_dev, n_tok, n_hot):
+        """Each layer's n_hot most-selected experts over n_tok tokens of an
+        eager, every-expert-resident pass (a hot-expert profile)."""
+        torch = self.torch
+        self.configure(E, 1)
+        rec = self.st.buffers(1, record=True)
+        counts = torch.zeros((len(self.layers), E), dtype=torch.int64, device="cuda")
+        ones = torch.ones((len(self.layers), K), dtype=torch.int64, device="cuda")
+        with torch.cuda.stream(self.stream):
+            for t in range(n_tok):
+                self.xin.copy_(x_dev[t:t + 1], non_blocking=True)
+                self.st.forward(self.xin, rec, self.stream)
+                counts.scatter_add_(1, rec["idx"].reshape(len(self.layers), -1).long(), ones)
+        torch.cuda.synchronize()
+        return [np.argsort(-c, kind="stable")[:n_hot].astype(np.int32).tolist() for c in counts.cpu().numpy()]
 
     def configure(self, n_slots, service=1):
         for layer in self.layers:
@@ -379,6 +396,8 @@ def decode_launch_time(torch, layers, x_dev, tokens):
     resident layers round-robin (inputs > L2), one fused kernel per call."""
     stream = torch.cuda.Stream()
     y = torch.empty((tokens, H), dtype=torch.bfloat16, device="cuda")
+    for i, layer in enumerate(layers):  # the call after layer i's is layer i + 1's
+        layer.set_next(layers[(i + 1) % len(layers)])
 
     def step():
         for t in range(tokens):
@@ -531,6 +550,9 @@ def run_default(args):
     x_pin = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).pin_memory()
     x_dev = x_pin.to("cuda")
     sb = StackBench(torch, layers)
+    if args.hot > 0:
+        # each layer also warms the next layer's hot experts (profile of the warm-up tokens)
+        sb.st.link(sb.hot_lists(x_dev, WARM_TOKENS, args.hot))
 
     def barrier():
         if pg:
@@ -592,6 +614,8 @@ def run_default(args):
 
     ms_res, ms_pool, e2e_ms = max_over_ranks([ms_res, ms_pool, e2e_ms], pg, device="cuda")
     if rank != 0:
+        for l in layers:
+            l.set_next(None)
         for l in layers + wide:
             l.close()
         pg.destroy_process_group() if pg else None
@@ -610,7 +634,9 @@ def run_default(args):
         "data": "synthetic",
         "config": {"workload": STACK_WORKLOAD, "layers": N_LAYERS, "slots_per_layer": POOL_SLOTS,
                    "tokens_per_step": WINDOW_TOKENS, "warmup_tokens_per_step": WARM_TOKENS,
-                   "l2": "inputs larger than L2 (43.5 GB of expert weights)", "parallelism": f"replicas x{ws}"},
+                   "l2": "inputs larger than L2 (43.5 GB of expert weights)", "parallelism": f"replicas x{ws}",
+                   "next_layer_l2_warmup": "router rows + shared expert" + (f" + {args.hot} hot experts from a "
+                                                                            "64-token profile" if args.hot else "")},
         "roofline": {"bound": "hbm", "kernel": "decode_kernel (fused router + top-k + hit check + gate/up + down), "
                                                "resident stack", "achieved": achieved, "peak": pk["hbm_gbs"],
                      "unit": "GB/s", "frac": achieved / pk["hbm_gbs"], "peak_kind": pk["kind"],
@@ -646,6 +672,8 @@ def run_default(args):
     if ws == 1 and args.cpu_sample:
         line["cpu_baseline"] = cpu_baseline(sample)
     print(json.dumps(line), flush=True)
+    for l in layers:
+        l.set_next(None)
     for l in layers + wide:
         l.close()
     if pg:
@@ -679,6 +707,8 @@ def run_single(args):
         out = c5_prefill(torch, layers[0], x_dev)
     print(json.dumps(out), flush=True)
     for l in layers:
+        l.set_next(None)
+    for l in layers:
         l.close()
 
 
@@ -693,6 +723,7 @@ def main():
                     help="stack: the 48-layer stack with every configuration (default); decode: one page-scale "
                          "layer, batch 1; prefill: one 4096-token chunk; batched: calls of --batch tokens")
     ap.add_argument("--batch", type=int, default=8, help="tokens per call for --workload batched (2..64)")
+    ap.add_argument("--hot", type=int, default=0, help="hot experts per layer the previous layer warms in L2")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -87,7 +87,25 @@ typedef struct {
   const float* router_bias;/* device, fp32 [E] (per-expert logit bias), or NULL for none; caller-owned */
   const uint8_t* experts;  /* host, E canonical blobs back to back; read during create only */
   const uint8_t* shared;   /* host, one canonical blob, or NULL when n_shared == 0; read during create only */
+  int32_t weight_format;   /* MOE_FMT_LINEAR4 (0) or MOE_FMT_CODEBOOK4 (1), for every blob of the layer */
 } moe_layer_desc_t;
+
+/*
+ * Weight formats.  Both store, per matrix, the nibble plane and the scale
+ * plane described above (one fp16 scale d per block of 32 along K); they
+ * differ in what a stored nibble u means:
+ *   MOE_FMT_LINEAR4    weight = d * (u - 8)
+ *   MOE_FMT_CODEBOOK4  weight = d * C[u], C = {-127, -90, -69, -53, -39, -27,
+ *                      -16, -5, 5, 16, 27, 39, 53, 69, 90, 127}: the standard
+ *                      normal distribution's quantiles at (u + 1/2) / 16
+ *                      scaled to +-127 and rounded, a non-linear 16-entry
+ *                      table per block scale (halogen-flash-server README,
+ *                      section "Bring your own GGUF", lists such lookup
+ *                      formats).  Runs on the fused decode kernel only
+ *                      (max_tokens <= 8); its lookups cost more issue slots
+ *                      than the linear format's arithmetic decode.
+ */
+enum { MOE_FMT_LINEAR4 = 0, MOE_FMT_CODEBOOK4 = 1 };
 
 /* Bytes of one expert blob (canonical and repacked sizes are equal). */
 MOE_API size_t moe_expert_bytes(int32_t hidden, int32_t inter);
@@ -113,8 +131,9 @@ MOE_API moe_status_t moe_unpack_expert(const uint8_t* gpu_layout, int32_t hidden
  * copy (the source of slot copies), uploads the shared expert, and
  * allocates the layer's device scratch.  The layer has no expert slots
  * until moe_slot_pool_configure.
- * Errors: INVALID_ARG (NULL/out-of-range fields), UNSUPPORTED (qblock != 32
- * or shapes this build does not implement), OUT_OF_MEMORY, CUDA.
+ * Errors: INVALID_ARG (NULL/out-of-range fields, unknown weight format),
+ * UNSUPPORTED (qblock != 32, shapes this build does not implement, or the
+ * codebook format with max_tokens > 8), OUT_OF_MEMORY, CUDA.
  * On error *out is NULL and nothing stays allocated.
  */
 MOE_API moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out);
@@ -275,6 +294,27 @@ enum { MOE_MISS_COPY_ENGINE = 0, MOE_MISS_SM_PULL = 1 };
 MOE_API moe_status_t moe_set_miss_service(moe_layer_t* layer, int32_t mode);
 
 /*
+ * Name the layer that runs after this one (the next layer of a stack, or
+ * the next layer object a caller cycles to), so that every later fused
+ * decode call of `layer` (T <= 8) spends the end of its run, when its own
+ * weights are consumed and HBM would idle, warming L2 with what the next
+ * layer's call loads first: its router rows and shared expert, and the
+ * listed experts (hot_experts[0 .. n_hot), e.g. a hot-expert profile, the
+ * Betelgeuse news page's section 机制) where they are resident in the next
+ * layer's slots.  A cache hint only: outputs, routing and the pool's
+ * decisions never depend on it; a listed expert that is not selected costs
+ * its bytes of HBM traffic.  next = NULL (and n_hot = 0) removes the link.
+ * next must have the layer's shapes and device, and must stay alive while
+ * linked; the addresses it warms are those of next's configuration at each
+ * call (a CUDA graph keeps those it was captured with: capture again after
+ * reconfiguring next).  Synchronizes the device.
+ * Errors: INVALID_ARG (null layer, mismatched next, n_hot outside 0..64,
+ * an expert out of range), CUDA.
+ */
+MOE_API moe_status_t moe_set_next_layer(moe_layer_t* layer, moe_layer_t* next, const int32_t* hot_experts,
+                                        int32_t n_hot);
+
+/*
  * Host-side fault injection for tests (no GPU fault is ever raised):
  *   fail_copy_n > 0: the n-th copy (counted from 1 after this call) is not
  *                    issued; it is reported to the device as failed, which
@@ -296,7 +336,7 @@ MOE_API void moe_destroy(moe_layer_t* layer);
  * k, writing topk_idx [T][k] (int32) and topk_w [T][k] (fp32), on the
  * current device and the given stream.
  *   router_w: device fp32 [E][H], 16-byte aligned; router_bias: device fp32
- *   [E] or NULL; x_bf16: device bf16 [T][H].
+ *   [E] or NULL; x_bf16: device bf16 [T][H], 16-byte aligned.
  * The logits are the compensated ones of moe_forward, computed in the same
  * order, so the selection and weights are bit-identical to its routing.
  * Scratch: a fixed 512 KiB device array inside the library (T * E <= 65536

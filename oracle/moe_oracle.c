@@ -89,8 +89,20 @@ static uint16_t double_to_bf16(double v) {
 /* Bytes of one R x K packed matrix: nibble plane then scale plane. */
 static int64_t matrix_bytes(int64_t R, int64_t K) { return R * (K / 2) + R * (K / 32) * 2; }
 
-/* Dequantize row r of an R x K packed matrix into out[K]. */
-static void dequant_row(const uint8_t* mat, int64_t R, int64_t K, int64_t r, double* out) {
+/*
+ * Weight formats (the stored 4-bit value u of an element and its block's
+ * fp16 scale d give the weight):
+ *   0  linear:   w = d * (u - 8)
+ *   1  codebook: w = d * C[u], C the 16 levels below: the standard normal
+ *      distribution's quantiles at (u + 1/2) / 16, scaled so that the
+ *      outermost is 127, rounded to integers (a non-linear 16-entry table
+ *      per block scale, the kind of format the halogen-flash-server README
+ *      lists under "Bring your own GGUF").
+ */
+static const double kLevels[16] = {-127, -90, -69, -53, -39, -27, -16, -5, 5, 16, 27, 39, 53, 69, 90, 127};
+
+/* Dequantize row r of an R x K packed matrix of format fmt into out[K]. */
+static void dequant_row(const uint8_t* mat, int64_t R, int64_t K, int64_t r, int fmt, double* out) {
   const uint8_t* nib = mat + r * (K / 2);
   const uint8_t* sc = mat + R * (K / 2) + r * (K / 32) * 2;
   for (int64_t c = 0; c < K; ++c) {
@@ -98,14 +110,17 @@ static void dequant_row(const uint8_t* mat, int64_t R, int64_t K, int64_t r, dou
     uint16_t d16 = (uint16_t)(sc[2 * blk] | (sc[2 * blk + 1] << 8));
     uint8_t byte = nib[c / 2];
     int u = (c % 2 == 0) ? (byte & 15) : (byte >> 4);
-    out[c] = half_to_double(d16) * (double)(u - 8);
+    out[c] = half_to_double(d16) * (fmt == 1 ? kLevels[u] : (double)(u - 8));
   }
 }
 
 /* Whole matrix, row-major R x K, for tests. */
-void oracle_dequant_matrix(const uint8_t* mat, int64_t R, int64_t K, double* out) {
-  for (int64_t r = 0; r < R; ++r) dequant_row(mat, R, K, r, out + r * K);
+void oracle_dequant_matrix(const uint8_t* mat, int64_t R, int64_t K, int64_t fmt, double* out) {
+  for (int64_t r = 0; r < R; ++r) dequant_row(mat, R, K, r, (int)fmt, out + r * K);
 }
+
+/* The codebook of format 1, for tests. */
+void oracle_levels(double* out) { memcpy(out, kLevels, sizeof(kLevels)); }
 
 int64_t oracle_expert_bytes(int64_t H, int64_t I) { return 3 * matrix_bytes(I, H); }
 
@@ -172,10 +187,11 @@ double oracle_topk(int64_t E, int64_t k, const double* l, int32_t* idx, double* 
 
 /*
  * One expert on one token: y[H] = W_d (silu(W_g x) * (W_u x)).
- * blob = canonical expert [W_g I x H][W_u I x H][W_d H x I].
+ * blob = canonical expert [W_g I x H][W_u I x H][W_d H x I] in weight format fmt.
  * h_out (optional) receives the I intermediate values.
  */
-void oracle_expert(const uint8_t* blob, int64_t H, int64_t I, const double* x, double* y, double* h_out) {
+void oracle_expert(const uint8_t* blob, int64_t H, int64_t I, int64_t fmt, const double* x, double* y,
+                   double* h_out) {
   const uint8_t* Wg = blob;
   const uint8_t* Wu = blob + matrix_bytes(I, H);
   const uint8_t* Wd = blob + 2 * matrix_bytes(I, H);
@@ -183,15 +199,15 @@ void oracle_expert(const uint8_t* blob, int64_t H, int64_t I, const double* x, d
   double* h = (double*)malloc((size_t)I * sizeof(double));
   for (int64_t i = 0; i < I; ++i) {
     double g = 0.0, u = 0.0;
-    dequant_row(Wg, I, H, i, row);
+    dequant_row(Wg, I, H, i, (int)fmt, row);
     for (int64_t c = 0; c < H; ++c) g += row[c] * x[c];
-    dequant_row(Wu, I, H, i, row);
+    dequant_row(Wu, I, H, i, (int)fmt, row);
     for (int64_t c = 0; c < H; ++c) u += row[c] * x[c];
     h[i] = g / (1.0 + exp(-g)) * u;
   }
   for (int64_t r = 0; r < H; ++r) {
     double s = 0.0;
-    dequant_row(Wd, H, I, r, row);
+    dequant_row(Wd, H, I, r, (int)fmt, row);
     for (int64_t i = 0; i < I; ++i) s += row[i] * h[i];
     y[r] = s;
   }
@@ -212,10 +228,11 @@ void oracle_expert(const uint8_t* blob, int64_t H, int64_t I, const double* x, d
  *            choice (weights still from the logits); for cases where the
  *            router's decision is a near-tie that another summation order
  *            may legitimately resolve the other way.
+ *   fmt:     weight format of every blob (0 linear, 1 codebook)
  */
 void oracle_moe_forward(int64_t H, int64_t I, int64_t E, int64_t k, const float* W_r, const float* bias,
                         const uint8_t* experts, const uint8_t* shared, const uint16_t* x, int64_t T, double* y,
-                        int32_t* idx, double* w, double* logits, double* gap, const int32_t* force) {
+                        int32_t* idx, double* w, double* logits, double* gap, const int32_t* force, int64_t fmt) {
   const int64_t eb = oracle_expert_bytes(H, I);
   double* l = (double*)malloc((size_t)(T * E) * sizeof(double));
   double* xd = (double*)malloc((size_t)H * sizeof(double));
@@ -239,11 +256,11 @@ void oracle_moe_forward(int64_t H, int64_t I, int64_t E, int64_t k, const float*
     double* yt = y + t * H;
     for (int64_t c = 0; c < H; ++c) yt[c] = 0.0;
     for (int64_t j = 0; j < k; ++j) {
-      oracle_expert(experts + (int64_t)it[j] * eb, H, I, xd, ye, NULL);
+      oracle_expert(experts + (int64_t)it[j] * eb, H, I, fmt, xd, ye, NULL);
       for (int64_t c = 0; c < H; ++c) yt[c] += wt[j] * ye[c];
     }
     if (shared) {
-      oracle_expert(shared, H, I, xd, ye, NULL);
+      oracle_expert(shared, H, I, fmt, xd, ye, NULL);
       for (int64_t c = 0; c < H; ++c) yt[c] += ye[c];
     }
   }

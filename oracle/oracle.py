@@ -13,14 +13,15 @@ def lib():
     if _lib is None:
         _lib = C.CDLL(_build.build())
         i64, p = C.c_int64, C.c_void_p
-        _lib.oracle_dequant_matrix.argtypes = [p, i64, i64, p]
+        _lib.oracle_dequant_matrix.argtypes = [p, i64, i64, i64, p]
+        _lib.oracle_levels.argtypes = [p]
         _lib.oracle_expert_bytes.argtypes = [i64, i64]
         _lib.oracle_expert_bytes.restype = i64
         _lib.oracle_router_logits.argtypes = [i64, i64, p, p, p, i64, p]
         _lib.oracle_topk.argtypes = [i64, i64, p, p, p, p]
         _lib.oracle_topk.restype = C.c_double
-        _lib.oracle_expert.argtypes = [p, i64, i64, p, p, p]
-        _lib.oracle_moe_forward.argtypes = [i64, i64, i64, i64, p, p, p, p, p, i64, p, p, p, p, p, p]
+        _lib.oracle_expert.argtypes = [p, i64, i64, i64, p, p, p]
+        _lib.oracle_moe_forward.argtypes = [i64, i64, i64, i64, p, p, p, p, p, i64, p, p, p, p, p, p, i64]
         _lib.oracle_rmsnorm.argtypes = [i64, p, C.c_double, p, p]
         _lib.oracle_residual.argtypes = [i64, p, p, p]
         _lib.oracle_to_bf16.argtypes = [i64, p, p]
@@ -41,11 +42,18 @@ def expert_bytes(H, I):
     return int(lib().oracle_expert_bytes(H, I))
 
 
-def dequant_matrix(mat, R, K):
-    """R x K float64 weights of one packed matrix (nibble plane + scale plane)."""
+def dequant_matrix(mat, R, K, fmt=0):
+    """R x K float64 weights of one packed matrix (nibble plane + scale plane) of weight format fmt."""
     mat = _c(mat, np.uint8)
     out = np.empty((R, K), np.float64)
-    lib().oracle_dequant_matrix(_ptr(mat), R, K, _ptr(out))
+    lib().oracle_dequant_matrix(_ptr(mat), R, K, fmt, _ptr(out))
+    return out
+
+
+def levels():
+    """The 16 levels of the codebook format (format 1)."""
+    out = np.empty(16, np.float64)
+    lib().oracle_levels(_ptr(out))
     return out
 
 
@@ -71,17 +79,17 @@ def topk(logits, k):
     return idx, w, br, gap
 
 
-def expert(blob, H, I, x):
+def expert(blob, H, I, x, fmt=0):
     """(y float64[H], h float64[I]) of one expert on float64 activations x[H]."""
     blob = _c(blob, np.uint8)
     x = _c(x, np.float64)
     y = np.empty(H, np.float64)
     h = np.empty(I, np.float64)
-    lib().oracle_expert(_ptr(blob), H, I, _ptr(x), _ptr(y), _ptr(h))
+    lib().oracle_expert(_ptr(blob), H, I, fmt, _ptr(x), _ptr(y), _ptr(h))
     return y, h
 
 
-def moe_forward(H, I, E, k, W_r, bias, experts, shared, x_bf16, force=None):
+def moe_forward(H, I, E, k, W_r, bias, experts, shared, x_bf16, force=None, fmt=0):
     """Layer on T tokens: dict(y [T,H] f64, idx [T,k], w [T,k], logits [T,E], gap [T])."""
     W_r = _c(W_r, np.float32)
     b = None if bias is None else _c(bias, np.float32)
@@ -96,7 +104,7 @@ def moe_forward(H, I, E, k, W_r, bias, experts, shared, x_bf16, force=None):
     gap = np.empty(T, np.float64)
     f = None if force is None else _c(force, np.int32).reshape(T, k)
     lib().oracle_moe_forward(H, I, E, k, _ptr(W_r), _ptr(b), _ptr(ex), _ptr(sh), _ptr(x), T, _ptr(y),
-                             _ptr(idx), _ptr(w), _ptr(logits), _ptr(gap), _ptr(f))
+                             _ptr(idx), _ptr(w), _ptr(logits), _ptr(gap), _ptr(f), fmt)
     return dict(y=y, idx=idx, w=w, logits=logits, gap=gap)
 
 

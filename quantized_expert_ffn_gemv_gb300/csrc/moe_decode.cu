@@ -100,6 +100,9 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -400,7 +403,6 @@ struct TopkScratch {
   unsigned long long* list;  // [kWarps][kListStride] each warp's best, in rank order
   unsigned long long* sel;   // [kMaxT][kMaxTopK] each token's k best, in rank order
   unsigned long long* surv;  // survivors: token t's at t * wpt * kMaxTopK (wpt warps per token, wpt * T <= kWarps)
-  unsigned long long* kth;   // [kWarps] each warp's k-th best (0: fewer than k)
   int* len;                  // [kWarps] entries in each warp's list
   int* nsurv;                // [kMaxT] survivors per token
 };
@@ -410,24 +412,22 @@ __device__ inline TopkScratch carve_topk(unsigned char* base) {
   TopkScratch s;
   s.list = reinterpret_cast<unsigned long long*>(base);
   s.sel = s.list + kWarps * kListStride;
-  s.kth = s.sel + kMaxT * kMaxTopK;
-  s.surv = s.kth + kWarps;
+  s.surv = s.sel + kMaxT * kMaxTopK;
   s.len = reinterpret_cast<int*>(s.surv + kSurvTotal);
   s.nsurv = s.len + kWarps;
   return s;
 }
 constexpr size_t kTopkScratchBytes =
-    8 * (kWarps * kListStride + kMaxT * kMaxTopK + kWarps + kSurvTotal) + 4 * (kWarps + kMaxT);
+    8 * (kWarps * kListStride + kMaxT * kMaxTopK + kSurvTotal) + 4 * (kWarps + kMaxT);
 // the shared-memory plan reserves 4 * kWarps * kMaxTopK words for it
 static_assert(kTopkScratchBytes <= (size_t)4 * kWarps * kMaxTopK * 8, "routing scratch");
 
 // Level 1: the k best of this warp's range [base, base + range) of one
-// token's experts, in rank order, into list[0..len); kth = the k-th best or
-// 0.  One key per lane: each lane's rank from 32 compares.  Several keys per
+// token's experts, in rank order, into list[0..len).  One key per lane: each lane's rank from 32 compares.  Several keys per
 // lane: k rounds of a warp maximum.
 template <int CPL>
 __device__ void warp_best(const unsigned long long* words, int E, int k, int base, int range, uint32_t tag,
-                          unsigned long long* list, unsigned long long* kth, int* len, const LayerArgs& a,
+                          unsigned long long* list, int* len, const LayerArgs& a,
                           uint64_t deadline) {
   const int lane = threadIdx.x & 31;
   uint64_t w[CPL];
@@ -445,43 +445,48 @@ __device__ void warp_best(const unsigned long long* words, int E, int k, int bas
       r += wi > w[0];
     }
     const int n = __popc(__ballot_sync(0xffffffffu, w[0] != 0ull));
-    const int nl = n < k ? n : k;
     if (w[0] != 0ull && r < k) list[r] = w[0];
-    if (lane == 0) {
-      len[0] = nl;
-      if (n < k) kth[0] = 0ull;
-    }
-    if (n >= k && r == k - 1) kth[0] = w[0];
+    if (lane == 0) len[0] = n < k ? n : k;
     return;
   }
   uint32_t taken = 0u;
   int nl = 0;
-  uint64_t m = 0ull;
   for (int r = 0; r < k; ++r) {
     uint64_t my = 0ull;
     int myj = -1;
 #pragma unroll
     for (int j = 0; j < CPL; ++j)
       if (!((taken >> j) & 1u) && w[j] > my) { my = w[j]; myj = j; }
-    m = warp_max_u64(my);
+    const uint64_t m = warp_max_u64(my);
     if (m == 0ull) break;
     if (my == m) taken |= 1u << myj;  // words are distinct: one lane wins
     if (lane == 0) list[r] = m;
     ++nl;
   }
-  if (lane == 0) {
-    len[0] = nl;
-    kth[0] = nl == k ? m : 0ull;
-  }
+  if (lane == 0) len[0] = nl;
 }
 
-// Level 2, step 1 (warp w of token t's wpt warps): the entries of list w
-// that are not below the best k-th of the token's warps (any selected
-// expert is among them) are appended to the token's survivors.
-__device__ __forceinline__ void keep_survivors(const TopkScratch& S, int t, int w, int wpt) {
+// Level 2, step 1 (warp w of token t's wpt warps): a threshold beta with at
+// least k of the token's keys at or above it, the k-th best of the top
+// 32 / wpt entries of each of the token's lists (32 keys, one per lane; each
+// warp computes it, no barrier); the entries of list w not below beta (every
+// selected expert is among them) are appended to the token's survivors.
+__device__ __forceinline__ void keep_survivors(const TopkScratch& S, int t, int w, int wpt, int k) {
   const int lane = threadIdx.x & 31;
-  const uint64_t kv = lane < wpt ? S.kth[t * wpt + lane] : 0ull;
-  const uint64_t beta = warp_max_u64(kv);
+  const int m = 32 / wpt, li = t * wpt + lane / m, ei = lane % m;
+  const uint64_t v = ei < S.len[li] ? S.list[li * kListStride + ei] : 0ull;
+  int r = 0;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const uint64_t vi = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(v >> 32), i) << 32) |
+                        __shfl_sync(0xffffffffu, (uint32_t)v, i);
+    r += vi > v;
+  }
+  const unsigned kb = __ballot_sync(0xffffffffu, v != 0ull && r == k - 1);
+  const int src = kb ? __ffs(kb) - 1 : 0;
+  uint64_t beta = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(v >> 32), src) << 32) |
+                  __shfl_sync(0xffffffffu, (uint32_t)v, src);
+  if (!kb) beta = 0ull;  // fewer than k keys in the sample: keep every entry
   const int n = S.len[w];
   const uint64_t e = lane < n ? S.list[w * kListStride + lane] : 0ull;
   const bool keep = e != 0ull && e >= beta;
@@ -553,13 +558,21 @@ __device__ __forceinline__ void finish_topk(unsigned long long* sel, int k, cons
 
 // ------------------------------------------------------------------ the kernel
 
+// ONE: the variant for one token with every expert resident and at most
+// 512 experts (the decode of a resident stack), compiled without the batch
+// loops, the slot-pool code and the wider top-k shapes so that the code one
+// launch runs stays small.
+template <bool ONE>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsigned long long* tagged_logits,
                                                              int32_t* pool_state, size_t smem_limit) {
   extern __shared__ __align__(128) unsigned char sm[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int G = gridDim.x, c = blockIdx.x;
-  const int H = a.H, I = a.I, E = a.E, k = a.k, T = a.T, NS = I / 16, NSh = a.n_shared;
+  const int H = a.H, I = a.I, E = a.E, k = a.k, T = ONE ? 1 : a.T, NS = I / 16, NSh = a.n_shared;
+  // weight format (the one-token variant serves the linear format only)
+  const int fmt = ONE ? 0 : a.fmt;
+  const uint32_t lut = fmt == 1 ? codebook_lut(threadIdx.x & 31) : 0u;
   const Plan PL = make_plan(H, I, E, k, T, G, smem_limit);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PL.bars);
   Ring R;
@@ -761,14 +774,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     const int xi = t_gu / NS, strip = t_gu % NS;
     const Task tk = task_of(a, L, xi, NSh);
     const int col_tok = (g < tk.cnt) ? (xi < NSh ? g : L.pair_token[tk.poff + g]) : 0;
-    if (tk.src) {  // a missed expert read from host memory by this group
+    if (!ONE && tk.src) {  // a missed expert read from host memory by this group
       const size_t off = (size_t)strip * R.gu_bytes;
       pull_strip(tk.src + off, const_cast<uint8_t*>(tk.base) + off, R.gu + s * R.gu_pitch, R.gu_bytes,
                  wg * 32 + lane, kGroupWarps * 32);
       named_sync(1 + grp, kGroupWarps * 32);
       if (wg == 0 && lane == 0) mbar_arrive(&R.full_gu[s]);
     }
-    const bool ok = wait_full(&R.full_gu[s], (m / R.gs) & 1, deadline, is_prod, P, X);
+    // warp-uniform: the codebook dequantization shuffles across all 32 lanes
+    const bool ok = __all_sync(0xffffffffu, wait_full(&R.full_gu[s], (m / R.gs) & 1, deadline, is_prod, P, X));
     float accg[4] = {0.f, 0.f, 0.f, 0.f}, accu[4] = {0.f, 0.f, 0.f, 0.f};
     const int nst = H / 64;
     if (ok) {
@@ -781,8 +795,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         const uint2 gsc = *reinterpret_cast<const uint2*>(sb + 8 * H + st * 64 + g * 8);
         const uint4 nu4 = *reinterpret_cast<const uint4*>(sb + 9 * H + st * 512 + lane * 16);
         const uint2 usc = *reinterpret_cast<const uint2*>(sb + 17 * H + st * 64 + g * 8);
-        supertile_mma(accg, ng4, gsc, b01, b23);
-        supertile_mma(accu, nu4, usc, b01, b23);
+        supertile_mma(accg, ng4, gsc, b01, b23, fmt, lut);
+        supertile_mma(accu, nu4, usc, b01, b23, fmt, lut);
       }
     }
     __syncwarp();
@@ -824,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   // Early path (one token, every expert resident): the experts start right
   // after the selection; a warp with no gate/up or down role finishes the
   // softmax, the combine mapping and the statistics meanwhile.
-  const bool early = T == 1 && !a.pool;
+  const bool early = ONE || (T == 1 && !a.pool);
   const int fin_warp = R.gs < kMaxGuStages ? R.gs * kGroupWarps : 0;
   for (int e = tid; e < E; e += kThreads) tokmask[e] = 0ull;
   if (tid < kMaxT) TS.nsurv[tid] = 0;
@@ -841,19 +855,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     if (t < T) {
       const unsigned long long* words = tagged_logits + (size_t)t * E;
       unsigned long long* lw = TS.list + warp * kListStride;
-      if (cpl == 1)
-        warp_best<1>(words, E, k, base, range, tag, lw, TS.kth + warp, TS.len + warp, a, deadline);
+      if (ONE || cpl == 1)
+        warp_best<1>(words, E, k, base, range, tag, lw, TS.len + warp, a, deadline);
       else if (cpl <= 2)
-        warp_best<2>(words, E, k, base, range, tag, lw, TS.kth + warp, TS.len + warp, a, deadline);
+        warp_best<2>(words, E, k, base, range, tag, lw, TS.len + warp, a, deadline);
       else if (cpl <= 4)
-        warp_best<4>(words, E, k, base, range, tag, lw, TS.kth + warp, TS.len + warp, a, deadline);
+        warp_best<4>(words, E, k, base, range, tag, lw, TS.len + warp, a, deadline);
       else if (cpl <= 8)
-        warp_best<8>(words, E, k, base, range, tag, lw, TS.kth + warp, TS.len + warp, a, deadline);
+        warp_best<8>(words, E, k, base, range, tag, lw, TS.len + warp, a, deadline);
       else
-        warp_best<16>(words, E, k, base, range, tag, lw, TS.kth + warp, TS.len + warp, a, deadline);
+        warp_best<16>(words, E, k, base, range, tag, lw, TS.len + warp, a, deadline);
     }
     __syncthreads();
-    if (t < T) keep_survivors(TS, t, warp, wpt);
+    if (t < T) keep_survivors(TS, t, warp, wpt, k);
     __syncthreads();
     if (t < T) rank_survivors(TS, t, wpt, wt * 32 + lane, k);
     __syncthreads();
@@ -878,7 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       s_nunion = k;
       s_nmiss = 0;
     }
-  } else if (T == 1) {
+  } else if (!ONE && T == 1) {
     if (tid < k) {
       const int e = L.s_idx[tid];
       L.u_expert[tid] = e;
@@ -893,7 +907,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       L.u_off[k] = k;
       s_nunion = k;
     }
-  } else {
+  } else if (!ONE) {
     const int P = T * k;
     int first = 0, ue = 0, po = 0, pos = 0, e = 0, t = 0;
     if (tid < P) {
@@ -938,7 +952,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   int32_t* nxt_slot = pool_state + (size_t)((seq + 1u) & 1u) * (E + 2 * S);
   int32_t* nxt_owner = nxt_slot + E;
   uint32_t* nxt_stamp = reinterpret_cast<uint32_t*>(nxt_owner + S);
-  if (!a.pool) {
+  if (ONE || !a.pool) {
     if (tid == 0 && !early) s_nmiss = 0;  // the early path set it before the barrier above
   } else {
     // pool scratch in region A after the routing lists: per slot owner, stamp
@@ -1088,6 +1102,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   // down: warp w takes expert entries w, w + 16, ...
   float* zbuf = reinterpret_cast<float*>(sm + PL.regA);  // [xi][32 lanes][4]
   __syncthreads();  // region A holds routing scratch until here
+  // This CTA's gate/up weights are consumed and HBM idles through the rest
+  // of the layer: warm L2 with what the next layer's kernel loads first (its
+  // router rows and shared-expert strips for this CTA's index) and with this
+  // CTA's share of the next layer's listed hot experts.
+  if (a.nx_W_r && tid == kThreads - 1) {
+    if (nrows > 0) prefetch_l2(a.nx_W_r + (size_t)r0 * H, (uint32_t)(nrows * H * 4));
+    if (a.nx_shared) {
+      if (c < NS) prefetch_l2(a.nx_shared + (size_t)c * R.gu_bytes, (uint32_t)R.gu_bytes);
+      if (has_dn) prefetch_l2(a.nx_shared + down_base(H, I) + (size_t)c * R.dn_bytes, (uint32_t)R.dn_bytes);
+    }
+    const int parts = NS + H / 16;
+    const int32_t* table = nullptr;
+    if (a.nx_pool_state) {
+      const uint32_t nseq = (uint32_t)ld_cg_i32(reinterpret_cast<const int*>(&a.nx_st->step)) + 1u;
+      table = a.nx_pool_state + (size_t)(nseq & 1u) * (E + 2 * a.nx_S);
+    }
+    for (int u = c; u < a.nx_n_hot * parts; u += G) {
+      const int e = __ldg(a.nx_hot + u / parts), pt = u % parts;
+      const int slot = table ? ld_cg_i32(table + e) : e;
+      if (slot < 0) continue;
+      const uint8_t* base = a.nx_arena + (int64_t)slot * a.blob;
+      if (pt < NS)
+        prefetch_l2(base + (size_t)pt * R.gu_bytes, (uint32_t)R.gu_bytes);
+      else
+        prefetch_l2(base + down_base(H, I) + (size_t)(pt - NS) * R.dn_bytes, (uint32_t)R.dn_bytes);
+    }
+  }
   if (has_dn && warp < R.ds) {
     // warp w owns down stage w: entries w, w + ds, ... in order
     const int nst = I / 64;
@@ -1113,7 +1154,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         }
       }
       __syncwarp();
-      if (tk.src) {  // a missed expert read from host memory by this warp
+      if (!ONE && tk.src) {  // a missed expert read from host memory by this warp
         const size_t off = (size_t)down_base(H, I) + (size_t)c * R.dn_bytes;
         pull_strip(tk.src + off, const_cast<uint8_t*>(tk.base) + off, R.dn + s * R.dn_pitch, R.dn_bytes, lane, 32);
         __syncwarp();
@@ -1129,7 +1170,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         cp_async_wait_all();
         __syncwarp();
       }
-      const bool ok = wait_full(&R.full_dn[s], (xi / R.ds) & 1, deadline, is_prod, P, X);
+      const bool ok = __all_sync(0xffffffffu, wait_full(&R.full_dn[s], (xi / R.ds) & 1, deadline, is_prod, P, X));
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       if (ok) {
         const unsigned char* sb = R.dn + s * R.dn_pitch;
@@ -1142,7 +1183,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
             const uint4 b23 = *reinterpret_cast<const uint4*>(hb + st * 64 + 8);
             const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
             const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
-            supertile_mma(acc, nb, scv, b01, b23);
+            supertile_mma(acc, nb, scv, b01, b23, fmt, lut);
           }
         } else {
           const int hrow = tk.poff + gsel;
@@ -1153,7 +1194,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
             const uint4 b23 = __ldcg(reinterpret_cast<const uint4*>(hr + 8));
             const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
             const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
-            supertile_mma(acc, nb, scv, b01, b23);
+            supertile_mma(acc, nb, scv, b01, b23, fmt, lut);
           }
         }
       }
@@ -1238,10 +1279,16 @@ cudaError_t decode_configure() {
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, decode_kernel);
+  e = cudaFuncGetAttributes(&fa, decode_kernel<false>);
   if (e != cudaSuccess) return e;
-  const size_t limit = (size_t)optin - fa.sharedSizeBytes;
-  e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
+  cudaFuncAttributes fa1;
+  e = cudaFuncGetAttributes(&fa1, decode_kernel<true>);
+  if (e != cudaSuccess) return e;
+  const size_t st = fa.sharedSizeBytes > fa1.sharedSizeBytes ? fa.sharedSizeBytes : fa1.sharedSizeBytes;
+  const size_t limit = (size_t)optin - st;
+  e = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
   if (e != cudaSuccess) return e;
   g_decode_smem_limit = limit;
   // whether a cooperative launch may also carry programmatic serialization:
@@ -1283,7 +1330,10 @@ cudaError_t launch_decode(const LayerArgs& a, unsigned long long* tagged_logits,
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = decode_config(dim3(G), dim3(kThreads), decode_smem_bytes(a.H, a.I, a.E, a.k, a.T, G), s,
                                          attr, pdl);
-  return cudaLaunchKernelEx(&cfg, decode_kernel, a, tagged_logits, pool_state, g_decode_smem_limit);
+  // one token per call, linear weights: one key per lane in top-k
+  const bool one = a.T == 1 && !a.pool && a.E <= 16 * 32 && a.fmt == 0;
+  return one ? cudaLaunchKernelEx(&cfg, decode_kernel<true>, a, tagged_logits, pool_state, g_decode_smem_limit)
+             : cudaLaunchKernelEx(&cfg, decode_kernel<false>, a, tagged_logits, pool_state, g_decode_smem_limit);
 }
 
 }  // namespace moe

@@ -91,6 +91,7 @@ struct LayerArgs {
   int H, E, k, I, n_shared, T;
   int n_slots, pool;  // pool = 0: every expert resident at slot == expert index
   int pull;           // pooled misses: 0 = host copy server, 1 = read by the kernel from the mapped master copy
+  int fmt;            // weight format: 0 linear 4-bit, 1 codebook (fused decode kernel only)
   const uint8_t* master;  // device address of the pinned host master copy (GPU layout, expert e at e * blob)
   const float* W_r;
   const float* bias;
@@ -126,7 +127,19 @@ struct LayerArgs {
   unsigned long long wait_timeout_ns;
   uint32_t* counters;   // [2][cnt_stride] gate/up completion counts, by step parity
   int cnt_stride;       // max distinct experts per call + 2
+  // L2 warm-up for the layer that runs next (moe_set_next_layer): its router
+  // rows and shared expert, and the listed experts in its resident slots.
+  // A cache hint only: results never depend on it.  nx_W_r null = none.
+  const float* nx_W_r;
+  const uint8_t* nx_shared;
+  const uint8_t* nx_arena;        // next layer's slot arena
+  const int32_t* nx_pool_state;   // next layer's double-buffered slot tables, or null (all resident: slot = e)
+  const DevState* nx_st;          // next layer's state (its step picks the current table)
+  int nx_S;                       // next layer's slot count
+  const int32_t* nx_hot;          // device [nx_n_hot] expert ids
+  int nx_n_hot;
 };
+constexpr int kMaxHotExperts = 64;
 
 // Launch helpers (moe_kernels.cu).  All return cudaSuccess or the launch error.
 cudaError_t launch_route(const LayerArgs& a, cudaStream_t s, bool pdl);

@@ -263,12 +263,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(LayerArgs a) {
   for (int t0 = 0; t0 < T; t0 += kRouteChunk) {
     const int nt = min(kRouteChunk, T - t0);
     __syncthreads();
-    const uint32_t* xsrc = reinterpret_cast<const uint32_t*>(a.x + (size_t)t0 * H);
-    for (int i = tid; i < nt * H / 2; i += kRouteThreads) {
-      const uint32_t v = xsrc[i];
-      xs[2 * i] = __uint_as_float(v << 16);
-      xs[2 * i + 1] = __uint_as_float(v & 0xFFFF0000u);
-    }
+    stage_x_f32<kRouteThreads>(a.x + (size_t)t0 * H, nt * H, xs, tid);
     __syncthreads();
     for (int tt = 0; tt < nt; ++tt) {
       // the canonical compensated order (moe_route.cuh): lane-strided float4
@@ -309,7 +304,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(LayerArgs a) {
 
 constexpr int kGuThreads = 128;  // 4 warps split the K = H reduction of a strip, as in the fused path
 constexpr int kGuWarpsPerTask = kGuThreads / 32;
-constexpr int kGuBatch = 4;      // super-tiles per warp with loads in flight together
+constexpr int kGuBatch = 2;      // super-tiles per warp with loads in flight together
 
 template <int NG>
 __global__ void __launch_bounds__(kGuThreads) gateup_kernel(LayerArgs a) {
@@ -363,23 +358,34 @@ __global__ void __launch_bounds__(kGuThreads) gateup_kernel(LayerArgs a) {
       for (int b = 0; b < kGuBatch; ++b) {
         const int st = st0 + kGuWarpsPerTask * b;
         if (st < nst) {
-          ngw[b] = ld_cg4(strip + st * 512 + lane * 16);
-          gsc[b] = ld_cg2(strip + 8 * H + st * 64 + g * 8);
-          nuw[b] = ld_cg4(strip + 9 * H + st * 512 + lane * 16);
-          usc[b] = ld_cg2(strip + 17 * H + st * 64 + g * 8);
+          ngw[b] = __ldcg(reinterpret_cast<const uint4*>(strip + st * 512 + lane * 16));
+          gsc[b] = __ldcg(reinterpret_cast<const uint2*>(strip + 8 * H + st * 64 + g * 8));
+          nuw[b] = __ldcg(reinterpret_cast<const uint4*>(strip + 9 * H + st * 512 + lane * 16));
+          usc[b] = __ldcg(reinterpret_cast<const uint2*>(strip + 17 * H + st * 64 + g * 8));
         }
       }
 #pragma unroll
       for (int b = 0; b < kGuBatch; ++b) {
         const int st = st0 + kGuWarpsPerTask * b;
         if (st < nst) {
+          // every token group's activation fragments first (plain loads the
+          // compiler may overlap), then the weights dequantized once and
+          // multiplied against each group
+          uint4 bx[NG][2];
+#pragma unroll
+          for (int q = 0; q < NG; ++q)
+            if (q < ng) {
+              const uint4* xr = reinterpret_cast<const uint4*>(a.x16 + (size_t)tok[q] * H + st * 64 + t4 * 16);
+              bx[q][0] = __ldcg(xr);
+              bx[q][1] = __ldcg(xr + 1);
+            }
+          const SupertileA ag = dequant_supertile(ngw[b], gsc[b]);
+          const SupertileA au = dequant_supertile(nuw[b], usc[b]);
 #pragma unroll
           for (int q = 0; q < NG; ++q) {
             if (q < ng) {
-              const __half* xr = a.x16 + (size_t)tok[q] * H + st * 64 + t4 * 16;
-              const uint4 b01 = ld_cg4(xr), b23 = ld_cg4(xr + 8);
-              supertile_mma(accg[q], ngw[b], gsc[b], b01, b23);
-              supertile_mma(accu[q], nuw[b], usc[b], b01, b23);
+              supertile_mma_pre(accg[q], ag, bx[q][0], bx[q][1]);
+              supertile_mma_pre(accu[q], au, bx[q][0], bx[q][1]);
             }
           }
         }
@@ -417,15 +423,19 @@ __global__ void __launch_bounds__(kGuThreads) gateup_kernel(LayerArgs a) {
 
 // ------------------------------------------------------------------ down + combine
 
-constexpr int kDnThreads = 512;  // 16 warps, one expert each per batch
+constexpr int kDnThreads = 256;  // 8 warps, one expert each per batch
 constexpr int kDnWarps = kDnThreads / 32;
-constexpr int kDnBatch = 8;      // super-tiles with loads in flight together
+constexpr int kDnBatch1 = 8;     // super-tiles with loads in flight together (one token group)
+constexpr int kDnBatch8 = 2;     // the same with eight token groups (registers)
 
 template <int NG>
 __global__ void __launch_bounds__(kDnThreads) down_kernel(LayerArgs a) {
   extern __shared__ __align__(16) float dsm[];
-  float* zbuf = dsm;                                   // [16 warps][NG][32 lanes][4]
+  float* zbuf = dsm;                                   // [warps][NG][32 lanes][4]
   float* yacc = dsm + kDnWarps * NG * 32 * 4;          // [T][16]
+  int* m_u = reinterpret_cast<int*>(yacc + a.T * 16);  // [T][k] union index of (t, j)
+  int* m_pos = m_u + a.T * a.k;                        // [T][k] its place among the expert's pairs
+  float* m_w = reinterpret_cast<float*>(m_pos + a.T * a.k);  // [T][k] routing weight
   pdl_wait();
   pdl_trigger();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -434,6 +444,14 @@ __global__ void __launch_bounds__(kDnThreads) down_kernel(LayerArgs a) {
   const int n_union = ld_cg_i32(&a.st->n_union);
   const int n_ex = n_union + a.n_shared;
   const int nst = I / 64;
+  // the combine's per-pair metadata, read once
+  for (int i = tid; i < T * k; i += kDnThreads) {
+    m_u[i] = __ldcg(a.tk_u + i);
+    m_pos[i] = __ldcg(a.tk_pos + i);
+    m_w[i] = __ldcg(a.topk_w + i);
+  }
+  __syncthreads();
+  constexpr int kDnBatch = NG > 1 ? kDnBatch8 : kDnBatch1;
   for (int r = blockIdx.x; r < H / 16; r += gridDim.x) {
     for (int q = tid; q < T * 16; q += kDnThreads) yacc[q] = 0.f;
     for (int b0 = 0; b0 < n_ex; b0 += kDnWarps) {
@@ -469,21 +487,26 @@ __global__ void __launch_bounds__(kDnThreads) down_kernel(LayerArgs a) {
           for (int b = 0; b < kDnBatch; ++b) {
             const int st = st0 + b;
             if (st < nst) {
-              nw[b] = ld_cg4(strip + st * 512 + lane * 16);
-              sc[b] = ld_cg2(strip + 8 * I + st * 64 + g * 8);
+              nw[b] = __ldcg(reinterpret_cast<const uint4*>(strip + st * 512 + lane * 16));
+              sc[b] = __ldcg(reinterpret_cast<const uint2*>(strip + 8 * I + st * 64 + g * 8));
             }
           }
 #pragma unroll
           for (int b = 0; b < kDnBatch; ++b) {
             const int st = st0 + b;
             if (st < nst) {
+              uint4 bh[NG][2];  // every group's h fragments first, then the products
 #pragma unroll
-              for (int q = 0; q < NG; ++q) {
+              for (int q = 0; q < NG; ++q)
                 if (q < ng) {
-                  const __half* hr = a.h16 + (size_t)hrow[q] * I + st * 64 + t4 * 16;
-                  supertile_mma(acc[q], nw[b], sc[b], ld_cg4(hr), ld_cg4(hr + 8));
+                  const uint4* hr = reinterpret_cast<const uint4*>(a.h16 + (size_t)hrow[q] * I + st * 64 + t4 * 16);
+                  bh[q][0] = __ldcg(hr);
+                  bh[q][1] = __ldcg(hr + 1);
                 }
-              }
+              const SupertileA ad = dequant_supertile(nw[b], sc[b]);  // once for every token group
+#pragma unroll
+              for (int q = 0; q < NG; ++q)
+                if (q < ng) supertile_mma_pre(acc[q], ad, bh[q][0], bh[q][1]);
             }
           }
         }
@@ -498,12 +521,12 @@ __global__ void __launch_bounds__(kDnThreads) down_kernel(LayerArgs a) {
         const int t = q >> 4, row = q & 15;
         float v = yacc[q];
         for (int j = 0; j < k; ++j) {
-          const int u = ld_cg_i32(&a.tk_u[t * k + j]);
+          const int u = m_u[t * k + j];
           if (u >= b0 && u < b0 + kDnWarps) {
-            const int pos = ld_cg_i32(&a.tk_pos[t * k + j]);
+            const int pos = m_pos[t * k + j];
             const int grp = pos >> 3, col = pos & 7;
             const int lz = (row & 7) * 4 + (col >> 1), rz = (row >> 3) * 2 + (col & 1);
-            v = fmaf(ld_cg_f32(&a.topk_w[t * k + j]), zbuf[(((u - b0) * NG + grp) * 32 + lz) * 4 + rz], v);
+            v = fmaf(m_w[t * k + j], zbuf[(((u - b0) * NG + grp) * 32 + lz) * 4 + rz], v);
           }
         }
         if (a.n_shared && n_union >= b0 && n_union < b0 + kDnWarps) {
@@ -572,7 +595,7 @@ cudaError_t launch(K kernel, int grid, int block, size_t smem, cudaStream_t s, b
 }
 
 size_t gateup_smem(int NG) { return sizeof(float) * kGuWarpsPerTask * NG * 32 * 8; }
-size_t down_smem(int NG, int T) { return sizeof(float) * (kDnWarps * NG * 32 * 4 + T * 16); }
+size_t down_smem(int NG, int T) { return sizeof(float) * (kDnWarps * NG * 32 * 4 + T * 16 + 3 * T * kMaxTopK); }
 
 }  // namespace
 

@@ -197,6 +197,9 @@ struct moe_layer {
   uint64_t wait_timeout_ns = 2000000000ull;
   unsigned long long* tagged_logits = nullptr;  // fused kernel: [T][E] (step << 32 | logit bits)
   int32_t* pool_state = nullptr;           // fused kernel: double-buffered slot table
+  moe_layer* next = nullptr;               // the layer whose weights calls warm in L2 (moe_set_next_layer)
+  int32_t* hot_dev = nullptr;              // [kMaxHotExperts] next layer's experts to warm
+  int32_t n_hot = 0;
 };
 
 namespace {
@@ -407,6 +410,8 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   if (d.max_tokens > kMaxTokens && d.hidden % 128) return MOE_ERR_UNSUPPORTED;  // prefill M-blocks of 128 rows
   if (d.n_shared != 0 && d.n_shared != 1) return MOE_ERR_UNSUPPORTED;
   if (!d.router_w || !d.experts || (d.n_shared && !d.shared)) return MOE_ERR_INVALID_ARG;
+  if (d.weight_format != MOE_FMT_LINEAR4 && d.weight_format != MOE_FMT_CODEBOOK4) return MOE_ERR_INVALID_ARG;
+  if (d.weight_format == MOE_FMT_CODEBOOK4 && d.max_tokens > 8) return MOE_ERR_UNSUPPORTED;  // fused kernel only
 
   DeviceGuard guard(d.device);
   if (!guard.ok) return MOE_ERR_INVALID_ARG;
@@ -485,7 +490,8 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
                o_uoff = carve(4ull * (Um + 1)), o_ptok = carve(4 * P),
                o_pw = carve(4 * P), o_tku = carve(4 * P), o_tkpos = carve(4 * P),
                o_h16 = carve(2ull * (P + Tb) * I), o_tki = carve(4ull * Tm * k), o_tkw = carve(4ull * Tm * k),
-               o_bar = carve(8ull * Tk * E), o_cnt = carve(8ull * (Um + 2)), o_pool = carve(4ull * 2 * 3 * E);
+               o_bar = carve(8ull * Tk * E), o_cnt = carve(8ull * (Um + 2)), o_pool = carve(4ull * 2 * 3 * E),
+               o_hot = carve(4ull * kMaxHotExperts);
   if (cudaMalloc(&L->dev_block, off) != cudaSuccess) {
     L->dev_block = nullptr;
     return fail(MOE_ERR_OUT_OF_MEMORY);
@@ -521,10 +527,12 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.wait_timeout_ns = L->wait_timeout_ns;
   a.master = (const uint8_t*)master_dev;
   a.pull = 1;  // misses read by the kernel from the mapped master copy (moe_set_miss_service)
+  a.fmt = d.weight_format;
   L->tagged_logits = (unsigned long long*)(b + o_bar);
   a.counters = (uint32_t*)(b + o_cnt);
   a.cnt_stride = Um + 2;
   L->pool_state = (int32_t*)(b + o_pool);
+  L->hot_dev = (int32_t*)(b + o_hot);
   if (decode_configure() != cudaSuccess) return fail(MOE_ERR_CUDA);
   if (const size_t pfb = prefill_scratch_bytes(H, I, E, k, Tm)) {
     if (prefill_configure() != cudaSuccess) return fail(MOE_ERR_CUDA);
@@ -690,10 +698,21 @@ moe_status_t forward_impl(moe_layer_t* L, const void* x, int32_t T, void* y, int
       a.xhat_out = (uint16_t*)pn->xhat;
       a.eps = pn->eps;
     }
+    const moe_layer* nx = L->next;
+    if (nx && nx->n_slots > 0) {
+      a.nx_W_r = nx->args.W_r;
+      a.nx_shared = nx->args.shared;
+      a.nx_arena = nx->args.arena;
+      a.nx_pool_state = nx->args.pool ? nx->pool_state : nullptr;
+      a.nx_st = nx->args.st;
+      a.nx_S = nx->args.n_slots;
+      a.nx_hot = L->hot_dev;
+      a.nx_n_hot = L->n_hot;
+    }
     if (launch_decode(a, L->tagged_logits, L->pool_state, L->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (a.pool) return MOE_ERR_UNSUPPORTED;  // the slot pool runs on the fused path only
+  if (a.pool || a.fmt != MOE_FMT_LINEAR4) return MOE_ERR_UNSUPPORTED;  // pools and codebooks: fused path only
   if (pn && launch_residual_rmsnorm((const uint16_t*)pn->x, (const uint16_t*)pn->y_prev, T, L->d.hidden, pn->eps,
                                     (uint16_t*)pn->x_out, (uint16_t*)pn->xhat, s) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -804,6 +823,22 @@ moe_status_t moe_set_miss_service(moe_layer_t* L, int32_t mode) {
   DeviceGuard guard(L->d.device);
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;  // no call in flight sees a half-set mode
   L->args.pull = mode == MOE_MISS_SM_PULL ? 1 : 0;
+  return MOE_OK;
+}
+
+moe_status_t moe_set_next_layer(moe_layer_t* L, moe_layer_t* next, const int32_t* hot_experts, int32_t n_hot) {
+  if (!L || n_hot < 0 || n_hot > kMaxHotExperts || (n_hot > 0 && (!hot_experts || !next))) return MOE_ERR_INVALID_ARG;
+  if (next && (next->d.hidden != L->d.hidden || next->d.n_experts != L->d.n_experts ||
+               next->d.inter != L->d.inter || next->d.n_shared != L->d.n_shared || next->d.device != L->d.device))
+    return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < n_hot; ++i)
+    if (hot_experts[i] < 0 || hot_experts[i] >= L->d.n_experts) return MOE_ERR_INVALID_ARG;
+  DeviceGuard guard(L->d.device);
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;  // no call in flight reads the list
+  if (n_hot > 0 && cudaMemcpy(L->hot_dev, hot_experts, 4ull * n_hot, cudaMemcpyHostToDevice) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  L->next = next;
+  L->n_hot = n_hot;
   return MOE_OK;
 }
 

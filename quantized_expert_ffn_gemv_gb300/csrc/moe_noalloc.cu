@@ -62,12 +62,7 @@ __global__ void __launch_bounds__(kNaThreads) route_noalloc_kernel(const float* 
   for (int t0 = 0; t0 < T; t0 += kNaChunk) {
     const int nt = min(kNaChunk, T - t0);
     __syncthreads();
-    const uint32_t* xsrc = reinterpret_cast<const uint32_t*>(x + (size_t)t0 * H);
-    for (int i = tid; i < nt * H / 2; i += kNaThreads) {
-      const uint32_t v = xsrc[i];
-      xs[2 * i] = __uint_as_float(v << 16);
-      xs[2 * i + 1] = __uint_as_float(v & 0xFFFF0000u);
-    }
+    moe::stage_x_f32<kNaThreads>(x + (size_t)t0 * H, nt * H, xs, tid);
     __syncthreads();
     for (int tt = 0; tt < nt; ++tt) {
       // the compensated router in the library's canonical order (moe_route.cuh)
@@ -155,7 +150,7 @@ extern "C" MOE_API moe_status_t moe_route_noalloc(const float* router_w, const f
                                                   int32_t T, int32_t hidden, int32_t n_experts, int32_t top_k,
                                                   int32_t* topk_idx, float* topk_w, void* cuda_stream) {
   if (!router_w || !x_bf16 || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
-  if (((uintptr_t)router_w & 15) || ((uintptr_t)x_bf16 & 3) || ((uintptr_t)topk_idx & 3) || ((uintptr_t)topk_w & 3))
+  if (((uintptr_t)router_w & 15) || ((uintptr_t)x_bf16 & 15) || ((uintptr_t)topk_idx & 3) || ((uintptr_t)topk_w & 3))
     return MOE_ERR_INVALID_ARG;
   if (T < 1 || hidden < 64 || hidden % 64 || n_experts < 1 || top_k < 1 || top_k > n_experts)
     return MOE_ERR_INVALID_ARG;

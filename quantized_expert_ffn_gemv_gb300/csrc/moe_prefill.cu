@@ -237,19 +237,33 @@ __global__ void __launch_bounds__(256) prefill_prep_kernel(LayerArgs a, PrefillA
       if (lane == 0) p.wnorm[e] = sqrtf(ss) * 1.001f;
     }
   }
+  // x -> fp16 rows, and each token's norm (warp per token), for the same bound
   int bad = 0;
-  for (size_t i = ((size_t)blockIdx.x * 256 + threadIdx.x) * 8; i < nx; i += stride * 8) {
-    const uint4 v = *reinterpret_cast<const uint4*>(a.x + i);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
+  {
+    const int lane = threadIdx.x & 31;
+    const int gw = (int)((blockIdx.x * 256 + threadIdx.x) >> 5), nwarps = (int)(gridDim.x * 8);
+    for (int t = gw; t < a.T; t += nwarps) {
+      float ss = 0.f;
+      for (int h8 = lane * 8; h8 < a.H; h8 += 256) {
+        const size_t i = (size_t)t * a.H + h8;
+        const uint4 v = *reinterpret_cast<const uint4*>(a.x + i);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        uint32_t o[4];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const float f0 = __uint_as_float(w[q] << 16), f1 = __uint_as_float(w[q] & 0xFFFF0000u);
-      bad |= !(fabsf(f0) < 65504.f) || !(fabsf(f1) < 65504.f);
-      o[q] = h2u(__floats2half2_rn(f0, f1));
+        for (int q = 0; q < 4; ++q) {
+          const float f0 = __uint_as_float(w[q] << 16), f1 = __uint_as_float(w[q] & 0xFFFF0000u);
+          bad |= !(fabsf(f0) < 65504.f) || !(fabsf(f1) < 65504.f);
+          ss = fmaf(f0, f0, fmaf(f1, f1, ss));
+          o[q] = h2u(__floats2half2_rn(f0, f1));
+        }
+        *reinterpret_cast<uint4*>(p.x16p + i) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) p.xnorm[t] = sqrtf(ss) * 1.001f;
     }
-    *reinterpret_cast<uint4*>(p.x16p + i) = make_uint4(o[0], o[1], o[2], o[3]);
   }
+  (void)nx;
   if (bad) set_error(a, MOE_ERR_DEVICE);
 }
 
@@ -359,16 +373,7 @@ __global__ void __launch_bounds__(256) prefill_topk_kernel(LayerArgs a, PrefillA
   }
   if (boundary) {
     const float lk = __shfl_sync(0xffffffffu, my_v, k - 1), lk1 = __shfl_sync(0xffffffffu, my_v, k);
-    const uint32_t* xw = reinterpret_cast<const uint32_t*>(a.x + (size_t)t * H);
-    float xs = 0.f;
-    for (int i = lane; i < H / 2; i += 32) {
-      const uint32_t v = xw[i];
-      xs = fmaf(bf_lo(v), bf_lo(v), xs);
-      xs = fmaf(bf_hi(v), bf_hi(v), xs);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) xs += __shfl_xor_sync(0xffffffffu, xs, o);
-    const float delta = kTcBound * __uint_as_float(s_wmax) * (sqrtf(xs) * 1.001f) + 1e-6f * (fabsf(lk) + 1.f);
+    const float delta = kTcBound * __uint_as_float(s_wmax) * __ldg(p.xnorm + t) + 1e-6f * (fabsf(lk) + 1.f);
     if (lk - lk1 <= 2.f * delta) {
       // above hi: surely selected; below lo: surely not; in between: exact
       const float hi = lk + 2.f * delta, lo = lk1 - 2.f * delta;
@@ -894,13 +899,15 @@ __global__ void __launch_bounds__(sm_warps(MODE) * 32) prefill_small_kernel(Laye
           for (int b = 0; b < kSmBatch; ++b) {
             const int st = st0 + NW * b;
             if (st < nst) {
+              const SupertileA tg = dequant_supertile(w0[b], s0[b]);  // once for both token groups
+              const SupertileA tu = dequant_supertile(w1[b], s1[b]);
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
                 if (q < ng) {
                   uint4 b01, b23;
                   sm_load_b(bs, K, q, st, g, t4, b01, b23);
-                  supertile_mma(ag[q], w0[b], s0[b], b01, b23);
-                  supertile_mma(au[q], w1[b], s1[b], b01, b23);
+                  supertile_mma_pre(ag[q], tg, b01, b23);
+                  supertile_mma_pre(au[q], tu, b01, b23);
                 }
               }
             }
@@ -951,12 +958,13 @@ __global__ void __launch_bounds__(sm_warps(MODE) * 32) prefill_small_kernel(Laye
           for (int b = 0; b < kSmBatch; ++b) {
             const int st = st0 + b;
             if (st < nst) {
+              const SupertileA td = dequant_supertile(w0[b], s0[b]);  // once for both token groups
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
                 if (q < ng) {
                   uint4 b01, b23;
                   sm_load_b(bs, K, q, st, g, t4, b01, b23);
-                  supertile_mma(acc[q], w0[b], s0[b], b01, b23);
+                  supertile_mma_pre(acc[q], td, b01, b23);
                 }
               }
             }
@@ -1279,7 +1287,8 @@ size_t prefill_scratch_bytes(int H, int I, int E, int k, int Tm) {
   return pf_align(4ull * (E + 1)) + 2 * pf_align(4ull * (E + 2)) + pf_align(8) + pf_align(16 * chunks) +
          pf_align(16ull * (E + 1)) +
          2 * pf_align(4 * P) +
-         2 * pf_align(4ull * E * words) + pf_align(6ull * E * H) + pf_align(4ull * E) + pf_align(2ull * Tm * H) +
+         2 * pf_align(4ull * E * words) + pf_align(6ull * E * H) + pf_align(4ull * E) + pf_align(4ull * Tm) +
+         pf_align(2ull * Tm * H) +
          pf_align(2 * P * I) +
          pf_align(2 * P * H);
 }
@@ -1306,6 +1315,7 @@ PrefillArgs prefill_carve(void* block, int H, int I, int E, int k, int Tm) {
   p.prefix = (int32_t*)carve(4ull * E * words);
   p.w_split = (uint16_t*)carve(6ull * E * H);
   p.wnorm = (float*)carve(4ull * E);
+  p.xnorm = (float*)carve(4ull * Tm);
   p.x16p = (__half*)carve(2ull * Tm * H);
   p.h16p = (__half*)carve(2 * P * I);
   p.z16 = (__half*)carve(2 * P * H);

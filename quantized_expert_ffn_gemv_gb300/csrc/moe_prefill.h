@@ -27,6 +27,7 @@ struct PrefillArgs {
   int32_t* prefix;      // [E][ceil(T/32)] set bits of row e in the words before each word
   uint16_t* w_split;    // [3][E][H] bf16 pieces of the router weights: W = W0 + W1 + W2
   float* wnorm;         // [E] Euclidean norms of the router rows (slightly rounded up)
+  float* xnorm;         // [T] Euclidean norms of the call's activation rows (slightly rounded up)
   __half* x16p;         // [T][H] fp16 activations
   __half* h16p;         // [T*k + T][I] fp16 h of each pair
   __half* z16;          // [T*(k+1)][H] fp16 expert outputs before the weighting

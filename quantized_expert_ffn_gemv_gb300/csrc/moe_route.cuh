@@ -10,7 +10,7 @@
 // product of Ogita, Rump and Oishi ("Accurate sum and dot product", SIAM J.
 // Sci. Comput. 26, 2005, algorithm Dot2).  Its error is bounded by
 // gamma_n^2 * sum |w x| (n = 64 terms per lane at H = 2048 plus five tree
-// levels): below 5e-10 there, about 1e-13 in practice.
+// levels): below 5e-10 there, and typically far smaller.
 //
 // Canonical summation order (every kernel follows it, so a logit has the
 // same bits on every path):  the H inputs split into four quarters; in
@@ -18,11 +18,11 @@
 // l + 64, ... of the quarter in that order (components x, y, z, w); the 32
 // lane partials are combined by an xor butterfly (offsets 16, 8, 4, 2, 1);
 // the quarters are then added in the order ((q0 + q1) + q2) + q3, then the
-// bias.  The pair (s, c) is finally rounded once to binary64.
+// bias.  The pair (s, c) is finally normalised to hi + lo.
 //
-// Key: the binary64 logit mapped to an unsigned integer that orders like the
-// value (NaN lowest, -0 = +0), keeping its 52 high bits (sign, exponent, 40
-// fraction bits: 2^-40 relative resolution).  The low 12 bits of the 64-bit
+// Key: the pair mapped to an unsigned integer that orders like its value
+// (NaN lowest, -0 = +0), keeping 52 high bits (2^-36 relative resolution
+// below hi's own 2^-24).  The low 12 bits of the 64-bit
 // words built from a key hold either the expert's complement 4095 - e (so
 // one unsigned compare ranks by logit, then lower index), or a call tag.
 #pragma once
@@ -94,27 +94,38 @@ __device__ __forceinline__ DF quarter_partial_bf16(const float* wq, const uint16
   return d;
 }
 
-// ((q0 + q1) + q2) + q3 + bias, rounded once to binary64, as a 52-bit key.
+// Order-preserving 32-bit image of a float (-0 as +0).
+__device__ __forceinline__ uint32_t fkey(float f) {
+  const uint32_t u = __float_as_uint(__fadd_rn(f, 0.f));
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// ((q0 + q1) + q2) + q3 + bias as a 52-bit key.  The sum is normalised to
+// hi + lo with hi = fl(hi + lo) (TwoSum, exact); hi then orders the values
+// and lo breaks ties of hi, so the 64-bit word fkey(hi) : fkey(lo) orders
+// exactly like hi + lo.  The key keeps its top 52 bits (lo to 12 of its
+// bits: 2^-36 relative).  Float arithmetic only: this GPU's FP64 units are
+// few and a handful of double operations stalled CTAs for microseconds.
 __device__ __forceinline__ uint64_t logit_key(DF q0, DF q1, DF q2, DF q3, float bias) {
   DF d = df_add(df_add(df_add(q0, q1), q2), q3);
   float s, e;
   two_sum(d.s, bias, s, e);
-  // an infinite sum (a -inf bias masks an expert) keeps its value; the error
-  // terms of an infinite sum are NaN and mean nothing
-  double v = isfinite(s) ? __dadd_rn((double)s, (double)__fadd_rn(d.c, e)) : (double)s;
-  if (v != v) return 1ull;  // NaN ranks below every number, -inf included
-  v = __dadd_rn(v, 0.0);    // -0 -> +0
-  uint64_t u = (uint64_t)__double_as_longlong(v);
-  u = (u >> 63) ? ~u : (u | 0x8000000000000000ull);
-  const uint64_t k = u >> 12;
+  float hi, lo;
+  if (isfinite(s)) {
+    two_sum(s, __fadd_rn(d.c, e), hi, lo);
+  } else {  // an infinite sum (a -inf bias masks an expert) keeps its value
+    hi = s;
+    lo = 0.f;
+  }
+  if (hi != hi || lo != lo) return 1ull;  // NaN ranks below every number, -inf included
+  const uint64_t k = (((uint64_t)fkey(hi) << 32) | fkey(lo)) >> 12;
   return k ? k : 1ull;  // 0 is reserved for "no entry"
 }
 
-// The logit a key stands for, as fp32 (for the softmax weights).
+// The logit a key stands for, as fp32 (its hi part; for the softmax weights).
 __device__ __forceinline__ float key_value(uint64_t key52) {
-  uint64_t u = key52 << 12;
-  u = (u >> 63) ? (u & 0x7FFFFFFFFFFFFFFFull) : ~u;
-  return (float)__longlong_as_double((long long)u);
+  const uint32_t k = (uint32_t)(key52 >> 20);
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
 // One unsigned compare ranks (larger logit, then lower expert index); 0 = none.
@@ -130,6 +141,33 @@ __device__ __forceinline__ uint64_t warp_max_u64(uint64_t v) {
   const uint32_t mh = __reduce_max_sync(0xffffffffu, hi);
   const uint32_t ml = __reduce_max_sync(0xffffffffu, hi == mh ? (uint32_t)v : 0u);
   return ((uint64_t)mh << 32) | ml;
+}
+
+// n bf16 activations (n a multiple of 8, 16-byte aligned) -> fp32 in shared
+// memory by NT threads: every thread's loads are issued before any of its
+// stores, so the staging costs one global round trip, not one per element.
+template <int NT>
+__device__ __forceinline__ void stage_x_f32(const uint16_t* src, int n, float* dst, int tid) {
+  constexpr int kPer = 8;  // 16-byte loads per thread in flight together
+  const uint4* s4 = reinterpret_cast<const uint4*>(src);
+  const int n8 = n / 8;
+  for (int i0 = 0; i0 < n8; i0 += NT * kPer) {
+    uint4 v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = i0 + j * NT + tid;
+      v[j] = i < n8 ? __ldcg(s4 + i) : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int i = i0 + j * NT + tid;
+      if (i < n8) {
+        float4* d = reinterpret_cast<float4*>(dst + 8 * i);
+        d[0] = make_float4(bf_lo(v[j].x), bf_hi(v[j].x), bf_lo(v[j].y), bf_hi(v[j].y));
+        d[1] = make_float4(bf_lo(v[j].z), bf_hi(v[j].z), bf_lo(v[j].w), bf_hi(v[j].w));
+      }
+    }
+  }
 }
 
 // One warp: the k best of one token's rank words staged in shared memory

@@ -23,9 +23,15 @@
  *                 low nibble when i is even, stored value u = q + 8
  *   scale plane   R * K/32 IEEE binary16 scales, one per block of 32
  *                 consecutive elements along K (the reduction axis).
- * Quantizer (4-bit symmetric, block 32, one fp16 scale):
+ * Quantizer, format 0 (4-bit symmetric, block 32, one fp16 scale):
  *   d = fp16_rn(amax / 7); q = clamp(round_half_even(w / d), -8, 7);
  *   an all-zero block (or one whose scale rounds to 0) stores d = 0, q = 0.
+ * Quantizer, format 1 (4-bit codebook, block 32, one fp16 scale; the
+ *   non-linear 16-entry lookup formats of the halogen-flash-server README,
+ *   section "Bring your own GGUF"): weight = d * C[u] with C the levels of
+ *   the standard normal's quantiles (u + 1/2) / 16, scaled to +-127 and
+ *   rounded (see kCodebook); d = fp16_rn(amax / 127); u = the level nearest
+ *   w / d, ties to the lower u; a zero block stores d = 0 and u = 8.
  */
 #include <stdint.h>
 #include <string.h>
@@ -208,12 +214,46 @@ void synth_quantize_rows(const float* w, int64_t R, int64_t K, uint8_t* nib, uin
   }
 }
 
+/* The codebook of format 1, ascending. */
+static const int kCodebook[16] = {-127, -90, -69, -53, -39, -27, -16, -5, 5, 16, 27, 39, 53, 69, 90, 127};
+
+void synth_quantize_rows_cb(const float* w, int64_t R, int64_t K, uint8_t* nib, uint16_t* scales) {
+  const int64_t nb = K / 32;
+  for (int64_t r = 0; r < R; ++r) {
+    for (int64_t b = 0; b < nb; ++b) {
+      const float* blk = w + r * K + b * 32;
+      double amax = 0.0;
+      for (int i = 0; i < 32; ++i) {
+        double a = fabs((double)blk[i]);
+        if (a > amax) amax = a;
+      }
+      uint16_t d16 = f64_to_f16(amax / 127.0);
+      double d = f16_value(d16);
+      scales[r * nb + b] = d16;
+      uint8_t* out = nib + r * (K / 2) + b * 16;
+      for (int i = 0; i < 32; i += 2) {
+        int u[2] = {8, 8};
+        for (int h = 0; h < 2 && d != 0.0; ++h) {
+          const double t = (double)blk[i + h] / d;
+          double best = fabs(t - kCodebook[0]);
+          u[h] = 0;
+          for (int c = 1; c < 16; ++c) {
+            const double e = fabs(t - kCodebook[c]);
+            if (e < best) { best = e; u[h] = c; }
+          }
+        }
+        out[i / 2] = (uint8_t)(u[0] | (u[1] << 4));
+      }
+    }
+  }
+}
+
 /* Bytes of one R x K packed matrix / of one expert blob. */
 int64_t synth_matrix_bytes(int64_t R, int64_t K) { return R * (K / 2) + R * (K / 32) * 2; }
 int64_t synth_expert_bytes(int64_t H, int64_t I) { return 3 * synth_matrix_bytes(I, H); }
 
 /* One R x K matrix of N(0, sigma^2) weights (fp32), quantized into `dst`. */
-static void gen_matrix(uint64_t key, int64_t R, int64_t K, double sigma, uint8_t* dst, float* rowbuf) {
+static void gen_matrix(uint64_t key, int64_t R, int64_t K, double sigma, int fmt, uint8_t* dst, float* rowbuf) {
   uint8_t* nib = dst;
   uint16_t* sc = (uint16_t*)(dst + R * (K / 2));
   for (int64_t r = 0; r < R; ++r) {
@@ -223,22 +263,26 @@ static void gen_matrix(uint64_t key, int64_t R, int64_t K, double sigma, uint8_t
       rowbuf[i] = to_f32(a * sigma);
       rowbuf[i + 1] = to_f32(b * sigma);
     }
-    synth_quantize_rows(rowbuf, 1, K, nib + r * (K / 2), sc + r * (K / 32));
+    if (fmt == 1)
+      synth_quantize_rows_cb(rowbuf, 1, K, nib + r * (K / 2), sc + r * (K / 32));
+    else
+      synth_quantize_rows(rowbuf, 1, K, nib + r * (K / 2), sc + r * (K / 32));
   }
 }
 
 /* One canonical expert blob; matrix m in {0: gate, 1: up, 2: down} uses key_m. */
-void synth_expert_blob(uint64_t key, int64_t H, int64_t I, double sigma, uint8_t* blob, float* scratch) {
+void synth_expert_blob(uint64_t key, int64_t H, int64_t I, double sigma, int fmt, uint8_t* blob, float* scratch) {
   const int64_t mb = synth_matrix_bytes(I, H);
-  gen_matrix(synth_key(key, 0, 0, 0, 0), I, H, sigma, blob, scratch);
-  gen_matrix(synth_key(key, 1, 0, 0, 0), I, H, sigma, blob + mb, scratch);
-  gen_matrix(synth_key(key, 2, 0, 0, 0), H, I, sigma, blob + 2 * mb, scratch);
+  gen_matrix(synth_key(key, 0, 0, 0, 0), I, H, sigma, fmt, blob, scratch);
+  gen_matrix(synth_key(key, 1, 0, 0, 0), I, H, sigma, fmt, blob + mb, scratch);
+  gen_matrix(synth_key(key, 2, 0, 0, 0), H, I, sigma, fmt, blob + 2 * mb, scratch);
 }
 
 typedef struct {
   uint64_t seed, layer, tag;
   int64_t H, I, e0, e1;
   double sigma;
+  int fmt;
   uint8_t* out;
 } job_t;
 
@@ -248,18 +292,19 @@ static void* expert_worker(void* p) {
   float* scratch = (float*)__builtin_alloca((size_t)K * sizeof(float));
   const int64_t eb = synth_expert_bytes(j->H, j->I);
   for (int64_t e = j->e0; e < j->e1; ++e)
-    synth_expert_blob(synth_key(j->seed, j->layer, j->tag, (uint64_t)e, 0), j->H, j->I, j->sigma,
+    synth_expert_blob(synth_key(j->seed, j->layer, j->tag, (uint64_t)e, 0), j->H, j->I, j->sigma, j->fmt,
                       j->out + (e - j->e0) * eb, scratch);
   return 0;
 }
 
 /*
  * Canonical blobs of experts [e0, e1) of `layer` (tag 3 = routed, 4 = shared)
- * written contiguously to `out`, on up to `threads` threads.
+ * in weight format `fmt`, written contiguously to `out`, on up to `threads`
+ * threads.
  */
 int synth_experts(uint64_t seed, uint64_t layer, uint64_t tag, int64_t H, int64_t I, int64_t e0, int64_t e1,
-                  double sigma, uint8_t* out, int threads) {
-  if (H % 32 || I % 32 || e1 < e0) return -1;
+                  double sigma, int fmt, uint8_t* out, int threads) {
+  if (H % 32 || I % 32 || e1 < e0 || fmt < 0 || fmt > 1) return -1;
   int64_t n = e1 - e0;
   if (threads < 1) threads = 1;
   if (threads > 64) threads = 64;
@@ -269,7 +314,7 @@ int synth_experts(uint64_t seed, uint64_t layer, uint64_t tag, int64_t H, int64_
   const int64_t eb = synth_expert_bytes(H, I);
   for (int t = 0; t < threads; ++t) {
     int64_t a = e0 + n * t / threads, b = e0 + n * (t + 1) / threads;
-    jobs[t] = (job_t){seed, layer, tag, H, I, a, b, sigma, out + (a - e0) * eb};
+    jobs[t] = (job_t){seed, layer, tag, H, I, a, b, sigma, fmt, out + (a - e0) * eb};
   }
   int ok[64] = {0};
   for (int t = 1; t < threads; ++t) ok[t] = pthread_create(&th[t], 0, expert_worker, &jobs[t]) == 0;

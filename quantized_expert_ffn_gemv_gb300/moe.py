@@ -18,7 +18,8 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 EXPORTS = ["moe_expert_bytes", "moe_repack_expert", "moe_unpack_expert", "moe_layer_create",
            "moe_slot_pool_configure", "moe_forward", "moe_residual_rmsnorm", "moe_get_stats", "moe_get_miss_log",
            "moe_set_wait_timeout_ns", "moe_debug_copy_faults", "moe_destroy", "moe_status_string",
-           "moe_route_noalloc", "moe_set_miss_service", "moe_slot_pool_seed", "moe_forward_norm"]
+           "moe_route_noalloc", "moe_set_miss_service", "moe_slot_pool_seed", "moe_forward_norm",
+           "moe_set_next_layer"]
 
 
 class MoeError(RuntimeError):
@@ -31,7 +32,7 @@ class LayerDesc(C.Structure):
     _fields_ = [("hidden", C.c_int32), ("n_experts", C.c_int32), ("top_k", C.c_int32), ("n_shared", C.c_int32),
                 ("inter", C.c_int32), ("qblock", C.c_int32), ("max_tokens", C.c_int32), ("device", C.c_int32),
                 ("router_w", C.c_void_p), ("router_bias", C.c_void_p), ("experts", C.c_void_p),
-                ("shared", C.c_void_p)]
+                ("shared", C.c_void_p), ("weight_format", C.c_int32)]
 
 
 class Stats(C.Structure):
@@ -67,6 +68,7 @@ def lib(build_if_missing=False):
         L.moe_get_miss_log.argtypes = [p, p, i64, C.POINTER(i64)]
         L.moe_set_wait_timeout_ns.argtypes = [p, u64]
         L.moe_set_miss_service.argtypes = [p, i32]
+        L.moe_set_next_layer.argtypes = [p, p, p, i32]
         L.moe_debug_copy_faults.argtypes = [p, i64, i32]
         L.moe_destroy.argtypes = [p]
         L.moe_destroy.restype = None
@@ -172,7 +174,8 @@ class MoeLayer:
         d = LayerDesc(hidden=shape.H, n_experts=shape.E, top_k=shape.k, n_shared=0 if shared is None else 1,
                       inter=shape.I, qblock=32, max_tokens=max_tokens, device=device,
                       router_w=self.W_r.data_ptr(), router_bias=None if self.bias is None else self.bias.data_ptr(),
-                      experts=experts.ctypes.data, shared=None if shared_np is None else shared_np.ctypes.data)
+                      experts=experts.ctypes.data, shared=None if shared_np is None else shared_np.ctypes.data,
+                      weight_format=getattr(shape, "fmt", 0))
         h = C.c_void_p()
         check(lib().moe_layer_create(C.byref(d), C.byref(h)), "moe_layer_create")
         self.h = h
@@ -232,6 +235,15 @@ class MoeLayer:
     def set_miss_service(self, mode):
         """1 = the kernel reads misses from host memory (default), 0 = host copy engine behind the doorbell."""
         check(lib().moe_set_miss_service(self.h, int(mode)), "moe_set_miss_service")
+
+    def set_next(self, nxt, hot=None):
+        """Warm L2 for `nxt` (the layer called after this one) at the end of
+        every decode call: its router rows, shared expert and the listed hot
+        experts.  nxt None removes the link."""
+        hot = np.ascontiguousarray(np.asarray([] if hot is None else hot, dtype=np.int32))
+        check(lib().moe_set_next_layer(self.h, None if nxt is None else nxt.h, hot.ctypes.data if len(hot) else None,
+                                       len(hot)), "moe_set_next_layer")
+        self.next = nxt
 
     def debug_copy_faults(self, fail_copy_n=0, pause=False):
         check(lib().moe_debug_copy_faults(self.h, fail_copy_n, int(pause)), "moe_debug_copy_faults")

@@ -33,6 +33,7 @@ class MoeStack:
         self.H = layers[0].shape.H
         self.k = layers[0].shape.k
         self.device = torch.device("cuda", device)
+        self.link()
 
     fused = True  # residual + RMSNorm inside each layer's call (moe_forward_norm)
 
@@ -88,6 +89,14 @@ class MoeStack:
             cur = 1 - cur
         return bufs["x"][cur][:T]
 
+    def link(self, hot=None):
+        """Each layer warms L2 for the next one at the end of its decode call
+        (router rows, shared expert, and hot[l + 1], a list of layer l + 1's
+        most-selected experts, when given); the last layer links to none."""
+        for l, layer in enumerate(self.layers):
+            nxt = self.layers[l + 1] if l + 1 < len(self.layers) else None
+            layer.set_next(nxt, None if (hot is None or nxt is None) else hot[l + 1])
+
     def seed(self, seeds):
         """Start every pooled layer's pool from its list of hot experts."""
         if len(seeds) != len(self.layers):
@@ -105,5 +114,8 @@ class MoeStack:
         return [l.stats()[0] for l in self.layers]
 
     def close(self):
+        for l in self.layers:
+            if getattr(l, "h", None):
+                l.set_next(None)
         for l in self.layers:
             l.close()

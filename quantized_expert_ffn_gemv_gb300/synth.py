@@ -32,11 +32,12 @@ def lib():
         _lib.synth_key.restype = u64
         _lib.synth_normal_f64.argtypes = [u64, u64, u64, p]
         _lib.synth_quantize_rows.argtypes = [p, i64, i64, p, p]
+        _lib.synth_quantize_rows_cb.argtypes = [p, i64, i64, p, p]
         _lib.synth_matrix_bytes.argtypes = [i64, i64]
         _lib.synth_matrix_bytes.restype = i64
         _lib.synth_expert_bytes.argtypes = [i64, i64]
         _lib.synth_expert_bytes.restype = i64
-        _lib.synth_experts.argtypes = [u64, u64, u64, i64, i64, i64, i64, C.c_double, p, C.c_int]
+        _lib.synth_experts.argtypes = [u64, u64, u64, i64, i64, i64, i64, C.c_double, C.c_int, p, C.c_int]
         _lib.synth_experts.restype = C.c_int
         _lib.synth_router.argtypes = [u64, u64, i64, i64, p]
         _lib.synth_zipf_bias.argtypes = [u64, u64, i64, C.c_double, p, p]
@@ -61,6 +62,7 @@ class LayerShape:
     I: int
     zipf_s: float = 0.0      # 0: no router bias
     expert_sigma: float = 0.02
+    fmt: int = 0             # weight format: 0 linear 4-bit (d * (u - 8)), 1 codebook (d * C[u])
 
     @property
     def matrix_bytes(self):
@@ -88,7 +90,8 @@ def experts(shape, layer, e0=0, e1=None, seed=MASTER_SEED, tag=TAG_ROUTED, out=N
     if out is None:
         out = np.empty(n * shape.expert_bytes, np.uint8)
     assert out.nbytes >= n * shape.expert_bytes and out.flags.c_contiguous
-    rc = lib().synth_experts(seed, layer, tag, shape.H, shape.I, e0, e1, shape.expert_sigma, _p(out), threads())
+    rc = lib().synth_experts(seed, layer, tag, shape.H, shape.I, e0, e1, shape.expert_sigma, shape.fmt, _p(out),
+                             threads())
     if rc != 0:
         raise RuntimeError(f"synth_experts failed ({rc})")
     return out
@@ -124,13 +127,14 @@ def activations(shape, layer, t0, T, stream=0, sub=None, seed=MASTER_SEED):
     return x
 
 
-def quantize_rows(w):
-    """Quantize float32 [R, K] into (nibbles uint8 [R, K/2], scales uint16 [R, K/32])."""
+def quantize_rows(w, fmt=0):
+    """Quantize float32 [R, K] into (nibbles uint8 [R, K/2], scales uint16 [R, K/32])
+    in weight format fmt (0 linear 4-bit, 1 codebook)."""
     w = np.ascontiguousarray(w, np.float32)
     R, K = w.shape
     nib = np.empty((R, K // 2), np.uint8)
     sc = np.empty((R, K // 32), np.uint16)
-    lib().synth_quantize_rows(_p(w), R, K, _p(nib), _p(sc))
+    (lib().synth_quantize_rows_cb if fmt == 1 else lib().synth_quantize_rows)(_p(w), R, K, _p(nib), _p(sc))
     return nib, sc
 
 

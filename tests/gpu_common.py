@@ -57,7 +57,7 @@ def run(layer, x_u16, T=None):
 def check_against_oracle(L, x_u16, y, idx, w, rows=None, w_rtol=W_RTOL):
     sh = L.shape
     rows = np.arange(x_u16.shape[0]) if rows is None else np.asarray(rows)
-    ref = oracle.moe_forward(sh.H, sh.I, sh.E, sh.k, L.W_r, L.bias, L.experts, L.shared, x_u16[rows])
+    ref = oracle.moe_forward(sh.H, sh.I, sh.E, sh.k, L.W_r, L.bias, L.experts, L.shared, x_u16[rows], fmt=sh.fmt)
     assert np.array_equal(idx[rows], ref["idx"]), "routing differs from the oracle"
     assert np.allclose(w[rows], ref["w"], rtol=w_rtol, atol=1e-7)
     yg = synth.bf16_to_f32(y[rows]).astype(np.float64)

@@ -32,7 +32,17 @@ def resampled_tokens(layer, t0, T, stream=0, gap=GAP, max_redraw=64):
     raise RuntimeError("could not resample near-ties")
 
 
-def dequant_numpy(mat, R, K):
+def codebook_levels():
+    """The codebook format's 16 levels from their definition: the standard
+    normal's quantiles at (u + 1/2)/16, scaled so the outermost is 127,
+    rounded to integers (scipy's inverse normal CDF, independent of the
+    oracle's and the library's own tables)."""
+    from scipy.stats import norm
+    z = norm.ppf((np.arange(16) + 0.5) / 16)
+    return np.round(127 * z / z[-1])
+
+
+def dequant_numpy(mat, R, K, fmt=0):
     """Independent numpy decoder of one packed matrix (nibble plane + scale plane)."""
     mat = np.asarray(mat, np.uint8)
     nib = mat[:R * K // 2].reshape(R, K // 2)
@@ -40,10 +50,12 @@ def dequant_numpy(mat, R, K):
     u = np.empty((R, K), np.int64)
     u[:, 0::2] = nib & 15
     u[:, 1::2] = nib >> 4
-    return (u - 8) * np.repeat(sc, 32, axis=1)
+    v = codebook_levels()[u] if fmt == 1 else (u - 8)
+    return v * np.repeat(sc, 32, axis=1)
 
 
-def expert_mats(blob, H, I):
+def expert_mats(blob, H, I, fmt=0):
     mb = I * H // 2 + I * H // 16
     b = np.asarray(blob, np.uint8)
-    return (dequant_numpy(b[:mb], I, H), dequant_numpy(b[mb:2 * mb], I, H), dequant_numpy(b[2 * mb:3 * mb], H, I))
+    return (dequant_numpy(b[:mb], I, H, fmt), dequant_numpy(b[mb:2 * mb], I, H, fmt),
+            dequant_numpy(b[2 * mb:3 * mb], H, I, fmt))

@@ -12,7 +12,7 @@ import pytest
 
 import oracle
 from quantized_expert_ffn_gemv_gb300 import synth
-from tests.inputs import dequant_numpy, expert_mats, resampled_tokens
+from tests.inputs import codebook_levels, dequant_numpy, expert_mats, resampled_tokens
 
 
 def silu(z):
@@ -145,7 +145,7 @@ def test_scale_is_fp16_of_amax_over_7():
 # ---------------------------------------------------------------- the layer against a dense numpy path
 
 
-def dense_layer(W_r, bias, blobs, shared, H, I, k, x_bf16):
+def dense_layer(W_r, bias, blobs, shared, H, I, k, x_bf16, fmt=0):
     """Independent dense float64 evaluation: every matrix fully dequantized
     (numpy decoder), softmax over all experts renormalised over the top k."""
     E = W_r.shape[0]
@@ -159,23 +159,25 @@ def dense_layer(W_r, bias, blobs, shared, H, I, k, x_bf16):
     eb = 3 * (I * H // 2 + I * H // 16)
     y = np.zeros(H)
     for wj, e in zip(wts, S):
-        g, u, d = expert_mats(blobs[e * eb:(e + 1) * eb], H, I)
+        g, u, d = expert_mats(blobs[e * eb:(e + 1) * eb], H, I, fmt)
         y += wj * (d @ (silu(g @ x) * (u @ x)))
     if shared is not None:
-        g, u, d = expert_mats(shared, H, I)
+        g, u, d = expert_mats(shared, H, I, fmt)
         y += d @ (silu(g @ x) * (u @ x))
     return y, np.array(S, np.int32), wts
 
 
-def test_dense_toy_four_experts():
+@pytest.mark.parametrize("fmt", [0, 1], ids=["linear", "codebook"])
+def test_dense_toy_four_experts(fmt):
     """E = 4, k = 4, H = 64, I = 32: the MoE result equals
-    sum_e softmax_e FFN_e(x) + FFN_shared(x) on fully dequantized weights."""
-    sh = synth.LayerShape(H=64, E=4, k=4, I=32, expert_sigma=0.3)
+    sum_e softmax_e FFN_e(x) + FFN_shared(x) on fully dequantized weights,
+    in both weight formats."""
+    sh = synth.LayerShape(H=64, E=4, k=4, I=32, expert_sigma=0.3, fmt=fmt)
     L = synth.make_layer(sh, layer=900)
     x = synth.activations(sh, 900, 0, 3)
-    r = oracle.moe_forward(64, 32, 4, 4, L.W_r, L.bias, L.experts, L.shared, x)
+    r = oracle.moe_forward(64, 32, 4, 4, L.W_r, L.bias, L.experts, L.shared, x, fmt=fmt)
     for t in range(3):
-        y, S, wts = dense_layer(L.W_r, L.bias, L.experts, L.shared, 64, 32, 4, x[t])
+        y, S, wts = dense_layer(L.W_r, L.bias, L.experts, L.shared, 64, 32, 4, x[t], fmt)
         assert np.array_equal(r["idx"][t], np.arange(4))
         assert np.allclose(r["w"][t], wts, rtol=1e-13, atol=0)
         assert np.allclose(r["y"][t], y, rtol=1e-12, atol=1e-14)
@@ -366,3 +368,71 @@ def test_all_logits_tied_picks_the_lowest_indices_with_zero_gap():
     assert np.array_equal(r["idx"], np.tile(np.arange(sh.k, dtype=np.int32), (2, 1)))
     assert np.all(r["w"] == 1.0 / 3.0) or np.allclose(r["w"], 1.0 / 3.0, rtol=1e-15, atol=0)
     assert np.all(r["gap"] == 0.0)
+
+
+# ---------------------------------------------------------------- the codebook weight format
+
+
+def test_codebook_levels_are_the_normal_quantiles():
+    lv = oracle.levels()
+    ref = codebook_levels()
+    assert np.array_equal(lv, ref)
+    assert np.all(np.diff(lv) > 0) and np.array_equal(lv, -lv[::-1]) and lv[-1] == 127
+    # every level is an integer, exact in binary16 (what the GPU multiplies)
+    assert np.array_equal(lv.astype(np.float16).astype(np.float64), lv)
+
+
+def test_codebook_dequant_matches_independent_decoder():
+    rng = np.random.default_rng(17)
+    R, K = 32, 128
+    nib = rng.integers(0, 256, size=(R, K // 2), dtype=np.uint8)  # every nibble value
+    sc = (rng.normal(size=(R, K // 32)) * 0.01).astype(np.float16)
+    mat = synth.pack_matrix(nib, sc.view(np.uint16))
+    a = oracle.dequant_matrix(mat, R, K, fmt=1)
+    assert np.array_equal(a, dequant_numpy(mat, R, K, fmt=1))
+    assert a[2, 1] == float(sc[2, 0]) * codebook_levels()[nib[2, 0] >> 4]
+
+
+@pytest.mark.parametrize("sigma", [0.02, 1.0])
+def test_codebook_quantizer_picks_the_nearest_level(sigma):
+    """The generator's codebook quantizer: d = fp16(amax / 127), each element
+    the nearest level of w / d (ties to the lower index, re-derived here by
+    brute force); dequantized error within half the widest level gap."""
+    rng = np.random.default_rng(19)
+    R, K = 32, 256
+    w = (rng.normal(size=(R, K)) * sigma).astype(np.float32)
+    w[3, 64:96] = 0.0
+    nib, sc = synth.quantize_rows(w, fmt=1)
+    lv = codebook_levels()
+    d = sc.view(np.float16).astype(np.float64)
+    assert np.array_equal(sc.view(np.float16),
+                          (np.abs(w.reshape(R, K // 32, 32)).max(axis=2).astype(np.float64) / 127).astype(np.float16))
+    u = np.empty((R, K), np.int64)
+    u[:, 0::2] = nib & 15
+    u[:, 1::2] = nib >> 4
+    dd = np.repeat(d, 32, axis=1)
+    t = np.where(dd > 0, w.astype(np.float64) / np.where(dd > 0, dd, 1), 0)
+    want = np.argmin(np.abs(t[..., None] - lv[None, None, :]), axis=2)  # first minimum: the lower index
+    nz = dd > 0
+    assert np.array_equal(u[nz], want[nz])
+    assert np.all(u[~nz] == 8)
+    deq = oracle.dequant_matrix(synth.pack_matrix(nib, sc), R, K, fmt=1)
+    gap = np.max(np.diff(lv)) / 2
+    assert np.all(np.abs(w.astype(np.float64) - deq) <= dd * gap + 1e-30)
+
+
+def test_codebook_closed_forms():
+    """x = 0 gives y = 0; identical experts give the same output whatever the routing."""
+    sh = synth.LayerShape(H=128, E=8, k=2, I=64, fmt=1)
+    L = synth.make_layer(sh, layer=31)
+    x0 = np.zeros((1, 128), np.uint16)
+    r = oracle.moe_forward(128, 64, 8, 2, L.W_r, L.bias, L.experts, L.shared, x0, fmt=1)
+    assert np.all(r["y"] == 0.0)
+    eb = sh.expert_bytes
+    one = L.experts[:eb]
+    same = np.tile(one, 8)
+    x = synth.activations(sh, 31, 0, 2)
+    a = oracle.moe_forward(128, 64, 8, 2, L.W_r, None, same, one, x, fmt=1)
+    for t in range(2):
+        ya, _ = oracle.expert(one, 128, 64, synth.bf16_to_f32(x[t]).astype(np.float64), fmt=1)
+        assert np.allclose(a["y"][t], 2 * ya, rtol=1e-12, atol=1e-15)
