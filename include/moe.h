@@ -280,12 +280,14 @@ MOE_API moe_status_t moe_set_wait_timeout_ns(moe_layer_t* layer, uint64_t ns);
  *    at once and write it into its slot for later calls; the copy server
  *    only logs the doorbell entry, so nothing in the call waits on the host.
  *  MOE_MISS_COPY_ENGINE: the kernel waits; the copy server copies the
- *    expert into its slot (cudaMemcpyAsync on its own streams) and publishes
- *    the slot's ready flag.  The copy server then needs the CUDA driver
- *    while the kernel runs; now and then (measured: 2 of 5 runs of 200
- *    tokens through 8 pooled layers with a stream synchronize every 2
- *    tokens) a copy is held back until the kernel's bounded wait ends the
- *    call with MOE_ERR_TIMEOUT (no hang, no dropped miss).
+ *    expert into its slot (cudaMemcpyAsync on the layer's copy streams) and
+ *    publishes the slot's ready flag with a stream memory operation.  The
+ *    copy streams are created at the device's highest priority: streams of
+ *    different priorities never share a hardware work queue, so a slot copy
+ *    is never queued behind compute work that itself waits for the kernel
+ *    that waits for the copy.  The kernel's wait stays bounded
+ *    (moe_set_wait_timeout_ns); if it runs out, the call ends with
+ *    MOE_ERR_TIMEOUT (no hang, no dropped miss).
  * Applies to calls launched afterwards; a CUDA graph captured earlier keeps
  * the mode it was captured with.  Synchronizes the device.
  * Errors: INVALID_ARG (null layer or unknown mode), CUDA.

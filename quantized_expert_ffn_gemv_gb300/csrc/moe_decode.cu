@@ -438,7 +438,7 @@ __device__ void warp_best(const unsigned long long* words, int E, int k, int bas
   }
   if (CPL == 1) {
     int r = 0;
-#pragma unroll
+#pragma unroll 4
     for (int i = 0; i < 32; ++i) {
       const uint64_t wi = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(w[0] >> 32), i) << 32) |
                           __shfl_sync(0xffffffffu, (uint32_t)w[0], i);
@@ -476,7 +476,7 @@ __device__ __forceinline__ void keep_survivors(const TopkScratch& S, int t, int 
   const int m = 32 / wpt, li = t * wpt + lane / m, ei = lane % m;
   const uint64_t v = ei < S.len[li] ? S.list[li * kListStride + ei] : 0ull;
   int r = 0;
-#pragma unroll
+#pragma unroll 4
   for (int i = 0; i < 32; ++i) {
     const uint64_t vi = ((uint64_t)__shfl_sync(0xffffffffu, (uint32_t)(v >> 32), i) << 32) |
                         __shfl_sync(0xffffffffu, (uint32_t)v, i);
@@ -562,7 +562,9 @@ __device__ __forceinline__ void finish_topk(unsigned long long* sel, int k, cons
 // 512 experts (the decode of a resident stack), compiled without the batch
 // loops, the slot-pool code and the wider top-k shapes so that the code one
 // launch runs stays small.
-template <bool ONE>
+// FMT: the weight format (0 linear, 1 codebook), fixed at compile time so the
+// linear format's inner loop carries no format test.
+template <bool ONE, int FMT>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsigned long long* tagged_logits,
                                                              int32_t* pool_state, size_t smem_limit) {
   extern __shared__ __align__(128) unsigned char sm[];
@@ -570,9 +572,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   const int g = lane >> 2, t4 = lane & 3;
   const int G = gridDim.x, c = blockIdx.x;
   const int H = a.H, I = a.I, E = a.E, k = a.k, T = ONE ? 1 : a.T, NS = I / 16, NSh = a.n_shared;
-  // weight format (the one-token variant serves the linear format only)
-  const int fmt = ONE ? 0 : a.fmt;
-  const uint32_t lut = fmt == 1 ? codebook_lut(threadIdx.x & 31) : 0u;
+  constexpr int fmt = FMT;
+  const uint32_t lut = FMT == 1 ? codebook_lut(threadIdx.x & 31) : 0u;
   const Plan PL = make_plan(H, I, E, k, T, G, smem_limit);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PL.bars);
   Ring R;
@@ -824,7 +825,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       // the warp's h stores happen before lane 0's release through the warp
       // barrier (no per-thread fence: the release covers them)
       __syncwarp();
-      if (lane == 0) red_release_add(&cnt_cur[xi], 1u);
+      if (lane == 0) red_release_add(&cnt_cur[xi * kCntPad], 1u);
     }
     named_sync(1 + grp, kGroupWarps * 32);
   };
@@ -1090,6 +1091,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     if (grp < R.gs)
       for (int m = grp; m < n_my; m += R.gs) gateup_task(m);
   }
+  // Missed experts read from host memory: the warps with no gate/up group
+  // (and no producer lane) pull this CTA's down strips of the first ds
+  // entries now, while the gate/up phase runs; the down strips do not
+  // depend on h, so the host-link round trip leaves the down phase.
+  const int pw0 = R.gs * kGroupWarps, npw = kProdWarp - pw0;
+  if (!ONE && has_dn && a.pull && warp >= pw0 && warp < kProdWarp) {
+    for (int xi = warp - pw0; xi < n_ex && xi < R.ds; xi += npw) {
+      const Task tk = task_of(a, L, xi, NSh);
+      if (!tk.src) continue;
+      const size_t off = (size_t)down_base(H, I) + (size_t)c * R.dn_bytes;
+      pull_strip(tk.src + off, const_cast<uint8_t*>(tk.base) + off, R.dn + xi * R.dn_pitch, R.dn_bytes, lane, 32);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&R.full_dn[xi]);
+    }
+  }
   // every gate/up copy must be issued before the block barrier below: a
   // group may still be waiting for one that only the producer can issue
   if (is_prod) {
@@ -1144,7 +1160,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       const int s = xi % R.ds;
       if (lane == 0) {
         int spins = 0;
-        while (ld_acquire_gpu_u32(&cnt_cur[xi]) < (uint32_t)NS) {
+        while (ld_acquire_gpu_u32(&cnt_cur[xi * kCntPad]) < (uint32_t)NS) {
           if (is_prod) pump(P, X);
           if (((++spins) & 15) == 0) {
             if (global_ns() > deadline) { set_error(a, MOE_ERR_TIMEOUT); break; }
@@ -1154,13 +1170,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         }
       }
       __syncwarp();
-      if (!ONE && tk.src) {  // a missed expert read from host memory by this warp
+      if (!ONE && tk.src && !(xi < R.ds && npw > 0)) {  // a miss not pulled early: read it now
         const size_t off = (size_t)down_base(H, I) + (size_t)c * R.dn_bytes;
         pull_strip(tk.src + off, const_cast<uint8_t*>(tk.base) + off, R.dn + s * R.dn_pitch, R.dn_bytes, lane, 32);
         __syncwarp();
         if (lane == 0) mbar_arrive(&R.full_dn[s]);
       }
-      const bool staged = tk.cnt <= hb_rows;
+      const bool staged = ONE || tk.cnt <= hb_rows;  // one token always fits
       if (staged) {
         const int per_row = I / 8;
         for (int o = lane; o < tk.cnt * per_row; o += 32) {
@@ -1279,17 +1295,19 @@ cudaError_t decode_configure() {
   e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
   cudaFuncAttributes fa;
-  e = cudaFuncGetAttributes(&fa, decode_kernel<false>);
-  if (e != cudaSuccess) return e;
-  cudaFuncAttributes fa1;
-  e = cudaFuncGetAttributes(&fa1, decode_kernel<true>);
-  if (e != cudaSuccess) return e;
-  const size_t st = fa.sharedSizeBytes > fa1.sharedSizeBytes ? fa.sharedSizeBytes : fa1.sharedSizeBytes;
+  const void* variants[3] = {(const void*)decode_kernel<true, 0>, (const void*)decode_kernel<false, 0>,
+                             (const void*)decode_kernel<false, 1>};
+  size_t st = 0;
+  for (const void* f : variants) {
+    e = cudaFuncGetAttributes(&fa, f);
+    if (e != cudaSuccess) return e;
+    st = fa.sharedSizeBytes > st ? fa.sharedSizeBytes : st;
+  }
   const size_t limit = (size_t)optin - st;
-  e = cudaFuncSetAttribute(decode_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(decode_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
-  if (e != cudaSuccess) return e;
+  for (const void* f : variants) {
+    e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)limit);
+    if (e != cudaSuccess) return e;
+  }
   g_decode_smem_limit = limit;
   // whether a cooperative launch may also carry programmatic serialization:
   // two launches of an empty kernel on a private stream (a refusal is a
@@ -1332,8 +1350,10 @@ cudaError_t launch_decode(const LayerArgs& a, unsigned long long* tagged_logits,
                                          attr, pdl);
   // one token per call, linear weights: one key per lane in top-k
   const bool one = a.T == 1 && !a.pool && a.E <= 16 * 32 && a.fmt == 0;
-  return one ? cudaLaunchKernelEx(&cfg, decode_kernel<true>, a, tagged_logits, pool_state, g_decode_smem_limit)
-             : cudaLaunchKernelEx(&cfg, decode_kernel<false>, a, tagged_logits, pool_state, g_decode_smem_limit);
+  if (one) return cudaLaunchKernelEx(&cfg, decode_kernel<true, 0>, a, tagged_logits, pool_state, g_decode_smem_limit);
+  if (a.fmt == 1)
+    return cudaLaunchKernelEx(&cfg, decode_kernel<false, 1>, a, tagged_logits, pool_state, g_decode_smem_limit);
+  return cudaLaunchKernelEx(&cfg, decode_kernel<false, 0>, a, tagged_logits, pool_state, g_decode_smem_limit);
 }
 
 }  // namespace moe

@@ -41,6 +41,7 @@ constexpr int kMaxExperts = 4096;
 constexpr int kMaxHidden = 4096;
 constexpr int kMaxInter = 4096;
 constexpr int kRingSize = 4096;
+constexpr int kCntPad = 32;  // u32 per 128-byte line: each expert's counter has a cache line of its own
 constexpr uint32_t kReadyError = 0x80000000u;  // OR-ed into a ready flag when the copy failed
 
 // Byte offsets inside one expert in GPU layout.
@@ -57,18 +58,25 @@ __host__ __device__ inline int frag_pos(int k) {
 }
 
 // Device-resident per-layer state.
-struct DevState {
+// Three cache lines: the step state (read by every CTA at kernel start and
+// written once per call), the sticky error (polled inside bounded waits) and
+// the statistics (atomics), so that polling one never contends with writes
+// to another.
+struct alignas(128) DevState {
   uint32_t step;      // routing steps done; the current step's sequence number after increment
   uint32_t ticket;    // arrival counter of the route kernel's CTAs
-  int32_t error;      // sticky error (moe_status_t value), 0 = none
   int32_t n_union;    // distinct routed experts of the current step
   int32_t n_miss;     // misses of the current step
   uint32_t ring_head; // doorbell entries written so far
   uint32_t dstep;     // fused decode calls so far (tags the logits they publish)
-  int32_t pad;
+  int32_t pad0[26];
+  int32_t error;      // sticky error (moe_status_t value), 0 = none
+  int32_t pad1[31];
   unsigned long long forwards, hits, misses, wait_ns;
   unsigned long long rechecks;  // prefill: experts whose logit was recomputed exactly near the top-k boundary
+  unsigned long long pad2[11];
 };
+static_assert(sizeof(DevState) == 384, "DevState: three 128-byte lines");
 
 struct RingEntry {
   uint32_t seq;
@@ -102,7 +110,7 @@ struct LayerArgs {
   HostMapped* hm;  // device address of the mapped host block
   uint32_t* ready;       // [E] per slot: step whose copy has landed (host copy server)
   float* logits;        // [T][E] tensor-core router output (prefill path)
-  unsigned long long* keys;  // [T <= 64][E] router keys of the batched path (moe_route.cuh)
+  float* wnorm;         // [E] router row norms (batched path's error bound)
   __half* x16;          // [T][H] B-fragment order
   int32_t* u_expert;    // [Umax]
   int32_t* u_slot;      // [Umax]
@@ -125,8 +133,8 @@ struct LayerArgs {
   uint16_t* xhat_out;      // bf16 [T][H]: the normalised layer input
   float eps;
   unsigned long long wait_timeout_ns;
-  uint32_t* counters;   // [2][cnt_stride] gate/up completion counts, by step parity
-  int cnt_stride;       // max distinct experts per call + 2
+  uint32_t* counters;   // [2][cnt_stride] gate/up completion counts, by step parity, one per 128-byte line
+  int cnt_stride;       // (max distinct experts per call + 2) * kCntPad
   // L2 warm-up for the layer that runs next (moe_set_next_layer): its router
   // rows and shared expert, and the listed experts in its resident slots.
   // A cache hint only: results never depend on it.  nx_W_r null = none.
@@ -144,13 +152,13 @@ constexpr int kMaxHotExperts = 64;
 // Launch helpers (moe_kernels.cu).  All return cudaSuccess or the launch error.
 cudaError_t launch_route(const LayerArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_gateup(const LayerArgs& a, cudaStream_t s, bool pdl, int grid);
-cudaError_t launch_down(const LayerArgs& a, cudaStream_t s, bool pdl, int grid);
+cudaError_t launch_down(const LayerArgs& a, cudaStream_t s, bool pdl, int nw);
 cudaError_t launch_residual_rmsnorm(const uint16_t* x, const uint16_t* y, int T, int H, float eps, uint16_t* x_out,
                                     uint16_t* xhat, cudaStream_t s);
 size_t route_smem_bytes(int H, int E);
 cudaError_t configure_kernels(int H, int E);
-int gateup_max_blocks_per_sm(int T);
-int down_max_blocks_per_sm(int T);
+int gateup_max_blocks_per_sm(int H);
+int down_warps(int T, int k, int n_shared, int I);
 
 // Fused single-launch decode path (moe_decode.cu), T <= 8.
 size_t decode_smem_bytes(int H, int I, int E, int k, int T, int G);

@@ -482,16 +482,15 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
     off += align256(bytes);
     return o;
   };
-  const int Tl = Tm > kMaxTokens ? Tm : 1;   // fp32 logits: the prefill path only
+  const int Tl = Tm;                         // fp32 logits: the batched path (any T the fused kernel declines), prefill
   const int Tk = Tb > 8 ? Tb : 8;            // the fused kernel publishes 8 token rows every call
   const size_t o_st = carve(sizeof(DevState)), o_ready = carve(4ull * E), o_logits = carve(4ull * Tl * E),
-               o_keys = carve(8ull * Tb * E),
                o_x16 = carve(2ull * Tb * H), o_uexp = carve(4ull * Um), o_uslot = carve(4ull * Um),
                o_uoff = carve(4ull * (Um + 1)), o_ptok = carve(4 * P),
                o_pw = carve(4 * P), o_tku = carve(4 * P), o_tkpos = carve(4 * P),
                o_h16 = carve(2ull * (P + Tb) * I), o_tki = carve(4ull * Tm * k), o_tkw = carve(4ull * Tm * k),
-               o_bar = carve(8ull * Tk * E), o_cnt = carve(8ull * (Um + 2)), o_pool = carve(4ull * 2 * 3 * E),
-               o_hot = carve(4ull * kMaxHotExperts);
+               o_bar = carve(8ull * Tk * E), o_cnt = carve(8ull * (Um + 2) * kCntPad), o_pool = carve(4ull * 2 * 3 * E),
+               o_hot = carve(4ull * kMaxHotExperts), o_wnorm = carve(4ull * E);
   if (cudaMalloc(&L->dev_block, off) != cudaSuccess) {
     L->dev_block = nullptr;
     return fail(MOE_ERR_OUT_OF_MEMORY);
@@ -512,7 +511,7 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.hm = L->hm_dev;
   a.ready = (uint32_t*)(b + o_ready);
   a.logits = (float*)(b + o_logits);
-  a.keys = (unsigned long long*)(b + o_keys);
+  a.wnorm = (float*)(b + o_wnorm);
   a.x16 = (__half*)(b + o_x16);
   a.u_expert = (int32_t*)(b + o_uexp);
   a.u_slot = (int32_t*)(b + o_uslot);
@@ -530,7 +529,7 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.fmt = d.weight_format;
   L->tagged_logits = (unsigned long long*)(b + o_bar);
   a.counters = (uint32_t*)(b + o_cnt);
-  a.cnt_stride = Um + 2;
+  a.cnt_stride = (Um + 2) * kCntPad;
   L->pool_state = (int32_t*)(b + o_pool);
   L->hot_dev = (int32_t*)(b + o_hot);
   if (decode_configure() != cudaSuccess) return fail(MOE_ERR_CUDA);
@@ -723,13 +722,13 @@ moe_status_t forward_impl(moe_layer_t* L, const void* x, int32_t T, void* y, int
   }
   const int Um = L->d.n_experts < T * L->d.top_k ? L->d.n_experts : T * L->d.top_k;
   const int max_tasks = (L->d.n_shared + Um) * (L->d.inter / 16);
-  int gu_grid = L->sm_count * gateup_max_blocks_per_sm(T);
+  int gu_grid = L->sm_count * gateup_max_blocks_per_sm(L->d.hidden);
   if (gu_grid > max_tasks) gu_grid = max_tasks;
-  int dn_grid = L->sm_count * down_max_blocks_per_sm(T);
-  if (dn_grid > L->d.hidden / 16) dn_grid = L->d.hidden / 16;
+  const int dn_warps = down_warps(T, L->d.top_k, L->d.n_shared, L->d.inter);
+  if (dn_warps < 1) return MOE_ERR_UNSUPPORTED;
   if (launch_route(a, s, true) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_gateup(a, s, true, gu_grid) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_down(a, s, true, dn_grid) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_down(a, s, true, dn_warps) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
