@@ -1166,7 +1166,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
             if (global_ns() > deadline) { set_error(a, MOE_ERR_TIMEOUT); break; }
             if (dev_error(a)) break;
           }
-          __nanosleep(32);
+          // no __nanosleep here: a sleeping warp was measured to wake up
+          // microseconds late now and then, which delayed the whole layer
         }
       }
       __syncwarp();
