@@ -238,7 +238,12 @@ MOE_API moe_status_t moe_forward_norm(moe_layer_t* layer, const void* x_bf16_dev
  * at moe_forward_norm), enqueued on the stream:
  *   x_out   = bf16(x + y)                 (y may be NULL: x_out = x)
  *   xhat    = bf16(x_out / sqrt(mean(x_out^2) + eps))   (no learned weight)
- * All device bf16 [T][H]; x_out may alias x; xhat must not alias the others.
+ * All device bf16 [T][H], 16-byte aligned, H a multiple of 8; x_out may alias
+ * x; xhat must not alias the others.  Per token, 256 threads take 8-element
+ * chunks (thread v: chunks v, v + 256, ...), accumulate the squares in
+ * element order, then a warp butterfly and the 8 warp sums in order.
+ * Errors: INVALID_ARG (NULL x/xhat, bad sizes, eps < 0 or NaN, misalignment,
+ * aliasing), CUDA.
  */
 MOE_API moe_status_t moe_residual_rmsnorm(const void* x_bf16_dev, const void* y_bf16_dev, int32_t T, int32_t hidden,
                                           float eps, void* x_out_bf16_dev, void* xhat_bf16_dev, void* cuda_stream);

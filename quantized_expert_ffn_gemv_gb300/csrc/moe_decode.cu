@@ -43,6 +43,7 @@
 #include "moe.h"
 #include "moe_internal.h"
 #include "moe_mma.cuh"
+#include "moe_norm.cuh"
 #include "moe_route.cuh"
 
 namespace moe {
@@ -656,23 +657,31 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   __shared__ float s_inv[kMaxT];
   if (a.resid) {
     // Fused pre-norm: xs = bf16(resid + y_prev) into xraw, and each token's
-    // sum of squares in residual_rmsnorm_kernel's order (256 threads per
-    // token, thread i over elements i, i + 256, ...; xor-shuffle warp sums;
-    // the 8 warp sums in order), so the result is bit-identical to that
-    // kernel's.
+    // sum of squares in residual_rmsnorm_kernel's order (moe_norm.cuh: 256
+    // threads per token over 8-element chunks), so the result is
+    // bit-identical to that kernel's.
     float* part = red;  // [kMaxT][8]
-    for (int t0 = 0; t0 < T; t0 += kThreads / 256) {
-      const int t = t0 + tid / 256, vt = tid % 256;
+    constexpr int kC = kMaxHidden / 8 / kNormThreads;
+    const int n8 = H / 8;
+    for (int t0 = 0; t0 < T; t0 += kThreads / kNormThreads) {
+      const int t = t0 + tid / kNormThreads, vt = tid % kNormThreads;
       float ss = 0.f;
-      if (t < T)
-        for (int i = vt; i < H; i += 256) {
-          float v = __uint_as_float((uint32_t)a.resid[(size_t)t * H + i] << 16);
-          if (a.y_prev) v += __uint_as_float((uint32_t)a.y_prev[(size_t)t * H + i] << 16);
-          const uint16_t b = __bfloat16_as_ushort(__float2bfloat16_rn(v));
-          xraw[t * H + i] = b;
-          const float vr = __uint_as_float((uint32_t)b << 16);
-          ss = fmaf(vr, vr, ss);
+      if (t < T) {
+        const uint4* x4 = reinterpret_cast<const uint4*>(a.resid + (size_t)t * H);
+        const uint4* y4 = a.y_prev ? reinterpret_cast<const uint4*>(a.y_prev + (size_t)t * H) : nullptr;
+        uint4 xv[kC], yv[kC];  // every load first: one round trip
+#pragma unroll
+        for (int cc = 0; cc < kC; ++cc) {
+          const int i = vt + kNormThreads * cc;
+          xv[cc] = i < n8 ? x4[i] : make_uint4(0u, 0u, 0u, 0u);
+          yv[cc] = (y4 && i < n8) ? y4[i] : make_uint4(0u, 0u, 0u, 0u);
         }
+#pragma unroll
+        for (int cc = 0; cc < kC; ++cc) {
+          const int i = vt + kNormThreads * cc;
+          if (i < n8) reinterpret_cast<uint4*>(xraw + (size_t)t * H)[i] = resid_chunk(xv[cc], yv[cc], y4 != nullptr, ss);
+        }
+      }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
       if (lane == 0 && t < T) part[t * 8 + vt / 32] = ss;
@@ -694,16 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       if (a.resid) {
         // xhat = bf16(xs * inv); this CTA writes its share of xs and xhat out
         const uint4 xs = *reinterpret_cast<const uint4*>(xraw + t * H + k8);
-        const float inv = s_inv[t];
-        const uint32_t xw[4] = {xs.x, xs.y, xs.z, xs.w};
-        uint32_t hw[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(xw[i] << 16) * inv));
-          const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(xw[i] & 0xFFFF0000u) * inv));
-          hw[i] = lo | (hi << 16);
-        }
-        v = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        v = scale_chunk(xs, s_inv[t]);
         if (o % G == c) {
           if (a.x_out) *reinterpret_cast<uint4*>(a.x_out + (size_t)t * H + k8) = xs;
           *reinterpret_cast<uint4*>(a.xhat_out + (size_t)t * H + k8) = v;
@@ -762,8 +762,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         key = logit_key(pr[0], pr[kMaxT], pr[2 * kMaxT], pr[3 * kMaxT], bias_v);
       }
       // key and call tag in one 64-bit word: a reader that sees this call's
-      // tag sees this call's key (no fence, no grid barrier)
+      // tag sees this call's key
       st_relaxed_u64(&tagged_logits[(size_t)t * E + e], (unsigned long long)((key << 12) | tag));
+    }
+    // one release per CTA once its rows are out: readers wait for all G
+    // releases of this call on one counter (one polling lane per CTA) and
+    // then read every key once, instead of every lane polling its keys'
+    // lines (which slowed some CTAs' loads by microseconds)
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      red_release_add(a.pub, 1u);
     }
   }
 
@@ -845,6 +854,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   if (tid < kMaxT) TS.nsurv[tid] = 0;
   if (c == 0)  // the other parity's counters, for the next call
     for (int i = tid; i < a.cnt_stride; i += kThreads) cnt_next[i] = 0u;
+  if (tid == 0) {
+    // all G CTAs of this call published: the counter reaches call * G
+    // (it only grows; the comparison survives wrap-around)
+    const uint32_t want = s_dseq * (uint32_t)G;
+    int spins = 0;
+    while ((int32_t)(ld_acquire_gpu_u32(a.pub) - want) < 0) {
+      if (((++spins) & 63) == 0 && global_ns() > deadline) {
+        set_error(a, MOE_ERR_TIMEOUT);
+        break;
+      }
+    }
+  }
+  __syncthreads();
   {
     // warps per token: 16, 8, 4 or 2 for T = 1, 2, 3-4, 5-8; each warp takes a
     // contiguous range of E / wpt experts, cpl per lane (e = base + lane + 32 j)

@@ -133,6 +133,7 @@ struct LayerArgs {
   uint16_t* xhat_out;      // bf16 [T][H]: the normalised layer input
   float eps;
   unsigned long long wait_timeout_ns;
+  uint32_t* pub;        // fused decode: router publications, G per call (own 128-byte line, only grows)
   uint32_t* counters;   // [2][cnt_stride] gate/up completion counts, by step parity, one per 128-byte line
   int cnt_stride;       // (max distinct experts per call + 2) * kCntPad
   // L2 warm-up for the layer that runs next (moe_set_next_layer): its router

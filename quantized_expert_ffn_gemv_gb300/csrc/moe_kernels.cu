@@ -26,6 +26,7 @@
 #include "moe.h"
 #include "moe_internal.h"
 #include "moe_mma.cuh"
+#include "moe_norm.cuh"
 #include "moe_route.cuh"
 
 namespace moe {
@@ -835,34 +836,46 @@ __global__ void __launch_bounds__(kDnThreads, 1) down_kernel(LayerArgs a, int nw
 
 // ------------------------------------------------------------------ residual + RMSNorm
 
-__global__ void __launch_bounds__(256) residual_rmsnorm_kernel(const uint16_t* x, const uint16_t* y, int H, float eps,
-                                                                 uint16_t* x_out, uint16_t* xhat) {
-  extern __shared__ float xs[];  // [H]
-  __shared__ float part[8];
+__global__ void __launch_bounds__(kNormThreads) residual_rmsnorm_kernel(const uint16_t* x, const uint16_t* y, int H,
+                                                                          float eps, uint16_t* x_out, uint16_t* xhat) {
+  extern __shared__ __align__(16) uint4 xs4[];  // [H / 8] bf16 chunks of x + y
+  __shared__ float part[kNormThreads / 32];
   const int t = blockIdx.x, tid = threadIdx.x;
+  constexpr int kC = kMaxHidden / 8 / kNormThreads;  // chunks per thread
+  const int n8 = H / 8;
   // programmatic dependent launch: let the next kernel start its prologue,
   // then wait for the work that wrote x and y
   pdl_trigger();
   pdl_wait();
+  const uint4* x4 = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+  const uint4* y4 = y ? reinterpret_cast<const uint4*>(y + (size_t)t * H) : nullptr;
+  uint4 xv[kC], yv[kC];  // every load of the thread first
+#pragma unroll
+  for (int c = 0; c < kC; ++c) {
+    const int i = tid + kNormThreads * c;
+    xv[c] = i < n8 ? x4[i] : make_uint4(0u, 0u, 0u, 0u);
+    yv[c] = (y4 && i < n8) ? y4[i] : make_uint4(0u, 0u, 0u, 0u);
+  }
   float ss = 0.f;
-  for (int i = tid; i < H; i += 256) {
-    float v = __uint_as_float((uint32_t)x[(size_t)t * H + i] << 16);
-    if (y) v += __uint_as_float((uint32_t)y[(size_t)t * H + i] << 16);
-    const __nv_bfloat16 b = __float2bfloat16_rn(v);
-    const float vr = __bfloat162float(b);
-    xs[i] = vr;
-    ss = fmaf(vr, vr, ss);
+#pragma unroll
+  for (int c = 0; c < kC; ++c) {
+    const int i = tid + kNormThreads * c;
+    if (i < n8) xs4[i] = resid_chunk(xv[c], yv[c], y4 != nullptr, ss);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
   if ((tid & 31) == 0) part[tid >> 5] = ss;
   __syncthreads();
   float tot = 0.f;
-  for (int w = 0; w < 8; ++w) tot += part[w];
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += part[w];
   const float inv = 1.0f / sqrtf(tot / (float)H + eps);
-  for (int i = tid; i < H; i += 256) {
-    if (x_out) x_out[(size_t)t * H + i] = __bfloat16_as_ushort(__float2bfloat16_rn(xs[i]));
-    xhat[(size_t)t * H + i] = __bfloat16_as_ushort(__float2bfloat16_rn(xs[i] * inv));
+#pragma unroll
+  for (int c = 0; c < kC; ++c) {
+    const int i = tid + kNormThreads * c;
+    if (i < n8) {
+      if (x_out) reinterpret_cast<uint4*>(x_out + (size_t)t * H)[i] = xs4[i];
+      reinterpret_cast<uint4*>(xhat + (size_t)t * H)[i] = scale_chunk(xs4[i], inv);
+    }
   }
 }
 
@@ -932,7 +945,7 @@ cudaError_t configure_kernels(int H, int E) {
     g_down_smem = (size_t)optin - fa.sharedSizeBytes;
   }
   e = cudaFuncSetAttribute(residual_rmsnorm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)(sizeof(float) * kMaxHidden));
+                           (int)(2 * kMaxHidden));
   (void)H;
   (void)E;
   return e;
@@ -992,8 +1005,8 @@ cudaError_t launch_residual_rmsnorm(const uint16_t* x, const uint16_t* y, int T,
                                     uint16_t* xhat, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(T);
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = sizeof(float) * H;
+  cfg.blockDim = dim3(kNormThreads);
+  cfg.dynamicSmemBytes = 2 * (size_t)H;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

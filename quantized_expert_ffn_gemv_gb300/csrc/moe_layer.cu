@@ -490,7 +490,8 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
                o_pw = carve(4 * P), o_tku = carve(4 * P), o_tkpos = carve(4 * P),
                o_h16 = carve(2ull * (P + Tb) * I), o_tki = carve(4ull * Tm * k), o_tkw = carve(4ull * Tm * k),
                o_bar = carve(8ull * Tk * E), o_cnt = carve(8ull * (Um + 2) * kCntPad), o_pool = carve(4ull * 2 * 3 * E),
-               o_hot = carve(4ull * kMaxHotExperts), o_wnorm = carve(4ull * E);
+               o_hot = carve(4ull * kMaxHotExperts), o_wnorm = carve(4ull * E),
+               o_pub = carve(128);
   if (cudaMalloc(&L->dev_block, off) != cudaSuccess) {
     L->dev_block = nullptr;
     return fail(MOE_ERR_OUT_OF_MEMORY);
@@ -508,6 +509,7 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.shared = L->shared_dev;
   a.blob = L->blob;
   a.st = (DevState*)(b + o_st);
+  a.pub = (uint32_t*)(b + o_pub);
   a.hm = L->hm_dev;
   a.ready = (uint32_t*)(b + o_ready);
   a.logits = (float*)(b + o_logits);
@@ -761,6 +763,8 @@ moe_status_t moe_residual_rmsnorm(const void* x, const void* y, int32_t T, int32
                                   void* xhat, void* stream) {
   if (!x || !xhat || T < 1 || hidden < 1 || hidden > kMaxHidden || !(eps >= 0.f)) return MOE_ERR_INVALID_ARG;
   if (xhat == x || (y && xhat == y) || (x_out && xhat == x_out)) return MOE_ERR_INVALID_ARG;
+  if ((((uintptr_t)x | (uintptr_t)y | (uintptr_t)x_out | (uintptr_t)xhat) & 15) || hidden % 8)
+    return MOE_ERR_INVALID_ARG;
   if (launch_residual_rmsnorm((const uint16_t*)x, (const uint16_t*)y, T, hidden, eps, (uint16_t*)x_out,
                               (uint16_t*)xhat, (cudaStream_t)stream) != cudaSuccess)
     return MOE_ERR_CUDA;
