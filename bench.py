@@ -111,7 +111,7 @@ def source_hash():
     only while the kernel it was measured on is unchanged."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_expert_ffn_gemv_gb300", "csrc")
-    for f in ("moe_decode.cu", "moe_internal.h", "moe_mma.cuh", "moe_route.cuh"):
+    for f in ("moe_decode.cu", "moe_internal.h", "moe_mma.cuh", "moe_route.cuh", "moe_norm.cuh"):
         h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
@@ -687,7 +687,7 @@ def run_single(args):
     __graft_entry__.build()
     from quantized_expert_ffn_gemv_gb300 import moe, synth
     torch.cuda.set_device(0)
-    n = C2_REPLICAS if args.workload == "decode" else 4
+    n = (args.replicas or C2_REPLICAS) if args.workload == "decode" else 4
     mt = 1 if args.workload == "decode" else PREFILL_T
     layers = []
     for l in range(n):
@@ -697,7 +697,7 @@ def run_single(args):
     x_host = synth.activations(synth.PAGE, 1000, 0, PREFILL_T, stream=9)
     x_dev = torch.from_numpy(x_host.view(np.int16)).view(torch.bfloat16).cuda()
     if args.workload == "decode":
-        ms, _, _, _ = decode_launch_time(torch, layers, x_dev, C2_TOKENS)
+        ms, _, _, _ = decode_launch_time(torch, layers, x_dev, args.tokens or C2_TOKENS)
         pk = peaks()
         out = {"workload": "c2 decode", "tokens_per_s": 1e3 / ms, "us_per_token": ms * 1e3,
                "frac": STEP_BYTES_PER_TOKEN / (ms * 1e-3) / 1e9 / pk["hbm_gbs"]}
@@ -724,6 +724,9 @@ def main():
                          "layer, batch 1; prefill: one 4096-token chunk; batched: calls of --batch tokens")
     ap.add_argument("--batch", type=int, default=8, help="tokens per call for --workload batched (2..64)")
     ap.add_argument("--hot", type=int, default=0, help="hot experts per layer the previous layer warms in L2")
+    ap.add_argument("--replicas", type=int, default=0, help="--workload decode: layer replicas (default 8; 1 for a "
+                                                              "small profiling case)")
+    ap.add_argument("--tokens", type=int, default=0, help="--workload decode: tokens per graph (default 1000)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

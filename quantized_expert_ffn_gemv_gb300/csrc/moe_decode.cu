@@ -770,10 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     // then read every key once, instead of every lane polling its keys'
     // lines (which slowed some CTAs' loads by microseconds)
     __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      red_release_add(a.pub, 1u);
-    }
+    if (tid == 0) red_release_add(a.pub, 1u);  // cumulative over the CTA's stores before the barrier
   }
 
   // ---- gate/up of one strip by a group of four warps (K split four ways)
