@@ -831,7 +831,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       // the warp's h stores happen before lane 0's release through the warp
       // barrier (no per-thread fence: the release covers them)
       __syncwarp();
-      if (lane == 0) red_release_add(&cnt_cur[xi * kCntPad], 1u);
+      if (lane == 0) red_release_add(&cnt_cur[(xi * (NS / 4) + strip / 4) * kCntPad], 1u);
     }
     named_sync(1 + grp, kGroupWarps * 32);
   };
@@ -1177,44 +1177,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     for (int xi = warp; xi < n_ex; xi += R.ds) {
       const Task tk = task_of(a, L, xi, NSh);
       const int s = xi % R.ds;
-      if (lane == 0) {
-        int spins = 0;
-        while (ld_acquire_gpu_u32(&cnt_cur[xi * kCntPad]) < (uint32_t)NS) {
-          if (is_prod) pump(P, X);
-          if (((++spins) & 15) == 0) {
-            if (global_ns() > deadline) { set_error(a, MOE_ERR_TIMEOUT); break; }
-            if (dev_error(a)) break;
-          }
-          // no __nanosleep here: a sleeping warp was measured to wake up
-          // microseconds late now and then, which delayed the whole layer
-        }
-      }
-      __syncwarp();
       if (!ONE && tk.src && !(xi < R.ds && npw > 0)) {  // a miss not pulled early: read it now
         const size_t off = (size_t)down_base(H, I) + (size_t)c * R.dn_bytes;
         pull_strip(tk.src + off, const_cast<uint8_t*>(tk.base) + off, R.dn + s * R.dn_pitch, R.dn_bytes, lane, 32);
         __syncwarp();
         if (lane == 0) mbar_arrive(&R.full_dn[s]);
       }
-      const bool staged = ONE || tk.cnt <= hb_rows;  // one token always fits
-      if (staged) {
-        const int per_row = I / 8;
-        for (int o = lane; o < tk.cnt * per_row; o += 32) {
-          const int r = o / per_row, cc = o - r * per_row;
-          cp_async16(hbuf + r * hstride + cc * 8, a.h16 + (size_t)(tk.poff + r) * I + cc * 8);
-        }
-        cp_async_wait_all();
-        __syncwarp();
-      }
       const bool ok = __all_sync(0xffffffffu, wait_full(&R.full_dn[s], (xi / R.ds) & 1, deadline, is_prod, P, X));
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      if (ok) {
-        const unsigned char* sb = R.dn + s * R.dn_pitch;
-        const int gsel = (g < tk.cnt) ? g : 0;
+      const unsigned char* sb = R.dn + s * R.dn_pitch;
+      const int gsel = (g < tk.cnt) ? g : 0;
+      const bool staged = ONE || tk.cnt <= hb_rows;  // one token always fits
+      // The K range of the down product comes in 64-wide chunks (four gate/up
+      // strips each, one counter each): the warp multiplies every chunk whose
+      // h is complete, in chunk order, while later strips are still being
+      // computed elsewhere; the accumulation order is the same as for one
+      // pass over all of K.
+      const uint32_t* cnt_x = cnt_cur + (size_t)xi * nst * kCntPad;
+      int done = 0, spins = 0;
+      bool alive = ok;
+      while (alive && done < nst) {
+        const int ch = done + lane;
+        const bool rdy = ch < nst && ld_acquire_gpu_u32(&cnt_x[(size_t)ch * kCntPad]) >= 4u;
+        const unsigned m = __ballot_sync(0xffffffffu, rdy);
+        const int nr = (m == 0xffffffffu) ? 32 : __ffs(~m) - 1;  // chunks ready, in order from done
+        if (nr == 0) {
+          if (is_prod) pump(P, X);
+          bool stop = false;
+          if (((++spins) & 15) == 0) {
+            if (global_ns() > deadline) {
+              if (lane == 0) set_error(a, MOE_ERR_TIMEOUT);
+              stop = true;
+            } else if (dev_error(a)) {
+              stop = true;
+            }
+          }
+          // no __nanosleep here: a sleeping warp was measured to wake up
+          // microseconds late now and then, which delayed the whole layer
+          alive = !__any_sync(0xffffffffu, stop);
+          continue;
+        }
+        __syncwarp();  // the lanes' acquires order every lane's h reads below
         if (staged) {
+          const int per_row = nr * 8;  // 16-byte pieces of the ready chunks, per token row
+          for (int o = lane; o < tk.cnt * per_row; o += 32) {
+            const int r = o / per_row, rem = o - r * per_row;
+            const int col = done * 64 + rem * 8;
+            cp_async16(hbuf + r * hstride + col, a.h16 + (size_t)(tk.poff + r) * I + col);
+          }
+          cp_async_wait_all();
+          __syncwarp();
           const __half* hb = hbuf + gsel * hstride + t4 * 16;
-#pragma unroll 4
-          for (int st = 0; st < nst; ++st) {
+#pragma unroll 2
+          for (int st = done; st < done + nr; ++st) {
             const uint4 b01 = *reinterpret_cast<const uint4*>(hb + st * 64);
             const uint4 b23 = *reinterpret_cast<const uint4*>(hb + st * 64 + 8);
             const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
@@ -1224,7 +1239,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         } else {
           const int hrow = tk.poff + gsel;
 #pragma unroll 2
-          for (int st = 0; st < nst; ++st) {
+          for (int st = done; st < done + nr; ++st) {
             const __half* hr = a.h16 + (size_t)hrow * I + st * 64 + t4 * 16;
             const uint4 b01 = __ldcg(reinterpret_cast<const uint4*>(hr));
             const uint4 b23 = __ldcg(reinterpret_cast<const uint4*>(hr + 8));
@@ -1233,6 +1248,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
             supertile_mma(acc, nb, scv, b01, b23, fmt, lut);
           }
         }
+        done += nr;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&R.empty_dn[s]);

@@ -41,7 +41,7 @@ constexpr int kMaxExperts = 4096;
 constexpr int kMaxHidden = 4096;
 constexpr int kMaxInter = 4096;
 constexpr int kRingSize = 4096;
-constexpr int kCntPad = 32;  // u32 per 128-byte line: each expert's counter has a cache line of its own
+constexpr int kCntPad = 32;  // u32 per 128-byte line: each counter has a cache line of its own
 constexpr uint32_t kReadyError = 0x80000000u;  // OR-ed into a ready flag when the copy failed
 
 // Byte offsets inside one expert in GPU layout.
@@ -134,8 +134,9 @@ struct LayerArgs {
   float eps;
   unsigned long long wait_timeout_ns;
   uint32_t* pub;        // fused decode: router publications, G per call (own 128-byte line, only grows)
-  uint32_t* counters;   // [2][cnt_stride] gate/up completion counts, by step parity, one per 128-byte line
-  int cnt_stride;       // (max distinct experts per call + 2) * kCntPad
+  uint32_t* counters;   // [2][cnt_stride] gate/up strips done per (expert, 64-wide chunk of I), by step parity,
+                        // one counter per 128-byte line
+  int cnt_stride;       // (max distinct experts per call + 2) * (I / 64) * kCntPad
   // L2 warm-up for the layer that runs next (moe_set_next_layer): its router
   // rows and shared expert, and the listed experts in its resident slots.
   // A cache hint only: results never depend on it.  nx_W_r null = none.

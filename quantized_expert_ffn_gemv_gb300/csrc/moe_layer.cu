@@ -489,7 +489,7 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
                o_uoff = carve(4ull * (Um + 1)), o_ptok = carve(4 * P),
                o_pw = carve(4 * P), o_tku = carve(4 * P), o_tkpos = carve(4 * P),
                o_h16 = carve(2ull * (P + Tb) * I), o_tki = carve(4ull * Tm * k), o_tkw = carve(4ull * Tm * k),
-               o_bar = carve(8ull * Tk * E), o_cnt = carve(8ull * (Um + 2) * kCntPad), o_pool = carve(4ull * 2 * 3 * E),
+               o_bar = carve(8ull * Tk * E), o_cnt = carve(8ull * (Um + 2) * (I / 64) * kCntPad), o_pool = carve(4ull * 2 * 3 * E),
                o_hot = carve(4ull * kMaxHotExperts), o_wnorm = carve(4ull * E),
                o_pub = carve(128);
   if (cudaMalloc(&L->dev_block, off) != cudaSuccess) {
@@ -531,7 +531,7 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.fmt = d.weight_format;
   L->tagged_logits = (unsigned long long*)(b + o_bar);
   a.counters = (uint32_t*)(b + o_cnt);
-  a.cnt_stride = (Um + 2) * kCntPad;
+  a.cnt_stride = (Um + 2) * (I / 64) * kCntPad;
   L->pool_state = (int32_t*)(b + o_pool);
   L->hot_dev = (int32_t*)(b + o_hot);
   if (decode_configure() != cudaSuccess) return fail(MOE_ERR_CUDA);
