@@ -101,6 +101,10 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
@@ -152,7 +156,7 @@ __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
 
 struct Plan {
   int rows_max, umax, gu_stages, dn_stages;
-  size_t bars, x16, xraw, regA, gu, dn, red, lists, total;
+  size_t bars, x16, xraw, regA, gu, dn, red, lists, pooltab, total;
 };
 
 __host__ __device__ inline size_t al128(size_t v) { return (v + 127) & ~size_t(127); }
@@ -189,6 +193,10 @@ __host__ __device__ inline Plan plan_with(int H, int I, int E, int k, int T, int
   o += al128((size_t)kWarps * 32 * 8 * 4);
   p.lists = o;
   o += al128((size_t)T * k * 4 * 5 + (size_t)(p.umax + 2) * 4 * 4 + 64 * 8);
+  // a pooled call's slot table, slot owners and stamps (S <= E), loaded
+  // while the router and the top-k run
+  p.pooltab = o;
+  o += al128((size_t)E * 12);
   p.total = o;
   return p;
 }
@@ -729,6 +737,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   __syncthreads();
   const uint32_t seq = s_seq;
   const uint32_t tag = s_dseq & kTagMask;  // this call's tag on the published logits
+  // Pooled call: this step's slot table, owners and stamps start for shared
+  // memory now (written by the previous call, complete at the wait above);
+  // the hit check after the top-k then needs no round trip to L2.
+  int* slot_s = reinterpret_cast<int*>(sm + PL.pooltab);
+  int* own_s = slot_s + E;
+  uint32_t* stp_s = reinterpret_cast<uint32_t*>(own_s + a.n_slots);
+  if (!ONE && a.pool) {
+    const int32_t* pre = pool_state + (size_t)(seq & 1u) * (E + 2 * a.n_slots);
+    for (int i = tid; i < E + 2 * a.n_slots; i += kThreads) cp_async4(slot_s + i, pre + i);
+    cp_async_commit();
+  }
   uint32_t* cnt_cur = a.counters + (size_t)(seq & 1u) * a.cnt_stride;
   uint32_t* cnt_next = a.counters + (size_t)((seq + 1u) & 1u) * a.cnt_stride;
 
@@ -845,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   // Early path (one token, every expert resident): the experts start right
   // after the selection; a warp with no gate/up or down role finishes the
   // softmax, the combine mapping and the statistics meanwhile.
-  const bool early = ONE || (T == 1 && !a.pool);
+  const bool early = ONE || T == 1;
   const int fin_warp = R.gs < kMaxGuStages ? R.gs * kGroupWarps : 0;
   for (int e = tid; e < E; e += kThreads) tokmask[e] = 0ull;
   if (tid < kMaxT) TS.nsurv[tid] = 0;
@@ -966,9 +985,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   // slot hit check: identity when every expert is resident, else LRU on the
   // double-buffered pool state (every CTA derives the same victims)
   const int S = a.n_slots;
-  int32_t* pre_slot = pool_state + (size_t)(seq & 1u) * (E + 2 * S);
-  int32_t* pre_owner = pre_slot + E;
-  uint32_t* pre_stamp = reinterpret_cast<uint32_t*>(pre_owner + S);
   int32_t* nxt_slot = pool_state + (size_t)((seq + 1u) & 1u) * (E + 2 * S);
   int32_t* nxt_owner = nxt_slot + E;
   uint32_t* nxt_stamp = reinterpret_cast<uint32_t*>(nxt_owner + S);
@@ -977,37 +993,52 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   } else {
     // pool scratch in region A after the routing lists: per slot owner, stamp
     // and candidate key; per union entry its miss number; the ranked victims
-    int* own_s = reinterpret_cast<int*>(sm + PL.regA + al128((size_t)E * 8) + (size_t)4 * kWarps * kMaxTopK * 8);
-    uint32_t* stp_s = reinterpret_cast<uint32_t*>(own_s + S);
-    unsigned long long* key_s = reinterpret_cast<unsigned long long*>(stp_s + S);  // 8-byte aligned: 8S bytes precede it
+    // the step's tables (slot_s, own_s, stp_s) arrived during the routing;
+    // region A after the routing lists holds the candidate keys, each union
+    // entry's miss number and the ranked victims
+    unsigned long long* key_s = reinterpret_cast<unsigned long long*>(
+        sm + PL.regA + al128((size_t)E * 8) + (size_t)4 * kWarps * kMaxTopK * 8);
     int* miss_no = reinterpret_cast<int*>(key_s + S);
     int* victim = miss_no + PL.umax + 2;
     __shared__ int s_ncand;
+    cp_async_wait_all();
+    __syncthreads();
     // this CTA's slice of the next state starts as a copy of the current one
-    // (loads issued now, stored after the decision)
+    // (read now, stored after the decision)
     const int e0 = (int)((long long)c * E / G), e1 = (int)((long long)(c + 1) * E / G);
     const int q0 = (int)((long long)c * S / G), q1 = (int)((long long)(c + 1) * S / G);
     const int ce = e0 + tid, cq = q0 + tid;
-    const int cp_slot = ce < e1 ? ld_cg_i32(&pre_slot[ce]) : 0;
-    const int cp_owner = cq < q1 ? ld_cg_i32(&pre_owner[cq]) : 0;
-    const int cp_stamp = cq < q1 ? ld_cg_i32((const int*)&pre_stamp[cq]) : 0;
+    const int cp_slot = ce < e1 ? slot_s[ce] : 0;
+    const int cp_owner = cq < q1 ? own_s[cq] : 0;
+    const int cp_stamp = cq < q1 ? (int)stp_s[cq] : 0;
     for (int u = tid; u < n_union; u += kThreads) {
-      L.u_slot[u] = ld_cg_i32(&pre_slot[L.u_expert[u]]);
+      L.u_slot[u] = slot_s[L.u_expert[u]];
       L.u_wait[u] = 0u;
     }
     if (tid == 0) s_ncand = 0;
     __syncthreads();
-    // misses in ascending expert order (the union order) get numbers 0, 1, ...
+    // misses in ascending expert order get numbers 0, 1, ... (the union is
+    // in that order, except for one token, whose union is in rank order)
     if (warp == 0) {
-      int base = 0;
-      for (int u0 = 0; u0 < n_union; u0 += 32) {
-        const int u = u0 + lane;
-        const bool m = u < n_union && L.u_slot[u] < 0;
+      if (early) {  // n_union = k <= 32: one entry per lane
+        const bool m = lane < n_union && L.u_slot[lane] < 0;
+        const int me = lane < n_union ? L.u_expert[lane] : INT_MAX;
         const unsigned b = __ballot_sync(0xffffffffu, m);
-        if (m) miss_no[u] = base + __popc(b & ((1u << lane) - 1u));
-        base += __popc(b);
+        int r = 0;
+        for (int j = 0; j < n_union; ++j) r += ((b >> j) & 1u) && L.u_expert[j] < me;
+        if (m) miss_no[lane] = r;
+        if (lane == 0) s_nmiss = __popc(b);
+      } else {
+        int base = 0;
+        for (int u0 = 0; u0 < n_union; u0 += 32) {
+          const int u = u0 + lane;
+          const bool m = u < n_union && L.u_slot[u] < 0;
+          const unsigned b = __ballot_sync(0xffffffffu, m);
+          if (m) miss_no[u] = base + __popc(b & ((1u << lane) - 1u));
+          base += __popc(b);
+        }
+        if (lane == 0) s_nmiss = base;
       }
-      if (lane == 0) s_nmiss = base;
     }
     __syncthreads();
     const int nm = s_nmiss;
@@ -1015,11 +1046,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       // candidates: empty slots first (ascending), then slots whose expert this
       // call does not use, least recently used first, ties to the lower slot
       for (int q = tid; q < S; q += kThreads) {
-        const int ow = ld_cg_i32(&pre_owner[q]);
-        const uint32_t stp = (uint32_t)ld_cg_i32((const int*)&pre_stamp[q]);
-        own_s[q] = ow;
-        stp_s[q] = stp;
-        const bool elig = ow < 0 || tokmask[ow] == 0ull;
+        const int ow = own_s[q];
+        const uint32_t stp = stp_s[q];
+        // the token masks are filled later on the one-token path: there the
+        // union (k entries) says which experts this call uses
+        bool used = false;
+        if (early) {
+          for (int j = 0; j < n_union; ++j) used |= L.u_expert[j] == ow;
+        } else {
+          used = ow >= 0 && tokmask[ow] != 0ull;
+        }
+        const bool elig = ow < 0 || !used;
         key_s[q] = elig ? (((unsigned long long)(ow >= 0) << 44) | ((unsigned long long)stp << 12) | (unsigned long long)q)
                         : ~0ull;
         if (elig) atomicAdd(&s_ncand, 1);
@@ -1044,16 +1081,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       __syncthreads();
       // CTA 0 rings the host doorbell as soon as the misses are placed
       if (c == 0 && tid == 0) {
-        int i = 0;
         const uint32_t head0 = a.st->ring_head;
         for (int u = 0; u < n_union; ++u)
-          if (L.u_wait[u] != 0u) {
-            volatile RingEntry* re = &a.hm->ring[(head0 + (uint32_t)i) % kRingSize];
+          if (L.u_wait[u] != 0u) {  // entries in ascending expert order
+            volatile RingEntry* re = &a.hm->ring[(head0 + (uint32_t)miss_no[u]) % kRingSize];
             re->seq = seq;
             re->expert = L.u_expert[u];
             re->slot = L.u_slot[u];
             re->served = a.pull ? 1u : 0u;
-            ++i;
           }
         __threadfence_system();
         a.st->ring_head = head0 + (uint32_t)nm;

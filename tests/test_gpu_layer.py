@@ -136,6 +136,28 @@ def test_residual_rmsnorm_against_oracle():
     assert ulp_off <= 16 * 2048 * 1e-3  # only values next to a rounding tie may differ
 
 
+def test_residual_rmsnorm_in_place_and_misaligned():
+    """x_out may alias x (each thread reads its chunks before it writes them);
+    a pointer off a 16-byte boundary is refused before any launch."""
+    import torch
+    from quantized_expert_ffn_gemv_gb300 import moe
+    sh = synth.PAGE
+    x = synth.activations(sh, 7, 0, 4)
+    yv = synth.activations(sh, 8, 0, 4)
+    xd, yd = to_torch_bf16(x), to_torch_bf16(yv)
+    xh = torch.empty_like(xd)
+    moe.residual_rmsnorm(xd, yd, 1e-6, xd, xh)  # in place
+    torch.cuda.synchronize()
+    got = from_torch_bf16(xd)
+    for t in range(4):
+        assert np.array_equal(got[t], oracle.residual(x[t], yv[t]))
+    buf = torch.empty(4 * 2048 + 8, dtype=torch.bfloat16, device="cuda")
+    off = buf[1:1 + 4 * 2048].view(4, 2048)  # 2 bytes past a 16-byte boundary
+    with pytest.raises(moe.MoeError) as e:
+        moe.residual_rmsnorm(off, None, 1e-6, None, xh)
+    assert e.value.code == 1
+
+
 def test_activation_out_of_fp16_range_is_reported(small):
     from quantized_expert_ffn_gemv_gb300 import moe
     x, _ = resampled_tokens(small, 0, 1)
