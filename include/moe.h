@@ -145,14 +145,26 @@ MOE_API moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t*
  * next configure call, 256-byte aligned).
  *  - n_slots == E: every expert resident.  All blobs are copied into the
  *    arena now (synchronously); no host traffic during moe_forward.
- *  - min(E, max_tokens*k) <= n_slots < E: the pool starts empty (or as
- *    moe_slot_pool_seed sets it); misses are served from the pinned host
+ *  - min(E, min(max_tokens, 8)*k) <= n_slots < E: the pool starts empty (or
+ *    as moe_slot_pool_seed sets it); misses are served from the pinned host
  *    master copy (moe_set_miss_service).  Eviction is LRU over forward
- *    calls: the misses of a call are filled in ascending expert index,
- *    taking empty slots first (ascending), then slots whose expert the call
- *    does not use, least recently used first (ties to the lower slot).
+ *    calls of at most 8 tokens: the misses of a call are filled in ascending
+ *    expert index, taking empty slots first (ascending), then slots whose
+ *    expert the call does not use, least recently used first (ties to the
+ *    lower slot).
+ *    With max_tokens > 64 a prefill call (T > 64) lends the pool's last
+ *    slots (Basalt README, section "Prompt chunks"): its scratch occupies the
+ *    last ceil(scratch / blob) slots, up to 16 slots below them stage the
+ *    touched experts the pool does not hold below the lent range (copied
+ *    from the master copy, in waves), and afterwards every lent slot gets
+ *    its expert back: the pool's table, stamps and contents are unchanged
+ *    and the call does not count as a step.  Such a call synchronizes its
+ *    stream once (after routing, to read which experts it touches), so it
+ *    cannot be captured in a CUDA graph.  Calls of 9..64 tokens are refused
+ *    (UNSUPPORTED).
  * Errors: INVALID_ARG (NULL arena, n_slots out of range), OUT_OF_MEMORY
- * when n_slots * moe_expert_bytes() > arena_bytes (the request is never
+ * when n_slots * moe_expert_bytes() > arena_bytes, or when a pool cannot
+ * lend the prefill scratch plus one staging slot (the request is never
  * shrunk), UNSUPPORTED (n_slots < E on a layer the fused decode kernel does
  * not take: more than 16 x SMs hidden rows, more than min(1024, 8 x SMs)
  * experts, or a shared-memory plan that does not fit; the layer keeps its
@@ -203,8 +215,9 @@ MOE_API moe_status_t moe_slot_pool_seed(moe_layer_t* layer, const int32_t* exper
  * A token's y depends only on its own x on the first two paths; the prefill
  * path meets the same tolerances but not bit-equality with them.
  * Errors (synchronous): INVALID_ARG (T out of 1..max_tokens, NULL x/y),
- * STATE (no pool configured, or a sticky error), UNSUPPORTED (T > 8 with a
- * slot pool of fewer than E slots), CUDA (launch failure).
+ * STATE (no pool configured, or a sticky error), UNSUPPORTED (9 <= T <= 64
+ * with a slot pool of fewer than E slots; larger T lend slots, see
+ * moe_slot_pool_configure), CUDA (launch failure).
  */
 MOE_API moe_status_t moe_forward(moe_layer_t* layer, const void* x_bf16_dev, int32_t T, void* y_bf16_dev,
                                  int32_t* topk_idx_dev, float* topk_w_dev, void* cuda_stream);

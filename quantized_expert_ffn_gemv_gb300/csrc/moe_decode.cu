@@ -869,7 +869,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   for (int e = tid; e < E; e += kThreads) tokmask[e] = 0ull;
   if (tid < kMaxT) TS.nsurv[tid] = 0;
   if (c == 0)  // the other parity's counters, for the next call
-    for (int i = tid; i < a.cnt_stride; i += kThreads) cnt_next[i] = 0u;
+    for (int i = tid; i < a.cnt_stride / kCntPad; i += kThreads) cnt_next[(size_t)i * kCntPad] = 0u;
   if (tid == 0) {
     // all G CTAs of this call published: the counter reaches call * G
     // (it only grows; the comparison survives wrap-around)

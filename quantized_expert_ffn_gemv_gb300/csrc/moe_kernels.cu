@@ -145,7 +145,8 @@ __device__ void route_finish(const LayerArgs& a, unsigned char* smem) {
   __syncthreads();
   const uint32_t seq = s_seq;
   // keep the fused decode path's gate/up counters of the next step at zero
-  for (int i = tid; i < a.cnt_stride; i += kSelThreads) a.counters[(size_t)((seq + 1u) & 1u) * a.cnt_stride + i] = 0u;
+  for (int i = tid; i < a.cnt_stride / kCntPad; i += kSelThreads)
+    a.counters[(size_t)((seq + 1u) & 1u) * a.cnt_stride + (size_t)i * kCntPad] = 0u;
 
   // ---- the tokens' selections (route_select_kernel), ascending expert index
   for (int p = tid; p < T * k; p += kSelThreads) {

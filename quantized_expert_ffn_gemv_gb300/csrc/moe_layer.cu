@@ -173,8 +173,16 @@ struct moe_layer {
   uint8_t* master = nullptr;  // pinned host, GPU layout, E experts
   uint8_t* shared_dev = nullptr;
   void* dev_block = nullptr;
-  void* pf_block = nullptr;  // prefill scratch (max_tokens > 64 only)
+  void* pf_block = nullptr;  // prefill scratch (max_tokens > 64, no slot pool)
   PrefillArgs pf{};
+  // Prefill on a pooled layer lends the pool's last slots: the scratch
+  // occupies slots [S - lend_scratch, S), the experts the call needs that are
+  // not resident below lend_first are staged through slots
+  // [lend_first, S - lend_scratch) in waves, and every lent slot's expert is
+  // copied back from the master copy after the call.
+  int lend_first = 0, lend_scratch = 0;
+  int32_t* pf_host = nullptr;        // pinned: counts [E + 1], device state, both pool tables
+  const uint8_t** pf_tables = nullptr;  // pinned: one [E] base table per wave
   PrefillMaps pf_maps{};
   TensorMapEncodeFn encode_map = nullptr;
   HostMapped* hm_host = nullptr;
@@ -369,6 +377,8 @@ void free_layer(moe_layer* L) {
     if (cs) cudaStreamDestroy(cs);
   if (L->dev_block) cudaFree(L->dev_block);
   if (L->pf_block) cudaFree(L->pf_block);
+  if (L->pf_host) cudaFreeHost(L->pf_host);
+  if (L->pf_tables) cudaFreeHost(L->pf_tables);
   if (L->shared_dev) cudaFree(L->shared_dev);
   if (L->hm_host) cudaFreeHost(L->hm_host);
   if (L->master) cudaFreeHost(L->master);
@@ -584,10 +594,73 @@ bool write_pool_state(moe_layer* L, const std::vector<int32_t>& slot_of, const s
          cudaMemcpy(L->args.ready, zeros.data(), 4ull * E, cudaMemcpyHostToDevice) == cudaSuccess;
 }
 
+}  // extern "C"
+
+namespace {
+
+constexpr int kLendStage = 16;  // slots a pooled prefill stages missing experts through
+
+// Where a layer's prefill scratch lives for its current configuration: its
+// own allocation when every expert is resident; the pool's last slots when it
+// has a pool (Basalt README, section "Prompt chunks": the prompt path's
+// buffers are carved from the expert cache's last slots and the experts in
+// them are copied back afterwards).  Refuses a pool too small to lend the
+// scratch and one staging slot (Basalt README, section "Memory floors":
+// refuse what does not fit instead of shrinking it).
+moe_status_t configure_prefill_scratch(moe_layer* L) {
+  const int H = L->d.hidden, I = L->d.inter, E = L->d.n_experts, k = L->d.top_k, Tm = L->d.max_tokens;
+  const size_t pfb = prefill_scratch_bytes(H, I, E, k, Tm);
+  L->lend_first = L->lend_scratch = 0;
+  if (!pfb) return MOE_OK;
+  const int S = L->n_slots;
+  if (L->args.pool) {
+    const int n_scr = (int)((pfb + (size_t)L->blob - 1) / (size_t)L->blob);
+    const int room = S - n_scr;
+    if (room < 1) return MOE_ERR_OUT_OF_MEMORY;
+    const int R = room < kLendStage ? room : kLendStage;
+    L->lend_scratch = n_scr;
+    L->lend_first = S - n_scr - R;
+    if (L->pf_block) {
+      cudaFree(L->pf_block);
+      L->pf_block = nullptr;
+    }
+    L->pf = prefill_carve(L->arena + (size_t)(S - n_scr) * (size_t)L->blob, H, I, E, k, Tm);
+    if (!L->pf_host &&
+        cudaHostAlloc((void**)&L->pf_host,
+                      sizeof(int32_t) * ((size_t)E + 1 + 2 * (3 * (size_t)E)) + sizeof(DevState) + 128,
+                      cudaHostAllocDefault) != cudaSuccess) {
+      L->pf_host = nullptr;
+      return MOE_ERR_OUT_OF_MEMORY;
+    }
+    if (!L->pf_tables &&
+        cudaHostAlloc((void**)&L->pf_tables, sizeof(uint8_t*) * (size_t)E * ((size_t)E + 1), cudaHostAllocDefault) !=
+            cudaSuccess) {  // one table per wave, at most E waves
+      L->pf_tables = nullptr;
+      return MOE_ERR_OUT_OF_MEMORY;
+    }
+  } else if (!L->pf_block) {
+    if (cudaMalloc(&L->pf_block, pfb) != cudaSuccess) {
+      L->pf_block = nullptr;
+      return MOE_ERR_OUT_OF_MEMORY;
+    }
+    if (cudaMemset(L->pf_block, 0, pfb) != cudaSuccess) return MOE_ERR_CUDA;
+    L->pf = prefill_carve(L->pf_block, H, I, E, k, Tm);
+  }
+  if (!prefill_encode_maps(L->encode_map, L->pf, H, I, E, k, Tm, &L->pf_maps)) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
 moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* arena_dev, size_t arena_bytes) {
   if (!L || !arena_dev) return MOE_ERR_INVALID_ARG;
   const int E = L->d.n_experts;
-  const int need = E < L->d.max_tokens * L->d.top_k ? E : L->d.max_tokens * L->d.top_k;
+  // a pool serves calls of up to 8 tokens in the fused kernel (prefill calls
+  // lend slots, below); every distinct expert of one call needs a slot
+  const int calls = L->d.max_tokens < 8 ? L->d.max_tokens : 8;
+  const int need = E < calls * L->d.top_k ? E : calls * L->d.top_k;
   if (n_slots < need || n_slots > E) return MOE_ERR_INVALID_ARG;
   if (((uintptr_t)arena_dev & 255) != 0) return MOE_ERR_INVALID_ARG;
   if ((size_t)n_slots * (size_t)L->blob > arena_bytes) return MOE_ERR_OUT_OF_MEMORY;
@@ -620,6 +693,8 @@ moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* aren
     for (int e = 0; e < E; ++e) slot_of[e] = -1;
   }
   if (!write_pool_state(L, slot_of, owner)) return unconfigured(MOE_ERR_CUDA);
+  const moe_status_t pf = configure_prefill_scratch(L);
+  if (pf != MOE_OK) return unconfigured(pf);
   if (a.pool) {
     try {
       register_layer(L);
@@ -678,6 +753,80 @@ bool overlap(const void* p, const void* q, size_t n) {
 // x is the layer input; with a pre-norm it is the xhat buffer, which the
 // fused kernel writes itself and the other paths get from
 // residual_rmsnorm_kernel first.
+// A prefill call on a pooled layer (Basalt README, section "Prompt chunks").
+// The scratch sits in the lent slots; after routing, the host reads which
+// experts the call touches and where the pool holds them (one stream
+// synchronize), then runs the expert GEMMs in waves: the first with every
+// touched expert resident below the lent slots, each wave with up to R
+// missing experts copied from the pinned master copy into the staging
+// slots.  Afterwards every lent slot gets its own expert back, so the pool
+// (table, LRU stamps, contents) is exactly what it was before the call.
+moe_status_t prefill_lend(moe_layer* L, const LayerArgs& a, cudaStream_t s) {
+  const int E = L->d.n_experts, S = L->n_slots;
+  const size_t blob = (size_t)L->blob;
+  const int first = L->lend_first, scr0 = S - L->lend_scratch, R = scr0 - first;
+  uint8_t* arena = L->arena;
+  if (cudaMemsetAsync(arena + (size_t)scr0 * blob, 0, (size_t)L->lend_scratch * blob, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (launch_prefill_route(a, L->pf, L->pf_maps, L->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
+  int32_t* counts = L->pf_host;
+  const size_t ds_off = ((sizeof(int32_t) * ((size_t)E + 1)) + 127) & ~size_t(127);
+  DevState* ds = reinterpret_cast<DevState*>(reinterpret_cast<uint8_t*>(L->pf_host) + ds_off);
+  int32_t* tabs = reinterpret_cast<int32_t*>(ds + 1);
+  if (cudaMemcpyAsync(counts, L->pf.counts, sizeof(int32_t) * (E + 1), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(ds, a.st, sizeof(DevState), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(tabs, L->pool_state, sizeof(int32_t) * 2 * ((size_t)E + 2 * S), cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ds->error) return MOE_ERR_STATE;
+  // the table the next decode call starts from (prefill leaves the step alone)
+  const int32_t* slot_of = tabs + (size_t)((ds->step + 1u) & 1u) * ((size_t)E + 2 * S);
+  const int32_t* owner = slot_of + E;
+  std::vector<int> stage;
+  const uint8_t** t0 = L->pf_tables;
+  for (int e = 0; e < E; ++e) {
+    t0[e] = nullptr;
+    if (counts[e] <= 0) continue;
+    const int q = slot_of[e];
+    if (q >= 0 && q < first)
+      t0[e] = arena + (size_t)q * blob;
+    else
+      stage.push_back(e);
+  }
+  const int waves = stage.empty() ? 1 : (int)((stage.size() + R - 1) / R);
+  uint64_t moved = 0;
+  for (int w = 0; w < waves; ++w) {
+    const uint8_t** t = L->pf_tables + (size_t)w * E;
+    if (w > 0)
+      for (int e = 0; e < E; ++e) t[e] = nullptr;
+    for (int i = 0; i < R; ++i) {
+      const size_t j = (size_t)w * R + i;
+      if (j >= stage.size()) break;
+      const int e = stage[j];
+      uint8_t* dst = arena + (size_t)(first + i) * blob;
+      if (cudaMemcpyAsync(dst, L->master + (size_t)e * blob, blob, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      t[e] = dst;
+      moved += blob;
+    }
+    if (cudaMemcpyAsync(L->pf.base_table, t, sizeof(uint8_t*) * E, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (launch_prefill_wave(a, L->pf, L->sm_count, w == 0, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (launch_prefill_combine(a, L->pf, s) != cudaSuccess) return MOE_ERR_CUDA;
+  for (int q = first; q < S; ++q) {
+    const int e = owner[q];
+    if (e < 0) continue;
+    if (cudaMemcpyAsync(arena + (size_t)q * blob, L->master + (size_t)e * blob, blob, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+    moved += blob;
+  }
+  L->h2d_bytes += moved;
+  return MOE_OK;
+}
+
 moe_status_t forward_impl(moe_layer_t* L, const void* x, int32_t T, void* y, int32_t* topk_idx, float* topk_w,
                           void* stream, const PreNorm* pn) {
   if (L->n_slots == 0) return MOE_ERR_STATE;
@@ -713,12 +862,15 @@ moe_status_t forward_impl(moe_layer_t* L, const void* x, int32_t T, void* y, int
     if (launch_decode(a, L->tagged_logits, L->pool_state, L->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (a.pool || a.fmt != MOE_FMT_LINEAR4) return MOE_ERR_UNSUPPORTED;  // pools and codebooks: fused path only
+  // codebook weights: fused path only; a pool: fused path (T <= 8) or a
+  // prefill call that lends slots (T > 64)
+  if (a.fmt != MOE_FMT_LINEAR4 || (a.pool && T <= kMaxTokens)) return MOE_ERR_UNSUPPORTED;
   if (pn && launch_residual_rmsnorm((const uint16_t*)pn->x, (const uint16_t*)pn->y_prev, T, L->d.hidden, pn->eps,
                                     (uint16_t*)pn->x_out, (uint16_t*)pn->xhat, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (T > kMaxTokens) {
     if (!prefill_encode_x(L->encode_map, x, L->d.hidden, T, &L->pf_maps)) return MOE_ERR_CUDA;
+    if (a.pool) return prefill_lend(L, a, s);
     if (launch_prefill(a, L->pf, L->pf_maps, L->sm_count, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }

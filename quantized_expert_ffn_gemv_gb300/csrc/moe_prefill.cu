@@ -866,7 +866,7 @@ __global__ void __launch_bounds__(sm_warps(MODE) * 32) prefill_small_kernel(Laye
     const int4 rec = ld_cg_int4(&p.small_rec[c]);
     const int e = rec.x, poff = rec.y, nt = rec.z;
     const int ng = (nt + 7) >> 3;
-    const uint8_t* base = (e < E) ? a.arena + (int64_t)e * a.blob : a.shared;
+    const uint8_t* base = (e < E) ? (p.base ? p.base[e] : a.arena + (int64_t)e * a.blob) : a.shared;
     // the chunk's B rows; rows past nt are zero (row addresses looked up once)
     __shared__ const __half* s_row[kSmallN];
     if (tid < kSmallN)
@@ -899,15 +899,13 @@ __global__ void __launch_bounds__(sm_warps(MODE) * 32) prefill_small_kernel(Laye
           for (int b = 0; b < kSmBatch; ++b) {
             const int st = st0 + NW * b;
             if (st < nst) {
-              const SupertileA tg = dequant_supertile(w0[b], s0[b]);  // once for both token groups
-              const SupertileA tu = dequant_supertile(w1[b], s1[b]);
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
                 if (q < ng) {
                   uint4 b01, b23;
                   sm_load_b(bs, K, q, st, g, t4, b01, b23);
-                  supertile_mma_pre(ag[q], tg, b01, b23);
-                  supertile_mma_pre(au[q], tu, b01, b23);
+                  supertile_mma(ag[q], w0[b], s0[b], b01, b23);
+                  supertile_mma(au[q], w1[b], s1[b], b01, b23);
                 }
               }
             }
@@ -958,13 +956,12 @@ __global__ void __launch_bounds__(sm_warps(MODE) * 32) prefill_small_kernel(Laye
           for (int b = 0; b < kSmBatch; ++b) {
             const int st = st0 + b;
             if (st < nst) {
-              const SupertileA td = dequant_supertile(w0[b], s0[b]);  // once for both token groups
 #pragma unroll
               for (int q = 0; q < 2; ++q) {
                 if (q < ng) {
                   uint4 b01, b23;
                   sm_load_b(bs, K, q, st, g, t4, b01, b23);
-                  supertile_mma_pre(acc[q], td, b01, b23);
+                  supertile_mma(acc[q], w0[b], s0[b], b01, b23);
                 }
               }
             }
@@ -1040,7 +1037,7 @@ __global__ void __launch_bounds__(kExpThreads, 1) prefill_expert_kernel(LayerArg
     int rb = 0;
     for (int t = blockIdx.x; t < n_tasks && ok; t += gridDim.x) {
       const Task tk = load_task(p, MB, t);
-      const uint8_t* base = (tk.e < E) ? a.arena + (int64_t)tk.e * a.blob : a.shared;
+      const uint8_t* base = (tk.e < E) ? (p.base ? p.base[tk.e] : a.arena + (int64_t)tk.e * a.blob) : a.shared;
       const int strip = lane & 7;
       const uint8_t* sp;
       if (MODE == 0)
@@ -1290,7 +1287,8 @@ size_t prefill_scratch_bytes(int H, int I, int E, int k, int Tm) {
          2 * pf_align(4ull * E * words) + pf_align(6ull * E * H) + pf_align(4ull * E) + pf_align(4ull * Tm) +
          pf_align(2ull * Tm * H) +
          pf_align(2 * P * I) +
-         pf_align(2 * P * H);
+         pf_align(2 * P * H) +
+         pf_align(8ull * E) + pf_align(16 * chunks) + pf_align(16ull * (E + 1)) + pf_align(8);
 }
 
 PrefillArgs prefill_carve(void* block, int H, int I, int E, int k, int Tm) {
@@ -1320,6 +1318,11 @@ PrefillArgs prefill_carve(void* block, int H, int I, int E, int k, int Tm) {
   p.h16p = (__half*)carve(2 * P * I);
   p.z16 = (__half*)carve(2 * P * H);
   p.words = (int)words;
+  p.base = nullptr;  // resident layer; a pooled call points it at its wave table
+  p.wave_chunk_rec = (int4*)carve(16 * ((size_t)E + 2 + P / kPfN));
+  p.wave_small_rec = (int4*)carve(16 * ((size_t)E + 1));
+  p.wave_n = (int32_t*)carve(8);
+  p.base_table = (const uint8_t**)carve(8ull * E);
   return p;
 }
 
@@ -1356,8 +1359,8 @@ cudaError_t prefill_configure() {
   return cudaFuncSetAttribute(prefill_router_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmem);
 }
 
-cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, const PrefillMaps& m, int sm_count,
-                           cudaStream_t s) {
+cudaError_t launch_prefill_route(const LayerArgs& a, const PrefillArgs& p, const PrefillMaps& m, int sm_count,
+                                 cudaStream_t s) {
   cudaError_t e;
   if ((e = cudaMemsetAsync(p.counts, 0, sizeof(int32_t) * (size_t)(a.E + 1), s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(p.bitmap, 0, sizeof(uint32_t) * (size_t)a.E * p.words, s)) != cudaSuccess) return e;
@@ -1383,13 +1386,67 @@ cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, const Prefi
   prefill_prefix_kernel<<<(a.E + 7) / 8, 256, 0, s>>>(a, p);
   prefill_scan_kernel<<<1, 1024, 0, s>>>(a, p);
   prefill_pairs_kernel<<<(a.T * (a.k + 1) + 255) / 256, 256, 0, s>>>(a, p);
+  return cudaGetLastError();
+}
+
+namespace {
+
+void launch_experts(const LayerArgs& a, const PrefillArgs& p, int sm_count, cudaStream_t s) {
   prefill_small_kernel<0><<<sm_count * 2, sm_warps(0) * 32, sm_smem(0, a.H), s>>>(a, p);
   prefill_expert_kernel<0><<<sm_count, kExpThreads, kGemmSmem, s>>>(a, p);
   prefill_small_kernel<1><<<sm_count * 8, sm_warps(1) * 32, sm_smem(1, a.I), s>>>(a, p);
   prefill_expert_kernel<1><<<sm_count, kExpThreads, kGemmSmem, s>>>(a, p);
+}
+
+// This wave's chunk records: those whose expert has a base in p.base (the
+// shared expert's in wave 0), in any order (each chunk writes its own rows).
+__global__ void __launch_bounds__(1024) prefill_wave_kernel(LayerArgs a, PrefillArgs p, int wave0) {
+  __shared__ int c0, c1;
+  const int tid = threadIdx.x, E = a.E;
+  if (tid == 0) c0 = c1 = 0;
+  __syncthreads();
+  const int n0 = ld_cg_i32(&p.n_chunks[0]), n1 = ld_cg_i32(&p.n_chunks[1]);
+  for (int i = tid; i < n0; i += blockDim.x) {
+    const int4 r = ld_cg_int4(&p.chunk_rec[i]);
+    if (r.x >= E ? wave0 != 0 : p.base[r.x] != nullptr) p.wave_chunk_rec[atomicAdd(&c0, 1)] = r;
+  }
+  for (int i = tid; i < n1; i += blockDim.x) {
+    const int4 r = ld_cg_int4(&p.small_rec[i]);
+    if (r.x >= E ? wave0 != 0 : p.base[r.x] != nullptr) p.wave_small_rec[atomicAdd(&c1, 1)] = r;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    p.wave_n[0] = c0;
+    p.wave_n[1] = c1;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill_wave(const LayerArgs& a, const PrefillArgs& p, int sm_count, bool wave0, cudaStream_t s) {
+  PrefillArgs q = p;
+  q.base = p.base_table;
+  prefill_wave_kernel<<<1, 1024, 0, s>>>(a, q, wave0 ? 1 : 0);
+  q.n_chunks = p.wave_n;
+  q.chunk_rec = p.wave_chunk_rec;
+  q.small_rec = p.wave_small_rec;
+  launch_experts(a, q, sm_count, s);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_prefill_combine(const LayerArgs& a, const PrefillArgs& p, cudaStream_t s) {
   const long long n = (long long)a.T * (a.H / 8);
   prefill_combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(a, p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, const PrefillMaps& m, int sm_count,
+                           cudaStream_t s) {
+  cudaError_t e = launch_prefill_route(a, p, m, sm_count, s);
+  if (e != cudaSuccess) return e;
+  launch_experts(a, p, sm_count, s);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_prefill_combine(a, p, s);
 }
 
 }  // namespace moe

@@ -32,6 +32,14 @@ struct PrefillArgs {
   __half* h16p;         // [T*k + T][I] fp16 h of each pair
   __half* z16;          // [T*(k+1)][H] fp16 expert outputs before the weighting
   int words;            // ceil(max_tokens / 32): row stride of bitmap and prefix
+  // Pooled layers (experts read in waves): per routed expert, where its blob
+  // is for the current wave, or null (not in this wave).  Null table: every
+  // expert at arena + e * blob (a resident layer).
+  const uint8_t** base;
+  const uint8_t** base_table;  // [E] storage for that table
+  int4* wave_chunk_rec;  // [max chunks] this wave's tensor-core chunks
+  int4* wave_small_rec;  // [E + 1] this wave's small chunks
+  int32_t* wave_n;       // [2] their counts
 };
 
 // TMA descriptors of the router GEMM (128-byte swizzle, bf16, 64-element boxes along K).
@@ -55,5 +63,12 @@ bool prefill_encode_x(TensorMapEncodeFn enc, const void* x, int H, int T, Prefil
 cudaError_t prefill_configure();
 cudaError_t launch_prefill(const LayerArgs& a, const PrefillArgs& p, const PrefillMaps& m, int sm_count,
                            cudaStream_t s);
+// The same call in three parts, for a pooled layer whose experts come in
+// waves: routing and grouping; the expert GEMMs of one wave (the chunks whose
+// expert has a base in p.base, the shared expert's in wave 0); the combine.
+cudaError_t launch_prefill_route(const LayerArgs& a, const PrefillArgs& p, const PrefillMaps& m, int sm_count,
+                                 cudaStream_t s);
+cudaError_t launch_prefill_wave(const LayerArgs& a, const PrefillArgs& p, int sm_count, bool wave0, cudaStream_t s);
+cudaError_t launch_prefill_combine(const LayerArgs& a, const PrefillArgs& p, cudaStream_t s);
 
 }  // namespace moe

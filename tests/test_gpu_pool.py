@@ -114,8 +114,9 @@ def test_seeding_errors(small):
 
 
 def test_pool_serves_up_to_eight_tokens_and_refuses_more(small):
-    """A pooled layer runs the fused path (T <= 8); a larger call is
-    MOE_ERR_UNSUPPORTED before any launch, and the layer stays usable."""
+    """A pooled layer runs the fused path (T <= 8); a call of 9 to 64 tokens
+    is MOE_ERR_UNSUPPORTED before any launch (larger calls lend slots:
+    tests/test_gpu_lend.py), and the layer stays usable."""
     import torch
     from quantized_expert_ffn_gemv_gb300 import moe
     x, _ = resampled_tokens(small, 950, 9)
