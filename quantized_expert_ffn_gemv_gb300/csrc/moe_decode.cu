@@ -161,7 +161,7 @@ struct Plan {
 
 __host__ __device__ inline size_t al128(size_t v) { return (v + 127) & ~size_t(127); }
 
-__host__ __device__ inline Plan plan_with(int H, int I, int E, int k, int T, int G, int gs, int ds) {
+__host__ __device__ inline Plan plan_with(int H, int I, int E, int k, int T, int G, int gs, int ds, bool pool) {
   Plan p;
   p.rows_max = (E + G - 1) / G;
   p.umax = E < T * k ? E : T * k;
@@ -196,18 +196,18 @@ __host__ __device__ inline Plan plan_with(int H, int I, int E, int k, int T, int
   // a pooled call's slot table, slot owners and stamps (S <= E), loaded
   // while the router and the top-k run
   p.pooltab = o;
-  o += al128((size_t)E * 12);
+  if (pool) o += al128((size_t)E * 12);
   p.total = o;
   return p;
 }
 
-__host__ __device__ inline Plan make_plan(int H, int I, int E, int k, int T, int G, size_t limit) {
+__host__ __device__ inline Plan make_plan(int H, int I, int E, int k, int T, int G, size_t limit, bool pool) {
   const int nex = (E < T * k ? E : T * k) + 1;
   const int want_dn = nex < kMaxDnStages ? nex : kMaxDnStages;
   const int gs_opts[4] = {3, 2, 2, 1};
   const int ds_opts[4] = {want_dn, want_dn < 8 ? want_dn : 8, want_dn < 4 ? want_dn : 4, want_dn < 2 ? want_dn : 2};
-  Plan p = plan_with(H, I, E, k, T, G, gs_opts[0], ds_opts[0]);
-  for (int i = 1; i < 4 && p.total > limit; ++i) p = plan_with(H, I, E, k, T, G, gs_opts[i], ds_opts[i]);
+  Plan p = plan_with(H, I, E, k, T, G, gs_opts[0], ds_opts[0], pool);
+  for (int i = 1; i < 4 && p.total > limit; ++i) p = plan_with(H, I, E, k, T, G, gs_opts[i], ds_opts[i], pool);
   return p;
 }
 
@@ -583,7 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   const int H = a.H, I = a.I, E = a.E, k = a.k, T = ONE ? 1 : a.T, NS = I / 16, NSh = a.n_shared;
   constexpr int fmt = FMT;
   const uint32_t lut = FMT == 1 ? codebook_lut(threadIdx.x & 31) : 0u;
-  const Plan PL = make_plan(H, I, E, k, T, G, smem_limit);
+  const Plan PL = make_plan(H, I, E, k, T, G, smem_limit, !ONE && a.pool);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + PL.bars);
   Ring R;
   R.full_gu = bars;
@@ -850,7 +850,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       // the warp's h stores happen before lane 0's release through the warp
       // barrier (no per-thread fence: the release covers them)
       __syncwarp();
-      if (lane == 0) red_release_add(&cnt_cur[(xi * (NS / 4) + strip / 4) * kCntPad], 1u);
+      // one token: a count per 64-wide chunk of I (the down product starts on
+      // each chunk as it completes); more tokens: one count per expert
+      if (lane == 0) red_release_add(&cnt_cur[(xi * (NS / 4) + (ONE ? strip / 4 : 0)) * kCntPad], 1u);
     }
     named_sync(1 + grp, kGroupWarps * 32);
   };
@@ -1232,10 +1234,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       int done = 0, spins = 0;
       bool alive = ok;
       while (alive && done < nst) {
-        const int ch = done + lane;
-        const bool rdy = ch < nst && ld_acquire_gpu_u32(&cnt_x[(size_t)ch * kCntPad]) >= 4u;
-        const unsigned m = __ballot_sync(0xffffffffu, rdy);
-        const int nr = (m == 0xffffffffu) ? 32 : __ffs(~m) - 1;  // chunks ready, in order from done
+        int nr;  // chunks ready, in order from done
+        if (ONE) {
+          const int ch = done + lane;
+          const bool rdy = ch < nst && ld_acquire_gpu_u32(&cnt_x[(size_t)ch * kCntPad]) >= 4u;
+          const unsigned m = __ballot_sync(0xffffffffu, rdy);
+          nr = (m == 0xffffffffu) ? 32 : __ffs(~m) - 1;
+        } else {
+          const bool rdy = lane == 0 && ld_acquire_gpu_u32(&cnt_x[0]) >= (uint32_t)NS;
+          nr = __shfl_sync(0xffffffffu, rdy ? nst : 0, 0);
+        }
         if (nr == 0) {
           if (is_prod) pump(P, X);
           bool stop = false;
@@ -1355,8 +1363,8 @@ cudaLaunchConfig_t decode_config(dim3 grid, dim3 block, size_t smem, cudaStream_
 
 }  // namespace
 
-size_t decode_smem_bytes(int H, int I, int E, int k, int T, int G) {
-  return make_plan(H, I, E, k, T, G, g_decode_smem_limit).total;
+size_t decode_smem_bytes(int H, int I, int E, int k, int T, int G, bool pool) {
+  return make_plan(H, I, E, k, T, G, g_decode_smem_limit, pool).total;
 }
 
 cudaError_t decode_configure() {
@@ -1402,11 +1410,11 @@ cudaError_t decode_configure() {
   return cudaSuccess;
 }
 
-bool decode_supported(int H, int I, int E, int k, int T, int G) {
+bool decode_supported(int H, int I, int E, int k, int T, int G, bool pool) {
   if (T > kMaxT || E > kMaxE || k > kMaxTopK) return false;
   if ((E + G - 1) / G > 8) return false;  // router: two warps per row, 16 warps
   if (H / 16 > G) return false;            // down: one 16-row output strip per CTA
-  return g_decode_smem_limit > 0 && decode_smem_bytes(H, I, E, k, T, G) <= g_decode_smem_limit;
+  return g_decode_smem_limit > 0 && decode_smem_bytes(H, I, E, k, T, G, pool) <= g_decode_smem_limit;
 }
 
 cudaError_t launch_decode(const LayerArgs& a, unsigned long long* tagged_logits, int32_t* pool_state, int G,
@@ -1417,8 +1425,8 @@ cudaError_t launch_decode(const LayerArgs& a, unsigned long long* tagged_logits,
   // keeps the plain stream order.
   const bool pdl = g_decode_pdl && (!a.pool || a.pull);
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = decode_config(dim3(G), dim3(kThreads), decode_smem_bytes(a.H, a.I, a.E, a.k, a.T, G), s,
-                                         attr, pdl);
+  const size_t smem = decode_smem_bytes(a.H, a.I, a.E, a.k, a.T, G, a.pool != 0);
+  cudaLaunchConfig_t cfg = decode_config(dim3(G), dim3(kThreads), smem, s, attr, pdl);
   // one token per call, linear weights: one key per lane in top-k
   const bool one = a.T == 1 && !a.pool && a.E <= 16 * 32 && a.fmt == 0;
   if (one) return cudaLaunchKernelEx(&cfg, decode_kernel<true, 0>, a, tagged_logits, pool_state, g_decode_smem_limit);

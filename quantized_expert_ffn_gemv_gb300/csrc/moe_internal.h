@@ -163,8 +163,8 @@ int gateup_max_blocks_per_sm(int H);
 int down_warps(int T, int k, int n_shared, int I);
 
 // Fused single-launch decode path (moe_decode.cu), T <= 8.
-size_t decode_smem_bytes(int H, int I, int E, int k, int T, int G);
-bool decode_supported(int H, int I, int E, int k, int T, int G);
+size_t decode_smem_bytes(int H, int I, int E, int k, int T, int G, bool pool);
+bool decode_supported(int H, int I, int E, int k, int T, int G, bool pool);
 cudaError_t decode_configure();
 cudaError_t launch_decode(const LayerArgs& a, unsigned long long* tagged_logits, int32_t* pool_state, int G,
                           cudaStream_t s);

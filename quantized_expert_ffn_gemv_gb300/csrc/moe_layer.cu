@@ -665,7 +665,7 @@ moe_status_t moe_slot_pool_configure(moe_layer_t* L, int32_t n_slots, void* aren
   if (((uintptr_t)arena_dev & 255) != 0) return MOE_ERR_INVALID_ARG;
   if ((size_t)n_slots * (size_t)L->blob > arena_bytes) return MOE_ERR_OUT_OF_MEMORY;
   // only the fused decode kernel serves a pool
-  if (n_slots < E && !decode_supported(L->d.hidden, L->d.inter, E, L->d.top_k, 1, L->sm_count))
+  if (n_slots < E && !decode_supported(L->d.hidden, L->d.inter, E, L->d.top_k, 1, L->sm_count, true))
     return MOE_ERR_UNSUPPORTED;
   DeviceGuard guard(L->d.device);
   if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
@@ -840,7 +840,7 @@ moe_status_t forward_impl(moe_layer_t* L, const void* x, int32_t T, void* y, int
   if (topk_w) a.topk_w = topk_w;
   a.wait_timeout_ns = L->wait_timeout_ns;
   cudaStream_t s = (cudaStream_t)stream;
-  if (decode_supported(L->d.hidden, L->d.inter, L->d.n_experts, L->d.top_k, T, L->sm_count)) {
+  if (decode_supported(L->d.hidden, L->d.inter, L->d.n_experts, L->d.top_k, T, L->sm_count, L->args.pool != 0)) {
     if (pn) {
       a.resid = (const uint16_t*)pn->x;
       a.y_prev = (const uint16_t*)pn->y_prev;
