@@ -1214,36 +1214,81 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     for (int xi = warp; xi < n_ex; xi += R.ds) {
       const Task tk = task_of(a, L, xi, NSh);
       const int s = xi % R.ds;
+      const uint32_t* cnt_x = cnt_cur + (size_t)xi * nst * kCntPad;
+      if (!ONE) {
+        // more tokens: the expert's one counter first (its strips stream in
+        // meanwhile), then every chunk at once below
+        if (lane == 0) {
+          int spins = 0;
+          while (ld_acquire_gpu_u32(&cnt_x[0]) < (uint32_t)NS) {
+            if (is_prod) pump(P, X);
+            if (((++spins) & 15) == 0) {
+              if (global_ns() > deadline) { set_error(a, MOE_ERR_TIMEOUT); break; }
+              if (dev_error(a)) break;
+            }
+            // no __nanosleep here: a sleeping warp was measured to wake up
+            // microseconds late now and then, which delayed the whole layer
+          }
+        }
+        __syncwarp();
+      }
       if (!ONE && tk.src && !(xi < R.ds && npw > 0)) {  // a miss not pulled early: read it now
         const size_t off = (size_t)down_base(H, I) + (size_t)c * R.dn_bytes;
         pull_strip(tk.src + off, const_cast<uint8_t*>(tk.base) + off, R.dn + s * R.dn_pitch, R.dn_bytes, lane, 32);
         __syncwarp();
         if (lane == 0) mbar_arrive(&R.full_dn[s]);
       }
+      const bool staged = ONE || tk.cnt <= hb_rows;  // one token always fits
+      if (!ONE && staged) {  // all of h, one round of copies, before the strip wait
+        const int per_row = I / 8;
+        for (int o = lane; o < tk.cnt * per_row; o += 32) {
+          const int r = o / per_row, cc = o - r * per_row;
+          cp_async16(hbuf + r * hstride + cc * 8, a.h16 + (size_t)(tk.poff + r) * I + cc * 8);
+        }
+        cp_async_wait_all();
+        __syncwarp();
+      }
       const bool ok = __all_sync(0xffffffffu, wait_full(&R.full_dn[s], (xi / R.ds) & 1, deadline, is_prod, P, X));
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       const unsigned char* sb = R.dn + s * R.dn_pitch;
       const int gsel = (g < tk.cnt) ? g : 0;
-      const bool staged = ONE || tk.cnt <= hb_rows;  // one token always fits
-      // The K range of the down product comes in 64-wide chunks (four gate/up
-      // strips each, one counter each): the warp multiplies every chunk whose
-      // h is complete, in chunk order, while later strips are still being
-      // computed elsewhere; the accumulation order is the same as for one
-      // pass over all of K.
-      const uint32_t* cnt_x = cnt_cur + (size_t)xi * nst * kCntPad;
-      int done = 0, spins = 0;
+      // One token: the K range of the down product comes in 64-wide chunks
+      // (four gate/up strips each, one counter each); the warp multiplies
+      // every chunk whose h is complete, in chunk order, while later strips
+      // are still being computed elsewhere.  More tokens: every chunk is
+      // complete here and staged above.  The accumulation order is one pass
+      // over K either way.
+      int done = ONE ? 0 : nst, spins = 0;
       bool alive = ok;
-      while (alive && done < nst) {
-        int nr;  // chunks ready, in order from done
-        if (ONE) {
-          const int ch = done + lane;
-          const bool rdy = ch < nst && ld_acquire_gpu_u32(&cnt_x[(size_t)ch * kCntPad]) >= 4u;
-          const unsigned m = __ballot_sync(0xffffffffu, rdy);
-          nr = (m == 0xffffffffu) ? 32 : __ffs(~m) - 1;
+      if (!ONE && ok) {
+        if (staged) {
+          const __half* hb = hbuf + gsel * hstride + t4 * 16;
+#pragma unroll 4
+          for (int st = 0; st < nst; ++st) {
+            const uint4 b01 = *reinterpret_cast<const uint4*>(hb + st * 64);
+            const uint4 b23 = *reinterpret_cast<const uint4*>(hb + st * 64 + 8);
+            const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
+            const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
+            supertile_mma(acc, nb, scv, b01, b23, fmt, lut);
+          }
         } else {
-          const bool rdy = lane == 0 && ld_acquire_gpu_u32(&cnt_x[0]) >= (uint32_t)NS;
-          nr = __shfl_sync(0xffffffffu, rdy ? nst : 0, 0);
+          const int hrow = tk.poff + gsel;
+#pragma unroll 2
+          for (int st = 0; st < nst; ++st) {
+            const __half* hr = a.h16 + (size_t)hrow * I + st * 64 + t4 * 16;
+            const uint4 b01 = __ldcg(reinterpret_cast<const uint4*>(hr));
+            const uint4 b23 = __ldcg(reinterpret_cast<const uint4*>(hr + 8));
+            const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
+            const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
+            supertile_mma(acc, nb, scv, b01, b23, fmt, lut);
+          }
         }
+      }
+      while (ONE && alive && done < nst) {
+        const int ch = done + lane;
+        const bool rdy = ch < nst && ld_acquire_gpu_u32(&cnt_x[(size_t)ch * kCntPad]) >= 4u;
+        const unsigned m = __ballot_sync(0xffffffffu, rdy);
+        const int nr = (m == 0xffffffffu) ? 32 : __ffs(~m) - 1;  // chunks ready, in order from done
         if (nr == 0) {
           if (is_prod) pump(P, X);
           bool stop = false;
@@ -1261,7 +1306,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
           continue;
         }
         __syncwarp();  // the lanes' acquires order every lane's h reads below
-        if (staged) {
+        {  // one token: its h always fits the staging buffer
           const int per_row = nr * 8;  // 16-byte pieces of the ready chunks, per token row
           for (int o = lane; o < tk.cnt * per_row; o += 32) {
             const int r = o / per_row, rem = o - r * per_row;
@@ -1271,21 +1316,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
           cp_async_wait_all();
           __syncwarp();
           const __half* hb = hbuf + gsel * hstride + t4 * 16;
-#pragma unroll 2
+#pragma unroll 4
           for (int st = done; st < done + nr; ++st) {
             const uint4 b01 = *reinterpret_cast<const uint4*>(hb + st * 64);
             const uint4 b23 = *reinterpret_cast<const uint4*>(hb + st * 64 + 8);
-            const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
-            const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
-            supertile_mma(acc, nb, scv, b01, b23, fmt, lut);
-          }
-        } else {
-          const int hrow = tk.poff + gsel;
-#pragma unroll 2
-          for (int st = done; st < done + nr; ++st) {
-            const __half* hr = a.h16 + (size_t)hrow * I + st * 64 + t4 * 16;
-            const uint4 b01 = __ldcg(reinterpret_cast<const uint4*>(hr));
-            const uint4 b23 = __ldcg(reinterpret_cast<const uint4*>(hr + 8));
             const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
             const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
             supertile_mma(acc, nb, scv, b01, b23, fmt, lut);
