@@ -11,32 +11,36 @@
 //              down strip start loading; x -> fp16 in B-fragment order.
 //   router     compensated (double-float) dot products, four warps per row;
 //              each logit's 52-bit order key is stored with a 12-bit call tag
-//              in one 64-bit word; readers poll for the tag (no grid barrier).
+//              in one 64-bit word; each CTA then releases one count on the
+//              layer's publication counter, and one lane per CTA waits for
+//              all of them before the block reads the keys once.
 //   routing    every CTA redundantly: each warp ranks its range of experts
 //              (one 64-bit compare orders by logit, then index) and keeps its
-//              k best; entries below the best warp's k-th cannot be selected;
-//              the survivors are ranked against each other, giving the k in
-//              rank order; then ascending expert order, softmax weights
-//              renormalised over the k, the union of selected experts
-//              and the (expert, token) pair lists, the slot hit check and LRU
-//              victims (double-buffered pool state; CTA 0 writes the next
-//              state and rings the host doorbell).  Betelgeuse news page,
-//              section 机制, 调度 row: the hit check runs in-stream on the GPU.
-//              One resident token takes an early path: the experts start as
-//              soon as the merge ends and an idle warp finishes the softmax.
+//              k best; entries below a threshold taken from the lists' heads
+//              cannot be selected; the survivors are ranked against each
+//              other, giving the k in rank order.  One token: the union is
+//              that order and the experts start at once while a spare warp
+//              computes the softmax weights and the combine mapping.  More
+//              tokens: ascending expert order, softmax renormalised over the
+//              k, the union and the (expert, token) pair lists.  Then the slot
+//              hit check and LRU victims (double-buffered pool state, its
+//              tables copied to shared memory during the routing; CTA 0 rings
+//              the host doorbell).  Betelgeuse news page, section 机制, 调度
+//              row: the hit check runs in-stream on the GPU.
 //   misses     by default the consuming warps read a missed expert's strips
 //              from the mapped pinned master copy themselves (and write them
 //              back to its slot); otherwise they wait for the slot's ready
 //              flag, set by the host copy server after its copy.
 //   gate/up    four warps per 16-row strip (K split four ways), one strip per
-//              ring stage at once; h = silu(g) * u goes to global as fp16 and the
-//              expert's completion counter (double-buffered by step parity)
-//              is bumped with a release reduction.
+//              ring stage at once; h = silu(g) * u goes to global as fp16 and a
+//              completion counter (per 64-wide chunk of I for one token, per
+//              expert otherwise; double-buffered by step parity, one cache line
+//              each) is bumped with a release reduction.
 //   down       warp w handles selected experts w, w + ds, ...: waits for the
-//              expert's counter, stages its h rows in shared memory with one
-//              round of cp.async, z = W_d h for this CTA's 16 output rows;
-//              then y = sum_j w_j z_j (ascending expert) + z_shared in fp32,
-//              rounded once to bf16.
+//              counters, stages h in shared memory with cp.async (one token:
+//              chunk by chunk as they complete), z = W_d h for this CTA's 16
+//              output rows; then y = sum_j w_j z_j (ascending expert) +
+//              z_shared in fp32, rounded once to bf16.
 #include <cfloat>
 #include <climits>
 

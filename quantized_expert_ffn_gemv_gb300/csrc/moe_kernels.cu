@@ -1,10 +1,12 @@
-// Decode-path kernels of the quantized MoE FFN layer (sm_103a).
+// Batched decode kernels of the quantized MoE FFN layer (sm_103a), for
+// calls the fused decode kernel does not take (9..64 tokens, or shapes it
+// declines), plus the separate residual + RMSNorm kernel.
 //
 // One moe_forward = four stream-ordered kernels chained with programmatic
 // dependent launch (griddepcontrol), so each grid is already resident when
 // its predecessor finishes:
-//   route_kernel   router GEMV in plain fp32 (four warps per expert row)
-//                  and the router rows' norms;
+//   route_kernel   router GEMV in plain fp32 (four warps per expert row,
+//                  blocks of 16 tokens) and the router rows' norms;
 //   route_select_kernel  CTA per token: the k best experts, exact (the
 //                  experts the fp32 error bound leaves in doubt are
 //                  recomputed with the canonical compensated router of
@@ -14,9 +16,10 @@
 //                  dequantized in registers into mma.m16n8k16 fragments,
 //                  fp32 accumulation with exact per-block scaling, then
 //                  h = silu(g) * u stored as fp16.
-//   down_kernel    per 16-row output strip: every selected expert's down rows,
-//                  then the routing-weighted combine in ascending expert
-//                  order (shared expert last) and one bf16 rounding.
+//   down_kernel    CTA per 16-row output strip: every selected expert's down
+//                  rows (warps over (expert, 8-token group) items), then the
+//                  routing-weighted combine in ascending expert order (shared
+//                  expert last) and one bf16 rounding.
 // These kernels serve layers whose experts are all resident (slot = expert);
 // a layer with a slot pool runs the fused decode kernel, which holds the
 // hit check (Betelgeuse news page, section 机制: 调度 and 显存 rows).
