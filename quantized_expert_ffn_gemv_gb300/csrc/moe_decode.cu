@@ -32,15 +32,20 @@
 //              back to its slot); otherwise they wait for the slot's ready
 //              flag, set by the host copy server after its copy.
 //   gate/up    four warps per 16-row strip (K split four ways), one strip per
-//              ring stage at once; h = silu(g) * u goes to global as fp16 and a
-//              completion counter (per 64-wide chunk of I for one token, per
-//              expert otherwise; double-buffered by step parity, one cache line
-//              each) is bumped with a release reduction.
-//   down       warp w handles selected experts w, w + ds, ...: waits for the
-//              counters, stages h in shared memory with cp.async (one token:
-//              chunk by chunk as they complete), z = W_d h for this CTA's 16
-//              output rows; then y = sum_j w_j z_j (ascending expert) +
-//              z_shared in fp32, rounded once to bf16.
+//              ring stage at once; h = silu(g) * u rounded to fp16.  One
+//              resident token: h goes out as 64-bit words tagged with the
+//              call (two values each) and a relaxed count per 64-wide chunk
+//              of I says when to look; otherwise h rows go out as fp16 and a
+//              per-expert counter is bumped with a release reduction
+//              (counters double-buffered by step parity, one cache line each).
+//   down       warp w handles selected experts w, w + ds, ...: one resident
+//              token: the chunks whose count is complete are read straight
+//              into the MMA fragments once every word carries the call's tag,
+//              while later strips are still being computed; otherwise the
+//              expert's counter, then its h staged in shared memory with
+//              cp.async.  z = W_d h for this CTA's 16 output rows; then
+//              y = sum_j w_j z_j (ascending expert) + z_shared in fp32,
+//              rounded once to bf16.
 #include <cfloat>
 #include <climits>
 
@@ -142,6 +147,14 @@ __device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long
 }
 __device__ __forceinline__ void red_release_add(uint32_t* p, uint32_t v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ void red_relaxed_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_relaxed_u32(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
 }
 __device__ __forceinline__ void named_sync(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
@@ -741,6 +754,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
   __syncthreads();
   const uint32_t seq = s_seq;
   const uint32_t tag = s_dseq & kTagMask;  // this call's tag on the published logits
+  const uint32_t htag_v = s_dseq;          // this call's tag on one-token h words
+  // One token, every expert resident: h goes through tagged words and the
+  // down product runs chunk by chunk as they complete.  Otherwise (pooled,
+  // or several tokens): h rows and one release-ordered counter per expert;
+  // the chunked form was measured slower in the pooled kernel.
+  constexpr bool tagged = ONE;
   // Pooled call: this step's slot table, owners and stamps start for shared
   // memory now (written by the previous call, complete at the wait above);
   // the hit check after the top-k then needs no round trip to L2.
@@ -843,20 +862,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         gsum[0] += p.x; gsum[1] += p.y; gsum[2] += p.z; gsum[3] += p.w;
         usum[0] += q.x; usum[1] += q.y; usum[2] += q.z; usum[3] += q.w;
       }
+      if (tagged) {
+        // one token (column 0: lanes with t4 = 0 hold rows g and g + 8): rows
+        // g, g + 1, g + 8, g + 9 sit at B-fragment positions p .. p + 3 (g
+        // even), written as two tagged words; the down product reads them
+        // with no counter and no release fence
+        const uint32_t q0 = __half_as_ushort(__float2half_rn(silu(gsum[0]) * usum[0]));
+        const uint32_t q2 = __half_as_ushort(__float2half_rn(silu(gsum[2]) * usum[2]));
+        const uint32_t q1 = __shfl_down_sync(0xffffffffu, q0, 4), q3 = __shfl_down_sync(0xffffffffu, q2, 4);
+        if (t4 == 0 && (g & 1) == 0) {
+          unsigned long long* dst = a.htag + (size_t)xi * (I / 2) + frag_pos(strip * 16 + g) / 2;
+          const unsigned long long tg = (unsigned long long)htag_v << 32;
+          st_relaxed_u64(dst, tg | (q1 << 16) | q0);
+          st_relaxed_u64(dst + 1, tg | (q3 << 16) | q2);
+        }
+        // a count per 64-wide chunk of I tells the readers when to look; it
+        // carries no release ordering (no fence here): a reader that gets
+        // ahead of the words sees an older tag and reads them again
+        __syncwarp();
+        if (lane == 0) red_relaxed_add(&cnt_cur[((size_t)xi * (NS / 4) + strip / 4) * kCntPad], 1u);
+      } else {
 #pragma unroll
-      for (int cc = 0; cc < 4; ++cc) {
-        const int rowin = (cc < 2) ? g : g + 8;
-        const int col = 2 * t4 + (cc & 1);
-        if (col < tk.cnt)
-          a.h16[(size_t)(tk.poff + col) * I + frag_pos(strip * 16 + rowin)] =
-              __float2half_rn(silu(gsum[cc]) * usum[cc]);
+        for (int cc = 0; cc < 4; ++cc) {
+          const int rowin = (cc < 2) ? g : g + 8;
+          const int col = 2 * t4 + (cc & 1);
+          if (col < tk.cnt)
+            a.h16[(size_t)(tk.poff + col) * I + frag_pos(strip * 16 + rowin)] =
+                __float2half_rn(silu(gsum[cc]) * usum[cc]);
+        }
+        // the warp's h stores happen before lane 0's release through the warp
+        // barrier (no per-thread fence: the release covers them); one count
+        // per strip on the expert's counter
+        __syncwarp();
+        if (lane == 0) red_release_add(&cnt_cur[(size_t)xi * (NS / 4) * kCntPad], 1u);
       }
-      // the warp's h stores happen before lane 0's release through the warp
-      // barrier (no per-thread fence: the release covers them)
-      __syncwarp();
-      // one token: a count per 64-wide chunk of I (the down product starts on
-      // each chunk as it completes); more tokens: one count per expert
-      if (lane == 0) red_release_add(&cnt_cur[(xi * (NS / 4) + (ONE ? strip / 4 : 0)) * kCntPad], 1u);
     }
     named_sync(1 + grp, kGroupWarps * 32);
   };
@@ -1218,10 +1257,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     for (int xi = warp; xi < n_ex; xi += R.ds) {
       const Task tk = task_of(a, L, xi, NSh);
       const int s = xi % R.ds;
-      const uint32_t* cnt_x = cnt_cur + (size_t)xi * nst * kCntPad;
-      if (!ONE) {
-        // more tokens: the expert's one counter first (its strips stream in
+      if (!tagged) {
+        // more tokens: the expert's counter first (its strips stream in
         // meanwhile), then every chunk at once below
+        const uint32_t* cnt_x = cnt_cur + (size_t)xi * nst * kCntPad;
         if (lane == 0) {
           int spins = 0;
           while (ld_acquire_gpu_u32(&cnt_x[0]) < (uint32_t)NS) {
@@ -1242,8 +1281,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
         __syncwarp();
         if (lane == 0) mbar_arrive(&R.full_dn[s]);
       }
-      const bool staged = ONE || tk.cnt <= hb_rows;  // one token always fits
-      if (!ONE && staged) {  // all of h, one round of copies, before the strip wait
+      const bool staged = !tagged && tk.cnt <= hb_rows;
+      if (staged) {  // all of h, one round of copies, before the strip wait
         const int per_row = I / 8;
         for (int o = lane; o < tk.cnt * per_row; o += 32) {
           const int r = o / per_row, cc = o - r * per_row;
@@ -1256,15 +1295,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       const unsigned char* sb = R.dn + s * R.dn_pitch;
       const int gsel = (g < tk.cnt) ? g : 0;
-      // One token: the K range of the down product comes in 64-wide chunks
-      // (four gate/up strips each, one counter each); the warp multiplies
-      // every chunk whose h is complete, in chunk order, while later strips
-      // are still being computed elsewhere.  More tokens: every chunk is
-      // complete here and staged above.  The accumulation order is one pass
-      // over K either way.
-      int done = ONE ? 0 : nst, spins = 0;
-      bool alive = ok;
-      if (!ONE && ok) {
+      if (!tagged && ok) {
         if (staged) {
           const __half* hb = hbuf + gsel * hstride + t4 * 16;
 #pragma unroll 4
@@ -1288,48 +1319,70 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
           }
         }
       }
-      while (ONE && alive && done < nst) {
-        const int ch = done + lane;
-        const bool rdy = ch < nst && ld_acquire_gpu_u32(&cnt_x[(size_t)ch * kCntPad]) >= 4u;
-        const unsigned m = __ballot_sync(0xffffffffu, rdy);
-        const int nr = (m == 0xffffffffu) ? 32 : __ffs(~m) - 1;  // chunks ready, in order from done
-        if (nr == 0) {
-          if (is_prod) pump(P, X);
-          bool stop = false;
-          if (((++spins) & 15) == 0) {
-            if (global_ns() > deadline) {
-              if (lane == 0) set_error(a, MOE_ERR_TIMEOUT);
-              stop = true;
-            } else if (dev_error(a)) {
-              stop = true;
+      if (tagged && ok) {
+        // One token: the chunk counters say which 64-wide chunks of h look
+        // complete; their words are read with one round trip (lane j holds
+        // word j of each chunk) and a chunk counts once all 32 words carry
+        // this call's tag.  The down product then runs on the leading valid
+        // chunks while later gate/up strips are still being computed
+        // elsewhere; each lane's B fragment comes from its 8 words by
+        // shuffles.  The accumulation order is one pass over K, as on the
+        // other paths.
+        constexpr int kBatch = 8;  // chunks read per round trip
+        const uint32_t* cnt_x = cnt_cur + (size_t)xi * nst * kCntPad;
+        const unsigned long long* hw = a.htag + (size_t)xi * (I / 2) + lane;
+        int done = 0, spins = 0;
+        while (done < nst) {
+          const int ch = done + lane;
+          const bool rdy = ch < nst && ld_relaxed_u32(&cnt_x[(size_t)ch * kCntPad]) >= 4u;
+          const unsigned m = __ballot_sync(0xffffffffu, rdy);
+          int nr = (m == 0xffffffffu) ? 32 : __ffs(~m) - 1;  // chunks counted complete, in order from done
+          nr = nr < kBatch ? nr : kBatch;
+          int nv = 0;
+          if (nr > 0) {
+            unsigned long long wv[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) wv[j] = (j < nr) ? ld_relaxed_u64(hw + (size_t)(done + j) * 32) : 0ull;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+              if (j < nr && nv == j && __all_sync(0xffffffffu, (uint32_t)(wv[j] >> 32) == htag_v)) nv = j + 1;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+              if (j < nv) {
+                const uint32_t lo = (uint32_t)wv[j];  // two fp16 values at positions 2 * lane, 2 * lane + 1
+                uint4 b01, b23;
+                b01.x = __shfl_sync(0xffffffffu, lo, t4 * 8 + 0);
+                b01.y = __shfl_sync(0xffffffffu, lo, t4 * 8 + 1);
+                b01.z = __shfl_sync(0xffffffffu, lo, t4 * 8 + 2);
+                b01.w = __shfl_sync(0xffffffffu, lo, t4 * 8 + 3);
+                b23.x = __shfl_sync(0xffffffffu, lo, t4 * 8 + 4);
+                b23.y = __shfl_sync(0xffffffffu, lo, t4 * 8 + 5);
+                b23.z = __shfl_sync(0xffffffffu, lo, t4 * 8 + 6);
+                b23.w = __shfl_sync(0xffffffffu, lo, t4 * 8 + 7);
+                const int st = done + j;
+                const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
+                const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
+                supertile_mma(acc, nb, scv, b01, b23, fmt, lut);
+              }
             }
+            done += nv;
           }
-          // no __nanosleep here: a sleeping warp was measured to wake up
-          // microseconds late now and then, which delayed the whole layer
-          alive = !__any_sync(0xffffffffu, stop);
-          continue;
-        }
-        __syncwarp();  // the lanes' acquires order every lane's h reads below
-        {  // one token: its h always fits the staging buffer
-          const int per_row = nr * 8;  // 16-byte pieces of the ready chunks, per token row
-          for (int o = lane; o < tk.cnt * per_row; o += 32) {
-            const int r = o / per_row, rem = o - r * per_row;
-            const int col = done * 64 + rem * 8;
-            cp_async16(hbuf + r * hstride + col, a.h16 + (size_t)(tk.poff + r) * I + col);
-          }
-          cp_async_wait_all();
-          __syncwarp();
-          const __half* hb = hbuf + gsel * hstride + t4 * 16;
-#pragma unroll 4
-          for (int st = done; st < done + nr; ++st) {
-            const uint4 b01 = *reinterpret_cast<const uint4*>(hb + st * 64);
-            const uint4 b23 = *reinterpret_cast<const uint4*>(hb + st * 64 + 8);
-            const uint4 nb = *reinterpret_cast<const uint4*>(sb + st * 512 + lane * 16);
-            const uint2 scv = *reinterpret_cast<const uint2*>(sb + 8 * I + st * 64 + g * 8);
-            supertile_mma(acc, nb, scv, b01, b23, fmt, lut);
+          if (nv == 0) {
+            if (is_prod) pump(P, X);
+            bool stop = false;
+            if (((++spins) & 15) == 0) {
+              if (global_ns() > deadline) {
+                if (lane == 0) set_error(a, MOE_ERR_TIMEOUT);
+                stop = true;
+              } else if (dev_error(a)) {
+                stop = true;
+              }
+            }
+            // no __nanosleep here: a sleeping warp was measured to wake up
+            // microseconds late now and then, which delayed the whole layer
+            if (__any_sync(0xffffffffu, stop)) break;
           }
         }
-        done += nr;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&R.empty_dn[s]);

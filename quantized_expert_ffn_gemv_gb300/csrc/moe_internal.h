@@ -120,6 +120,13 @@ struct LayerArgs {
   int32_t* tk_u;        // [T*k] union index of (t, j)
   int32_t* tk_pos;      // [T*k] position of (t, j) inside its expert's pairs
   __half* h16;          // [T*k + T][I] B-fragment order; shared expert rows after the routed ones
+  // Fused decode of one token with every expert resident: h of expert list
+  // entry xi (0 = shared expert when present) as 64-bit words, word j =
+  // (call tag << 32) | two fp16 values at B-fragment positions 2j, 2j + 1.
+  // Each word is one single-copy-atomic store, so a reader that sees this
+  // call's tag in it holds this call's values: the chunk counts that tell
+  // readers when to look need no release fence.
+  unsigned long long* htag;  // [k + 1][I / 2]
   int32_t* topk_idx;    // [T][k]
   float* topk_w;        // [T][k]
   const uint16_t* x;    // bf16 [T][H]

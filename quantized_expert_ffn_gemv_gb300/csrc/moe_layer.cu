@@ -501,7 +501,7 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
                o_h16 = carve(2ull * (P + Tb) * I), o_tki = carve(4ull * Tm * k), o_tkw = carve(4ull * Tm * k),
                o_bar = carve(8ull * Tk * E), o_cnt = carve(8ull * (Um + 2) * (I / 64) * kCntPad), o_pool = carve(4ull * 2 * 3 * E),
                o_hot = carve(4ull * kMaxHotExperts), o_wnorm = carve(4ull * E),
-               o_pub = carve(128);
+               o_pub = carve(128), o_htag = carve(4ull * (k + 1) * I);
   if (cudaMalloc(&L->dev_block, off) != cudaSuccess) {
     L->dev_block = nullptr;
     return fail(MOE_ERR_OUT_OF_MEMORY);
@@ -533,6 +533,7 @@ moe_status_t moe_layer_create(const moe_layer_desc_t* desc, moe_layer_t** out) {
   a.tk_u = (int32_t*)(b + o_tku);
   a.tk_pos = (int32_t*)(b + o_tkpos);
   a.h16 = (__half*)(b + o_h16);
+  a.htag = (unsigned long long*)(b + o_htag);  // zeroed above: tag 0 is never a call's
   a.topk_idx = (int32_t*)(b + o_tki);
   a.topk_w = (float*)(b + o_tkw);
   a.wait_timeout_ns = L->wait_timeout_ns;
