@@ -11,8 +11,8 @@
 //              down strip start loading; x -> fp16 in B-fragment order.
 //   router     compensated (double-float) dot products, four warps per row;
 //              each logit's 52-bit order key is stored with a 12-bit call tag
-//              in one 64-bit word; each CTA then releases one count on the
-//              layer's publication counter, and one lane per CTA waits for
+//              in one 64-bit word; each CTA then adds one relaxed count on
+//              the layer's publication counter, and one lane per CTA waits for
 //              all of them before the block reads the keys once.
 //   routing    every CTA redundantly: each warp ranks its range of experts
 //              (one 64-bit compare orders by logit, then index) and keeps its
@@ -807,12 +807,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       // tag sees this call's key
       st_relaxed_u64(&tagged_logits[(size_t)t * E + e], (unsigned long long)((key << 12) | tag));
     }
-    // one release per CTA once its rows are out: readers wait for all G
-    // releases of this call on one counter (one polling lane per CTA) and
-    // then read every key once, instead of every lane polling its keys'
-    // lines (which slowed some CTAs' loads by microseconds)
+    // one count per CTA once its rows are out: readers wait for all G counts
+    // of this call on one counter (one polling lane per CTA) and then read
+    // every key once, instead of every lane polling its keys' lines (which
+    // slowed some CTAs' loads by microseconds).  The count carries no release
+    // ordering (a fence here cost about 0.5 us per call): it only says when
+    // to read, and a reader that gets ahead of a key sees the previous
+    // call's tag in the word and reads it again.
     __syncthreads();
-    if (tid == 0) red_release_add(a.pub, 1u);  // cumulative over the CTA's stores before the barrier
+    if (tid == 0) red_relaxed_add(a.pub, 1u);
   }
 
   // ---- gate/up of one strip by a group of four warps (K split four ways)
@@ -920,7 +923,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
     // (it only grows; the comparison survives wrap-around)
     const uint32_t want = s_dseq * (uint32_t)G;
     int spins = 0;
-    while ((int32_t)(ld_acquire_gpu_u32(a.pub) - want) < 0) {
+    while ((int32_t)(ld_relaxed_u32(a.pub) - want) < 0) {
       if (((++spins) & 63) == 0 && global_ns() > deadline) {
         set_error(a, MOE_ERR_TIMEOUT);
         break;
