@@ -65,3 +65,34 @@ def test_reference_arm_does_no_work_off_rank_0(monkeypatch, capsys):
     monkeypatch.setenv("LOCAL_RANK", "1")
     assert bench.run_reference(None) is None
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_the_contract_line(monkeypatch, capsys):
+    """Rank 0 of the reference arm prints one JSON line with the keys the
+    driver reads (the oracle on a small layer shape here, so the CPU suite
+    stays fast; the line's shape is the same at page scale)."""
+    import json
+    import types
+    sys.path.insert(0, ROOT)
+    import bench
+    from quantized_expert_ffn_gemv_gb300 import synth
+    sh = synth.SMALL
+    monkeypatch.setattr(synth, "PAGE", sh)
+    monkeypatch.setattr(bench, "H", sh.H)
+    monkeypatch.setattr(bench, "E", sh.E)
+    monkeypatch.setattr(bench, "K", sh.k)
+    monkeypatch.setattr(bench, "I", sh.I)
+    monkeypatch.setattr(bench, "host_cores", lambda: 2)
+    for v in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(v, raising=False)
+    bench.run_reference(types.SimpleNamespace(steps=2, warmup=1))
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["metric"] == bench.METRIC and d["unit"] == bench.UNIT
+    assert d["value"] > 0 and d["n_gpus"] == 1 and d["steps"] == 2 and d["warmup"] == 1
+    assert d["higher_is_better"] is True and d["vs_baseline"] is None
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 2
+    assert d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    assert "workload" in d["config"]
