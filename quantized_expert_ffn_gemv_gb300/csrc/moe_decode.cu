@@ -868,8 +868,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(LayerArgs a, unsign
       if (tagged) {
         // one token (column 0: lanes with t4 = 0 hold rows g and g + 8): rows
         // g, g + 1, g + 8, g + 9 sit at B-fragment positions p .. p + 3 (g
-        // even), written as two tagged words; the down product reads them
-        // with no counter and no release fence
+        // even), written as two tagged words; the relaxed chunk count below
+        // tells the readers when to look, the tags what they may take
         const uint32_t q0 = __half_as_ushort(__float2half_rn(silu(gsum[0]) * usum[0]));
         const uint32_t q2 = __half_as_ushort(__float2half_rn(silu(gsum[2]) * usum[2]));
         const uint32_t q1 = __shfl_down_sync(0xffffffffu, q0, 4), q3 = __shfl_down_sync(0xffffffffu, q2, 4);
