@@ -119,9 +119,31 @@ def _stream_ptr(stream):
     return C.c_void_p(stream.cuda_stream)
 
 
+def _check_tensors(device, items):
+    """Each (name, tensor or None, dtype, shape) must match exactly, be
+    contiguous and live on `device` (a CUDA device); a mismatch raises
+    ValueError before anything reaches the library, so it is never an
+    out-of-bounds device access."""
+    for name, t, dt, shape in items:
+        if t is None:
+            continue
+        if t.dtype != dt or tuple(t.shape) != tuple(shape):
+            raise ValueError(f"{name}: expected {dt} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+        if t.device.type != "cuda" or t.device != device:
+            raise ValueError(f"{name} must be a CUDA tensor on {device}, got {t.device}")
+
+
 def residual_rmsnorm(x, y, eps, x_out, xhat, stream=None):
     """x_out = bf16(x + y); xhat = bf16(rmsnorm(x_out)); torch bf16 CUDA tensors [T, H]."""
+    import torch
+    if x.dim() != 2:
+        raise ValueError("x must be [T, H]")
     T, H = x.shape
+    bf = torch.bfloat16
+    _check_tensors(x.device, [("x", x, bf, (T, H)), ("y", y, bf, (T, H)), ("x_out", x_out, bf, (T, H)),
+                              ("xhat", xhat, bf, (T, H))])
     check(lib().moe_residual_rmsnorm(x.data_ptr(), None if y is None else y.data_ptr(), T, H, eps,
                                      None if x_out is None else x_out.data_ptr(), xhat.data_ptr(),
                                      _stream_ptr(stream)), "moe_residual_rmsnorm")
@@ -197,12 +219,21 @@ class MoeLayer:
         e = np.ascontiguousarray(np.asarray(experts, dtype=np.int32))
         check(lib().moe_slot_pool_seed(self.h, e.ctypes.data if len(e) else None, len(e)), "moe_slot_pool_seed")
 
+    def _check_io(self, T, acts, topk_idx, topk_w):
+        import torch
+        H, k = self.shape.H, self.shape.k
+        _check_tensors(self.device, [(n, t, torch.bfloat16, (T, H)) for n, t in acts] +
+                       [("topk_idx", topk_idx, torch.int32, (T, k)), ("topk_w", topk_w, torch.float32, (T, k))])
+
     def forward(self, x, y=None, topk_idx=None, topk_w=None, stream=None):
         """x: torch bf16 [T, H] on the layer's device; returns y (bf16 [T, H])."""
         import torch
+        if x.dim() != 2:
+            raise ValueError("x must be [T, H]")
         T = x.shape[0]
         if y is None:
             y = torch.empty_like(x)
+        self._check_io(T, [("x", x), ("y", y)], topk_idx, topk_w)
         check(lib().moe_forward(self.h, x.data_ptr(), T, y.data_ptr(),
                                 None if topk_idx is None else topk_idx.data_ptr(),
                                 None if topk_w is None else topk_w.data_ptr(), _stream_ptr(stream)), "moe_forward")
@@ -212,6 +243,10 @@ class MoeLayer:
         """One pre-norm stack layer: x_out = bf16(x + y_prev), xhat = bf16(rmsnorm(x_out)),
         y = MoE(xhat).  torch bf16 [T, H] tensors on the layer's device; y_prev and
         x_out may be None."""
+        if x.dim() != 2:
+            raise ValueError("x must be [T, H]")
+        self._check_io(x.shape[0], [("x", x), ("y_prev", y_prev), ("x_out", x_out), ("xhat", xhat), ("y", y)],
+                       topk_idx, topk_w)
         opt = lambda t: None if t is None else t.data_ptr()
         check(lib().moe_forward_norm(self.h, x.data_ptr(), opt(y_prev), x.shape[0], eps, opt(x_out),
                                      xhat.data_ptr(), y.data_ptr(), opt(topk_idx), opt(topk_w),

@@ -143,3 +143,42 @@ def test_binding_fails_loudly_without_the_library(moe, monkeypatch, tmp_path):
         moe.lib()
     with pytest.raises(RuntimeError, match="not built"):
         moe.expert_bytes(2048, 512)
+
+
+def test_binding_checks_forward_tensors_before_the_library(moe, monkeypatch):
+    """Shapes, dtypes, layouts and devices of forward / forward_norm /
+    residual_rmsnorm are checked in the binding: a mismatch raises ValueError
+    and never reaches the library (which here would fail the test)."""
+    import torch
+
+    def no_library():
+        raise AssertionError("the library was called")
+
+    monkeypatch.setattr(moe, "lib", no_library)
+    sh = synth.SMALL
+    layer = moe.MoeLayer.__new__(moe.MoeLayer)
+    layer.shape, layer.device, layer.h = sh, torch.device("cuda", 0), None
+    T, H, k = 3, sh.H, sh.k
+    bf = torch.bfloat16
+    x = torch.zeros(T, H, dtype=bf)
+    good = dict(x=x, y=torch.zeros(T, H, dtype=bf), topk_idx=torch.zeros(T, k, dtype=torch.int32),
+                topk_w=torch.zeros(T, k, dtype=torch.float32))
+    bad = [
+        dict(good, y=torch.zeros(T - 1, H, dtype=bf)),                          # y too short
+        dict(good, y=torch.zeros(T, H, dtype=torch.float16)),                   # wrong dtype
+        dict(good, topk_idx=torch.zeros(T, k + 1, dtype=torch.int32)),          # wrong k
+        dict(good, topk_w=torch.zeros(T, k, dtype=torch.float64)),              # wrong dtype
+        dict(good, x=torch.zeros(H, T, dtype=bf).t()),                          # not contiguous
+        dict(good, x=torch.zeros(T, H + 8, dtype=bf), y=torch.zeros(T, H + 8, dtype=bf)),  # wrong H
+        good,                                                                   # host tensors
+    ]
+    for kw in bad:
+        with pytest.raises(ValueError):
+            layer.forward(**kw)
+        with pytest.raises(ValueError):
+            layer.forward_norm(kw["x"], None, 1e-6, None, kw["y"], torch.zeros_like(kw["y"]), kw["topk_idx"],
+                               kw["topk_w"])
+    with pytest.raises(ValueError):
+        moe.residual_rmsnorm(x, torch.zeros(T, H + 8, dtype=bf), 1e-6, None, torch.zeros_like(x))
+    with pytest.raises(ValueError):
+        moe.residual_rmsnorm(x, None, 1e-6, None, torch.zeros_like(x))  # host tensors
